@@ -1,0 +1,533 @@
+#!/usr/bin/env python3
+"""Benchmark of the SGMV multi-LoRA hot path on GB300.
+
+One step = one pass of the whole path over one batch: group the batch's rows
+by adapter on the device (sgmv_build_segments_device), then the fused
+shrink+expand (sgmv_apply) with the row permutation -- both through the C ABI.
+The llama7b-stack workload groups once and applies all 224 projections.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the fp64 oracle on the host cores
+
+Prints one JSON line (rank 0).  `value` is rows/s with inputs resident in HBM;
+inputs are rotated over enough copies that one pass over them exceeds twice
+the L2 cache, and the K timed steps run as CUDA-graph replays.  `e2e` is the
+same metric with each step's inputs copied from pinned host memory and its
+result read back.  With N > 1 (torchrun) every rank runs an independent
+replica: the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGMV shrink+expand rows/s and achieved HBM GB/s (% of GB300 roofline)"
+UNIT = "rows/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="decode-distinct",
+                   choices=["tiny", "decode-distinct", "decode-shared", "decode-zipf", "prefill",
+                            "llama7b-stack"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="host-core budget of the oracle baseline sample")
+    p.add_argument("--soak-seconds", type=float, default=1.0,
+                   help="load before the timed region while clocks are sampled")
+    p.add_argument("--latency-iters", type=int, default=50)
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip e2e, cpu baseline and latency (for profiling runs)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def config_of(name, w, n_copies=None, l2_note=None):
+    cfg = {"workload": name, "T": w.T, "L": w.L, "H1": w.H1, "H2": w.H2, "r": w.r,
+           "inputs": str(w.dtype).replace("torch.", ""),
+           "y": str(w.y_dtype).replace("torch.", ""),
+           "segments": int(len(set(w.row_adapter.tolist()))), "parallelism": "replicas"}
+    if l2_note:
+        cfg["l2"] = l2_note
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(dev):
+    import torch
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    return str(dev.index or 0)
+
+
+# ------------------------------------------------------- our implementation
+class Batch:
+    """Device copy of one batch plus its metadata buffers."""
+
+    def __init__(self, w, dev, sgmv):
+        import torch
+
+        self.w = w
+        self.X = w.X.to(dev)
+        self.A = w.A.to(dev)
+        self.B = w.B.to(dev)
+        self.Y = w.Y0.to(dev).clone()
+        self.ra = w.row_adapter.to(dev)
+        self.smax = sgmv.sgmv_max_segments(w.T, w.L)
+        self.meta = (torch.empty(max(w.T, 1), dtype=torch.int32, device=dev),
+                     torch.empty(self.smax + 1, dtype=torch.int32, device=dev),
+                     torch.empty(max(self.smax, 1), dtype=torch.int32, device=dev),
+                     torch.empty(1, dtype=torch.int32, device=dev))
+
+    def group(self, sgmv):
+        sgmv.sgmv_build_segments_device(self.ra, self.w.L, out=self.meta)
+
+    def apply(self, sgmv):
+        perm, seg_ptr, idx, _ = self.meta
+        sgmv.sgmv_apply(self.Y, self.X, self.A, self.B, seg_ptr, idx, self.w.scale, perm=perm,
+                        S=self.smax)
+
+    def step(self, sgmv):
+        self.group(sgmv)
+        self.apply(sgmv)
+
+
+class StackBatch:
+    """All 224 projections of the llama7b-stack workload, resident on the device."""
+
+    def __init__(self, seed, dev, sgmv):
+        import torch
+        from rank_gemv_gb300 import workloads as wl
+
+        self.T, self.L, self.r = 128, 128, 16
+        self.projs = []
+        for layer in range(wl.LLAMA7B_LAYERS):
+            for p in range(len(wl.LLAMA7B_PROJ)):
+                X, A, B, Y0 = wl.stack_projection(seed, layer, p, device=dev)
+                self.projs.append((X, A, B, Y0))
+        self.ra = wl.stack_row_adapter(self.T).to(dev)
+        self.smax = sgmv.sgmv_max_segments(self.T, self.L)
+        self.meta = (torch.empty(self.T, dtype=torch.int32, device=dev),
+                     torch.empty(self.smax + 1, dtype=torch.int32, device=dev),
+                     torch.empty(self.smax, dtype=torch.int32, device=dev),
+                     torch.empty(1, dtype=torch.int32, device=dev))
+
+    def group(self, sgmv):
+        sgmv.sgmv_build_segments_device(self.ra, self.L, out=self.meta)
+
+    def apply(self, sgmv):
+        perm, seg_ptr, idx, _ = self.meta
+        for X, A, B, Y in self.projs:
+            sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
+
+    def step(self, sgmv):
+        self.group(sgmv)
+        self.apply(sgmv)
+
+    def bytes_moved(self):
+        from rank_gemv_gb300 import workloads as wl
+
+        tot = 0
+        for _, H1, H2 in wl.LLAMA7B_PROJ:
+            tot += self.L * (H1 * self.r + self.r * H2) * 2 + self.T * H1 * 2 + 2 * self.T * H2 * 2
+        return tot * wl.LLAMA7B_LAYERS
+
+
+def capture(fns):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for fn in fns:
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def timed_replays(graph_full, n_per_graph, graph_rem, K):
+    import torch
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(K // n_per_graph):
+        graph_full.replay()
+    if graph_rem is not None:
+        graph_rem.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    from rank_gemv_gb300 import build as _build
+    from rank_gemv_gb300 import sgmv
+    from rank_gemv_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sgmv.load_library()
+    K, W = args.steps, max(3, args.warmup)
+    seed = args.seed + rank
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+
+    if args.workload == "llama7b-stack":
+        stack = StackBatch(seed, dev, sgmv)
+        batches = [stack]
+        T = stack.T
+        bytes_step = stack.bytes_moved()
+        launches_step = 1 + len(stack.projs)
+        w0 = None
+        l2_note = f"inputs {bytes_step / 1e9:.1f} GB per step, larger than L2 ({l2 / 1e6:.0f} MB)"
+    else:
+        w0 = wl.make(args.workload, seed)
+        T = w0.T
+        bytes_step = w0.bytes_moved()
+        per_copy = (w0.X.nbytes + w0.A.nbytes + w0.B.nbytes + 2 * w0.Y0.nbytes)
+        n_copies = max(2, -(-2 * l2 // per_copy))
+        batches = [Batch(w0, dev, sgmv) for _ in range(n_copies)]
+        launches_step = 2
+        l2_note = (f"rotating {n_copies} input copies, {n_copies * per_copy / 1e6:.0f} MB per "
+                   f"rotation > 2 x L2 ({l2 / 1e6:.0f} MB)")
+
+    if world > 1:
+        dist.barrier()
+
+    # warm-up (eager), then the graphs of one rotation and of the remainder
+    for i in range(W):
+        batches[i % len(batches)].step(sgmv)
+    torch.cuda.synchronize()
+    assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during warm-up"
+    n = len(batches)
+    g_full = capture([(lambda b=b: b.step(sgmv)) for b in batches])
+    g_rem = capture([(lambda b=b: b.step(sgmv)) for b in batches[: K % n]]) if K % n else None
+    # kernel-only graphs (metadata already built) for the dominant kernel's duration
+    for b in batches:
+        b.group(sgmv)
+    k_full = capture([(lambda b=b: b.apply(sgmv)) for b in batches])
+    k_rem = capture([(lambda b=b: b.apply(sgmv)) for b in batches[: K % n]]) if K % n else None
+
+    # soak under the clock sampler, then the timed steps
+    sampler = ClockSampler(gpu_id_for(dev))
+    t_end = time.perf_counter() + args.soak_seconds
+    while time.perf_counter() < t_end:
+        g_full.replay()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed = timed_replays(g_full, n, g_rem, K)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    kernel_s = timed_replays(k_full, n, k_rem, K)
+    assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during timing"
+
+    if world > 1:
+        t = torch.tensor([elapsed, kernel_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed, kernel_s = float(t[0]), float(t[1])
+
+    value = world * K * T / elapsed
+    peak, peak_kind = measured_peak()
+    kernel_launch_s = kernel_s / (K * (launches_step - 1))
+    bytes_launch = bytes_step / (launches_step - 1)
+    achieved = bytes_launch / kernel_launch_s / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(args.workload, w0, l2_note=l2_note) if w0 is not None else {
+            "workload": "llama7b-stack", "T": T, "L": 128, "r": 16, "layers": 32,
+            "projections": 7, "inputs": "float16", "y": "float16", "segments": 128,
+            "parallelism": "replicas", "l2": l2_note},
+        "hbm_gbs": bytes_step * K / elapsed / 1e9,
+        "bytes_per_step": bytes_step,
+        "roofline": {"bound": "hbm", "kernel": "sgmv_cc_kernel (fused shrink+expand)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": bytes_launch,
+                     "launch_us": kernel_launch_s * 1e6},
+        "gpu_launches": K * launches_step,
+        "clocks": clocks,
+    }
+    if args.workload == "decode-distinct" and not args.no_extras:
+        out["latency_us"] = distinct_vs_shared(args, dev, sgmv, wl)
+    if not args.no_extras:
+        out["e2e"] = e2e(args, dev, sgmv, wl, world, seed, K, W)
+    if rank == 0 and world == 1 and not args.no_extras:
+        out["cpu_baseline"] = cpu_baseline(args, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def distinct_vs_shared(args, dev, sgmv, wl):
+    """Median latency of one step with L2 flushed before it, for the batch of
+    32 distinct adapters and for the same batch on one shared adapter."""
+    import torch
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for name in ("decode-distinct", "decode-shared"):
+        b = Batch(wl.make(name, args.seed), dev, sgmv)
+        for _ in range(5):
+            b.step(sgmv)
+        ts = []
+        for i in range(args.latency_iters):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            b.step(sgmv)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        res[name] = statistics.median(ts)
+    return {"distinct": res["decode-distinct"], "shared": res["decode-shared"],
+            "ratio": res["decode-distinct"] / res["decode-shared"],
+            "method": f"median of {args.latency_iters}, L2 flushed (256 MB write) before each"}
+
+
+def e2e(args, dev, sgmv, wl, world, seed, K, W):
+    """The metric through the public API with host buffers: per step, copy the
+    batch's rows, row->adapter ids and Y from pinned memory, group + apply,
+    copy Y back and wait for it on the host."""
+    import torch
+
+    if args.workload == "llama7b-stack":
+        # inputs per step: the 224 projections' X and Y rows and the ids
+        stack = StackBatch(seed, dev, sgmv)
+        hx = [X.cpu().pin_memory() for X, _, _, _ in stack.projs]
+        hy = [Y.cpu().pin_memory() for _, _, _, Y in stack.projs]
+        hout = [torch.empty_like(h).pin_memory() for h in hy]
+        hra = stack.ra.cpu().pin_memory()
+
+        def one():
+            stack.ra.copy_(hra, non_blocking=True)
+            for (X, _, _, Y), a, b in zip(stack.projs, hx, hy):
+                X.copy_(a, non_blocking=True)
+                Y.copy_(b, non_blocking=True)
+            stack.step(sgmv)
+            for (_, _, _, Y), o in zip(stack.projs, hout):
+                o.copy_(Y, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        h2d = sum(h.nbytes for h in hx) + sum(h.nbytes for h in hy) + hra.nbytes
+        d2h = sum(h.nbytes for h in hout)
+        T = stack.T
+        K = min(K, 20)
+    else:
+        w = wl.make(args.workload, seed)
+        b = Batch(w, dev, sgmv)
+        hx, hy, hra = w.X.pin_memory(), w.Y0.pin_memory(), w.row_adapter.pin_memory()
+        hout = torch.empty_like(hy).pin_memory()
+
+        def one():
+            b.X.copy_(hx, non_blocking=True)
+            b.Y.copy_(hy, non_blocking=True)
+            b.ra.copy_(hra, non_blocking=True)
+            b.step(sgmv)
+            hout.copy_(b.Y, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        h2d, d2h, T = hx.nbytes + hy.nbytes + hra.nbytes, hout.nbytes, w.T
+    for _ in range(W):
+        one()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    el = e0.elapsed_time(e1) / 1e3
+    return {"value": world * K * T / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3}
+
+
+# -------------------------------------------------- oracle (host cores)
+def _oracle_sample(name, seed):
+    """(step function, rows per step, rows/s scale, sample description) for the
+    oracle on a bounded sample of the workload."""
+    import oracle
+    from rank_gemv_gb300 import workloads as wl
+
+    if name == "llama7b-stack":
+        rows = 16
+        projs = [wl.stack_projection(seed, 0, p) for p in range(len(wl.LLAMA7B_PROJ))]
+        ra = wl.stack_row_adapter(128)[:rows]
+        widened = [tuple(oracle.widen(t[:rows] if i in (0, 3) else t) for i, t in enumerate(pr))
+                   for pr in projs]
+
+        def step():
+            perm, seg_ptr, idx = oracle.build_segments(ra, 128)
+            for X, A, B, Y in widened:
+                oracle.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, widened=True)
+
+        # one layer of 7 projections stands for 1/32 of a pass
+        return step, rows / 32.0, f"{rows} of 128 rows, layer 0 (7 of 224 projections)"
+    w = wl.make(name, seed)
+    per_row = w.H1 * w.r + w.r * w.H2
+    rows = int(max(1, min(w.T, 20e6 // per_row)))
+    X, A, B, Y = (oracle.widen(w.X[:rows]), oracle.widen(w.A), oracle.widen(w.B),
+                  oracle.widen(w.Y0[:rows]))
+    ra = w.row_adapter[:rows]
+
+    def step():
+        perm, seg_ptr, idx = oracle.build_segments(ra, w.L)
+        oracle.sgmv_apply(Y, X, A, B, seg_ptr, idx, w.scale, perm=perm, widened=True)
+
+    desc = "whole batch" if rows == w.T else f"first {rows} of {w.T} rows"
+    return step, float(rows), desc
+
+
+def cpu_baseline(args, budget_s):
+    step, rows, desc = _oracle_sample(args.workload, args.seed)
+    step()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": n * rows / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{desc}; {n} oracle passes (grouping + fp64 apply, one thread) "
+                      f"in {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from rank_gemv_gb300 import workloads as wl
+
+    step, rows, desc = _oracle_sample(args.workload, args.seed)
+    W = max(3, args.warmup)
+    for _ in range(W):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * rows / el
+    w = None if args.workload == "llama7b-stack" else wl.make(args.workload, args.seed)
+    cfg = config_of(args.workload, w) if w is not None else {"workload": "llama7b-stack"}
+    sample = f"{desc}; one oracle pass (grouping + fp64 apply, one thread) per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": W, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

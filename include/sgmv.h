@@ -1,0 +1,196 @@
+/*
+ * sgmv.h -- C ABI of libsgmv.so, Punica's SGMV multi-LoRA hot path on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * SGMV (Segmented Gather Matrix-Vector multiplication) adds each request's
+ * LoRA delta to its rows of a batch in which contiguous row segments use
+ * different adapters:
+ *
+ *     Y[row(p), :] += scale * (X[row(p), :] . A[idx[s]]) . B[idx[s]]
+ *         for every sorted position p in segment s = [seg_ptr[s], seg_ptr[s+1])
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [Article] "Punica: when LoRA fine-tuned models need multi-tenant serving"
+ *             (omica.com.cn):
+ *               §2.1 the LoRA part of a layer is x.A.B, A [H1, r], B [r, H2];
+ *               §2.2 SGMV = a segmented gather of A_i out of one stack of all
+ *                    adapters with v_i = x_i.A_i ("shrink"), then v_i.B_i with
+ *                    all B_i stacked the same way ("expand");
+ *               §5.1 the batch builder groups requests by LoRA id;
+ *               §5.2 a wrong rank or shape shows up as illegal memory access.
+ *   [Review]  "Punica: Multi-Tenant LoRA Serving" (nubint.ai review),
+ *             "Proposed method": the kernel works on segmented inputs and
+ *             outputs so that different LoRA models share one batch.
+ *   [Q&A]     "How to deploy several LoRA adapters without reloading the base
+ *             model (Punica, S-LoRA)?" (aivaro.ru):
+ *               §3.1 each request computes x = x + (x @ A) @ B;
+ *               §3.2 adapter weights sit in one contiguous buffer and the
+ *                    kernel selects them by index (segmented gather/scatter);
+ *                    the kernel accepts any rank r without recompiling.
+ *
+ * Layouts (all row-major, all tensors in device memory unless stated):
+ *   x  [T][H1]    f16 or bf16           batch input rows
+ *   A  [L][H1][r] same type as x        stacked adapter "A" matrices
+ *   B  [L][r][H2] same type as x        stacked adapter "B" matrices
+ *   y  [T][H2]    f16, bf16 or f32      output rows, updated in place
+ *   v  [T][r]     f32                   shrink result, by sorted position
+ *   perm    int32 [T] or NULL           physical row of sorted position p;
+ *                                       NULL means position p is row p
+ *   seg_ptr int32 [S+1]                 segment bounds in sorted positions,
+ *                                       non-decreasing, inside [0, T]
+ *   idx     int32 [S]                   adapter of each segment, in [-1, L);
+ *                                       -1 = no adapter (rows left unchanged)
+ * Empty segments are allowed; adjacent segments may share an adapter; rows
+ * outside [seg_ptr[0], seg_ptr[S]) are neither read nor written.  perm must
+ * be one-to-one on the covered positions.
+ *
+ * Requirements checked on the host (status returned, nothing launched):
+ *   pointers non-NULL where used and 16-byte aligned; H1 and H2 multiples of
+ *   8 and >= 8; 1 <= r <= 128; T >= 0; L >= 1; dtypes as above.  seg_ptr_host,
+ *   when given, is checked for bounds and order.
+ * Checked on the device (the bad segment or row is skipped and the sticky
+ * device error word is set; read it with sgmv_get_device_error):
+ *   idx outside [-1, L) -> SGMV_ERR_BAD_INDEX; a segment outside [0, T] or
+ *   with end < start -> SGMV_ERR_BAD_SEGMENTS; perm entry outside [0, T) ->
+ *   SGMV_ERR_BAD_INDEX.  No kernel traps or asserts; every wait in a kernel is
+ *   bounded and reports SGMV_ERR_TIMEOUT if it runs out.
+ *
+ * Ownership and execution: the caller owns every buffer; the library never
+ * allocates device memory.  Calls are asynchronous on `stream` (a
+ * cudaStream_t, NULL = legacy default stream), take no locks and keep no
+ * state except the device error word.  Kernels are launched with
+ * programmatic dependent launch: a kernel may start while the previous
+ * kernel on the stream finishes, and before it waits for that kernel it
+ * reads only A, B, row_adapter and the segment metadata.  So those inputs must
+ * not be written by the SGMV kernel launched just before on the same stream
+ * (x and y may be: they are read only after the wait).
+ */
+#ifndef SGMV_H
+#define SGMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGMV_OK = 0,
+    SGMV_ERR_INVALID_ARG = 1,   /* NULL pointer, size out of range, bad dtype */
+    SGMV_ERR_UNSUPPORTED = 2,   /* valid but outside what this build handles */
+    SGMV_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned, H1/H2 % 8 != 0 */
+    SGMV_ERR_BAD_INDEX = 4,     /* adapter id or perm entry out of range */
+    SGMV_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    SGMV_ERR_WORKSPACE = 6,     /* workspace smaller than sgmv_workspace_bytes */
+    SGMV_ERR_TIMEOUT = 7,       /* a bounded wait inside a kernel ran out */
+    SGMV_ERR_BAD_SEGMENTS = 8   /* seg_ptr out of [0, T] or decreasing */
+} sgmv_status;
+
+typedef enum {
+    SGMV_F16 = 0,
+    SGMV_BF16 = 1,
+    SGMV_F32 = 2                /* output y only */
+} sgmv_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *sgmv_status_string(int status);
+
+/* Detail of the last SGMV_ERR_CUDA returned on the calling thread (which CUDA
+ * call failed and its error string); empty if none.  Thread-local storage
+ * owned by the library, valid until the thread's next failing call. */
+const char *sgmv_last_error_string(void);
+
+/* Upper bound on the number of segments that grouping T rows over L adapters
+ * (ids -1..L-1) can produce: min(T, L + 1).  Size seg_ptr (bound + 1) and idx
+ * (bound) with it for sgmv_build_segments_device. */
+int32_t sgmv_max_segments(int32_t T, int32_t L);
+
+/*
+ * Group a batch's rows by adapter id, on the host ([Article] §5.1; [Review]
+ * "Proposed method").  Stable: ascending id with -1 first, original row order
+ * within an id, one segment per id that occurs.
+ *   row_adapter  host int32 [T], ids in [-1, L)
+ *   perm         host int32 [T]      out: physical row of each sorted position
+ *   seg_ptr      host int32 [T + 1]  out: S + 1 entries used
+ *   idx          host int32 [T]      out: S entries used
+ *   S            host int32 [1]      out: number of segments
+ * Returns SGMV_ERR_BAD_INDEX if an id is out of range (outputs undefined).
+ */
+int sgmv_build_segments(const int32_t *row_adapter, int32_t T, int32_t L,
+                        int32_t *perm, int32_t *seg_ptr, int32_t *idx,
+                        int32_t *S);
+
+/*
+ * The same grouping on the device, one small kernel, no host synchronisation.
+ * All pointers are device pointers.  seg_ptr must hold
+ * sgmv_max_segments(T, L) + 1 entries and idx sgmv_max_segments(T, L): past
+ * the real segment count the kernel writes empty segments (seg_ptr = T,
+ * idx = -1), so the arrays can be passed to the SGMV calls with
+ * S = sgmv_max_segments(T, L).  *S receives the real count.  An id out of
+ * range is grouped as -1 and sets SGMV_ERR_BAD_INDEX in the device error
+ * word.  Requires L <= 32767.
+ */
+int sgmv_build_segments_device(const int32_t *row_adapter, int32_t T, int32_t L,
+                               int32_t *perm, int32_t *seg_ptr, int32_t *idx,
+                               int32_t *S, void *stream);
+
+/*
+ * Bytes of device workspace that lets sgmv_apply use its tensor-core path for
+ * long segments.  sgmv_apply also accepts workspace == NULL with
+ * workspace_bytes == 0 and then runs every segment on the CUDA-core path.
+ */
+size_t sgmv_workspace_bytes(int32_t T, int32_t H1, int32_t H2, int32_t r);
+
+/*
+ * Shrink, the first SGMV step ([Article] §2.2):
+ *   v[p][k] = sum_h x[row(p)][h] * A[idx[s]][h][k]    (fp32 accumulation)
+ * v rows of segments with idx = -1 are set to 0; other rows of v are not
+ * written.  seg_ptr_host (host int32 [S+1] copy of seg_ptr, or NULL) lets the
+ * host size the launch exactly; without it the launch is sized by a bound.
+ */
+int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype,
+                const int32_t *perm, const int32_t *seg_ptr, const int32_t *idx,
+                int32_t S, const int32_t *seg_ptr_host, int32_t T, int32_t L,
+                int32_t H1, int32_t r, void *stream);
+
+/*
+ * Expand, the second SGMV step ([Article] §2.2), accumulated into y
+ * ([Q&A] §3.1):
+ *   y[row(p)][j] = round(y[row(p)][j] + scale * sum_k v[p][k] * B[idx[s]][k][j])
+ * computed in fp32 and rounded once (to nearest even) to y's type.
+ */
+int sgmv_expand(void *y, int y_dtype, const float *v, const void *B, int in_dtype,
+                float scale, const int32_t *perm, const int32_t *seg_ptr,
+                const int32_t *idx, int32_t S, const int32_t *seg_ptr_host,
+                int32_t T, int32_t L, int32_t H2, int32_t r, void *stream);
+
+/*
+ * Shrink and expand in one call: y += scale * (x . A[idx]) . B[idx] per
+ * segment, with v kept on chip (never written to device memory) on the
+ * CUDA-core path.  Segments of at least 64 rows use the tensor-core path when
+ * a workspace of sgmv_workspace_bytes() is given (it holds v for those rows).
+ * Result equals sgmv_shrink followed by sgmv_expand up to fp32 summation
+ * order.
+ */
+int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B,
+               int in_dtype, float scale, const int32_t *perm,
+               const int32_t *seg_ptr, const int32_t *idx, int32_t S,
+               const int32_t *seg_ptr_host, int32_t T, int32_t L, int32_t H1,
+               int32_t H2, int32_t r, void *workspace, size_t workspace_bytes,
+               void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's sticky
+ * error word.  Returns SGMV_OK if no kernel reported an error since the last
+ * read, else the first status code reported (SGMV_ERR_BAD_INDEX,
+ * SGMV_ERR_BAD_SEGMENTS or SGMV_ERR_TIMEOUT), or SGMV_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int sgmv_get_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGMV_H */

@@ -1,0 +1,384 @@
+// sgmv_api.cu -- the C ABI declared in include/sgmv.h: argument checks,
+// launch-shape choice and dispatch, host-side grouping, device error word.
+#include <algorithm>
+#include <climits>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "sgmv.h"
+#include "sgmv_internal.h"
+
+// Sticky device error word of this library (first reported status wins).
+__device__ int g_sgmv_error;
+
+namespace {
+
+using namespace sgmv;
+
+thread_local char g_last_error[256] = "";
+
+void note(const char *what, cudaError_t e) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int cuda_status(const char *what, int e) {
+    if (e == (int)cudaSuccess) return SGMV_OK;
+    note(what, (cudaError_t)e);
+    return SGMV_ERR_CUDA;
+}
+
+// Device address of the error word of the current device, looked up once per
+// device with that device current.
+int *error_word() {
+    static std::mutex mu;
+    static int *cache[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_sgmv_error);
+        if (e != cudaSuccess) {
+            note("cudaGetSymbolAddress(error word)", e);
+            return nullptr;
+        }
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int round8(int64_t v) { return (int)((v + 7) / 8 * 8); }
+int floor8(int64_t v) { return (int)(v / 8 * 8); }
+int floor16(int64_t v) { return (int)(v / 16 * 16); }
+int elem_size(int dt) { return dt == SGMV_F32 ? 4 : 2; }
+int rmax_of(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : r <= 64 ? 64 : 128; }
+
+int check_common(int32_t T, int32_t L, int32_t r, int32_t S, const int32_t *seg_ptr,
+                 const int32_t *idx, const int32_t *seg_ptr_host, int in_dtype) {
+    if (T < 0 || L < 1 || S < 0 || r < 1) return SGMV_ERR_INVALID_ARG;
+    if (r > 128) return SGMV_ERR_UNSUPPORTED;
+    if (in_dtype != SGMV_F16 && in_dtype != SGMV_BF16) return SGMV_ERR_INVALID_ARG;
+    if (S > 0 && (!seg_ptr || !idx)) return SGMV_ERR_INVALID_ARG;
+    if (seg_ptr_host) {
+        for (int32_t s = 0; s <= S; ++s)
+            if (seg_ptr_host[s] < 0 || seg_ptr_host[s] > T) return SGMV_ERR_BAD_SEGMENTS;
+        for (int32_t s = 0; s < S; ++s)
+            if (seg_ptr_host[s + 1] < seg_ptr_host[s]) return SGMV_ERR_BAD_SEGMENTS;
+    }
+    return SGMV_OK;
+}
+
+int check_dim(int32_t H) {
+    if (H < 1) return SGMV_ERR_INVALID_ARG;
+    if (H % 8 != 0) return SGMV_ERR_ALIGNMENT;
+    return SGMV_OK;
+}
+
+// Longest segment (host copy known) or -1.
+int32_t longest(const int32_t *sp, int32_t S) {
+    if (!sp) return -1;
+    int32_t m = 0;
+    for (int32_t s = 0; s < S; ++s) m = std::max(m, sp[s + 1] - sp[s]);
+    return m;
+}
+
+// Tile slots for segments of length in [min_len, max_len], `rows` rows per
+// tile: exact from the host copy of seg_ptr, else a bound that holds for any
+// segmentation of T positions into S segments.
+int64_t tile_slots(int32_t T, int32_t S, const int32_t *sp, int rows, int min_len, int max_len) {
+    if (sp) {
+        int64_t n = 0;
+        for (int32_t s = 0; s < S; ++s) {
+            const int32_t len = sp[s + 1] - sp[s];
+            if (len > 0 && len >= min_len && len <= max_len) n += ceil_div(len, rows);
+        }
+        return n;
+    }
+    return ((int64_t)T + (int64_t)S * (rows - 1)) / rows;
+}
+
+int cc_launch(int in_dtype, const CCLaunch &l) {
+    return in_dtype == SGMV_F16 ? cc_launch_f16(l) : cc_launch_bf16(l);
+}
+
+// CTAs per cluster for the shrink side: largest of 8/4/2/1 that leaves every
+// CTA at least 64 columns of H1 (and of H2 when it also expands).
+int choose_cluster(int32_t H1, int32_t H2) {
+    int cl = 8;
+    while (cl > 1 && (H1 < cl * 64 || (H2 > 0 && H2 < cl * 64))) cl >>= 1;
+    return cl;
+}
+
+void stage_sizes(CCParams &p, int mode, int elem) {
+    if (mode != kExpand) {
+        // A multiple of 16 columns keeps the h -> thread assignment of the
+        // shrink independent of the chunking, so every row's v is bitwise the
+        // same whatever the tile shape.
+        p.hs = std::min(p.hc, floor16(kStageBytes / ((int64_t)(p.r + p.rows) * elem)));
+        p.ax_stages = ceil_div(p.hc, p.hs) > 1 ? 2 : 1;
+    } else {
+        p.hs = 8;
+        p.ax_stages = 1;
+    }
+    if (mode != kShrink) {
+        p.js = std::min(p.jc, floor8(kStageBytes / ((int64_t)p.r * elem)));
+        p.b_stages = ceil_div(p.jc, p.js) > 1 ? 2 : 1;
+    } else {
+        p.js = 8;
+        p.b_stages = 1;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sgmv_status_string(int status) {
+    switch (status) {
+        case SGMV_OK: return "SGMV_OK";
+        case SGMV_ERR_INVALID_ARG: return "SGMV_ERR_INVALID_ARG";
+        case SGMV_ERR_UNSUPPORTED: return "SGMV_ERR_UNSUPPORTED";
+        case SGMV_ERR_ALIGNMENT: return "SGMV_ERR_ALIGNMENT";
+        case SGMV_ERR_BAD_INDEX: return "SGMV_ERR_BAD_INDEX";
+        case SGMV_ERR_CUDA: return "SGMV_ERR_CUDA";
+        case SGMV_ERR_WORKSPACE: return "SGMV_ERR_WORKSPACE";
+        case SGMV_ERR_TIMEOUT: return "SGMV_ERR_TIMEOUT";
+        case SGMV_ERR_BAD_SEGMENTS: return "SGMV_ERR_BAD_SEGMENTS";
+        default: return "SGMV_ERR_UNKNOWN";
+    }
+}
+
+const char *sgmv_last_error_string(void) { return g_last_error; }
+
+int32_t sgmv_max_segments(int32_t T, int32_t L) {
+    if (T <= 0 || L < 0) return 0;
+    return (int32_t)std::min<int64_t>(T, (int64_t)L + 1);
+}
+
+int sgmv_build_segments(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
+                        int32_t *seg_ptr, int32_t *idx, int32_t *S) {
+    if (T < 0 || L < 1 || !seg_ptr || !S) return SGMV_ERR_INVALID_ARG;
+    if (T > 0 && (!row_adapter || !perm || !idx)) return SGMV_ERR_INVALID_ARG;
+    for (int32_t t = 0; t < T; ++t)
+        if (row_adapter[t] < -1 || row_adapter[t] >= L) return SGMV_ERR_BAD_INDEX;
+    // Counting sort on key = id + 1: counts, then start positions.
+    std::vector<int32_t> start((size_t)L + 1, 0);
+    for (int32_t t = 0; t < T; ++t) ++start[(size_t)row_adapter[t] + 1];
+    int32_t pos = 0, s = 0;
+    for (int32_t b = 0; b <= L; ++b) {
+        const int32_t c = start[b];
+        if (c > 0) {
+            seg_ptr[s] = pos;
+            idx[s] = b - 1;
+            ++s;
+        }
+        start[b] = pos;
+        pos += c;
+    }
+    seg_ptr[s] = T;
+    for (int32_t t = 0; t < T; ++t) perm[start[(size_t)row_adapter[t] + 1]++] = t;
+    *S = s;
+    return SGMV_OK;
+}
+
+int sgmv_build_segments_device(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
+                               int32_t *seg_ptr, int32_t *idx, int32_t *S, void *stream) {
+    if (T < 0 || L < 1 || !seg_ptr || !S) return SGMV_ERR_INVALID_ARG;
+    if (T > 0 && (!row_adapter || !perm || !idx)) return SGMV_ERR_INVALID_ARG;
+    if (L > 32767) return SGMV_ERR_UNSUPPORTED;
+    int *err = error_word();
+    if (!err) return SGMV_ERR_CUDA;
+    return cuda_status("build_segments kernel",
+                       build_segments_launch(row_adapter, T, L, perm, seg_ptr, idx, S,
+                                             sgmv_max_segments(T, L), err,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+size_t sgmv_workspace_bytes(int32_t T, int32_t H1, int32_t H2, int32_t r) {
+    (void)H1;
+    (void)H2;
+    if (T <= 0 || r <= 0) return 0;
+    return (size_t)T * (size_t)r * 4u + 256u;
+}
+
+int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype, const int32_t *perm,
+                const int32_t *seg_ptr, const int32_t *idx, int32_t S, const int32_t *seg_ptr_host,
+                int32_t T, int32_t L, int32_t H1, int32_t r, void *stream) {
+    int st = check_common(T, L, r, S, seg_ptr, idx, seg_ptr_host, in_dtype);
+    if (st != SGMV_OK) return st;
+    if ((st = check_dim(H1)) != SGMV_OK) return st;
+    if (T == 0 || S == 0) return SGMV_OK;
+    if (!v || !x || !A) return SGMV_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(x) || !aligned16(A)) return SGMV_ERR_ALIGNMENT;
+
+    CCLaunch l = {};
+    CCParams &p = l.p;
+    p.x = x;
+    p.A = A;
+    p.v_out = v;
+    p.perm = perm;
+    p.seg_ptr = seg_ptr;
+    p.idx = idx;
+    p.S = S;
+    p.T = T;
+    p.L = L;
+    p.H1 = H1;
+    p.H2 = 8;
+    p.r = r;
+    const int32_t mx = longest(seg_ptr_host, S);
+    p.rows = mx > 0 ? std::min(kRowsMax, mx) : kRowsMax;
+    p.min_len = 1;
+    p.max_len = INT_MAX;
+    p.scale = 0.f;
+    const int cl = choose_cluster(H1, 0);
+    p.hc = round8(ceil_div(H1, cl));
+    p.jc = 8;
+    stage_sizes(p, kShrink, elem_size(in_dtype));
+    const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
+    if (slots == 0) return SGMV_OK;
+    if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
+    if (!(p.err = error_word())) return SGMV_ERR_CUDA;
+    l.mode = kShrink;
+    l.y_dtype = SGMV_F32;
+    l.rmax = rmax_of(r);
+    l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
+    l.cluster = cl;
+    p.cl = cl;
+    l.stream = static_cast<cudaStream_t>(stream);
+    l.pdl = true;
+    return cuda_status("shrink kernel", cc_launch(in_dtype, l));
+}
+
+int sgmv_expand(void *y, int y_dtype, const float *v, const void *B, int in_dtype, float scale,
+                const int32_t *perm, const int32_t *seg_ptr, const int32_t *idx, int32_t S,
+                const int32_t *seg_ptr_host, int32_t T, int32_t L, int32_t H2, int32_t r,
+                void *stream) {
+    int st = check_common(T, L, r, S, seg_ptr, idx, seg_ptr_host, in_dtype);
+    if (st != SGMV_OK) return st;
+    if ((st = check_dim(H2)) != SGMV_OK) return st;
+    if (y_dtype != SGMV_F16 && y_dtype != SGMV_BF16 && y_dtype != SGMV_F32)
+        return SGMV_ERR_INVALID_ARG;
+    if (T == 0 || S == 0) return SGMV_OK;
+    if (!y || !v || !B) return SGMV_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(v) || !aligned16(B)) return SGMV_ERR_ALIGNMENT;
+
+    CCLaunch l = {};
+    CCParams &p = l.p;
+    p.y = y;
+    p.B = B;
+    p.v_in = v;
+    p.perm = perm;
+    p.seg_ptr = seg_ptr;
+    p.idx = idx;
+    p.S = S;
+    p.T = T;
+    p.L = L;
+    p.H1 = 8;
+    p.H2 = H2;
+    p.r = r;
+    const int32_t mx = longest(seg_ptr_host, S);
+    p.rows = mx > 0 ? std::min(kRowsMax, mx) : kRowsMax;
+    p.min_len = 1;
+    p.max_len = INT_MAX;
+    p.scale = scale;
+    const int nx = (int)std::max<int64_t>(1, ceil_div(H2, 512));
+    p.jc = round8(ceil_div(H2, nx));
+    p.hc = 8;
+    stage_sizes(p, kExpand, elem_size(in_dtype));
+    const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
+    if (slots == 0) return SGMV_OK;
+    if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
+    if (!(p.err = error_word())) return SGMV_ERR_CUDA;
+    l.mode = kExpand;
+    l.y_dtype = y_dtype;
+    l.rmax = rmax_of(r);
+    l.grid = dim3((unsigned)ceil_div(H2, p.jc), (unsigned)slots, 1);
+    l.cluster = 1;
+    p.cl = 1;
+    l.stream = static_cast<cudaStream_t>(stream);
+    l.pdl = true;
+    return cuda_status("expand kernel", cc_launch(in_dtype, l));
+}
+
+int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B, int in_dtype,
+               float scale, const int32_t *perm, const int32_t *seg_ptr, const int32_t *idx,
+               int32_t S, const int32_t *seg_ptr_host, int32_t T, int32_t L, int32_t H1,
+               int32_t H2, int32_t r, void *workspace, size_t workspace_bytes, void *stream) {
+    int st = check_common(T, L, r, S, seg_ptr, idx, seg_ptr_host, in_dtype);
+    if (st != SGMV_OK) return st;
+    if ((st = check_dim(H1)) != SGMV_OK) return st;
+    if ((st = check_dim(H2)) != SGMV_OK) return st;
+    if (y_dtype != SGMV_F16 && y_dtype != SGMV_BF16 && y_dtype != SGMV_F32)
+        return SGMV_ERR_INVALID_ARG;
+    if (workspace && workspace_bytes < sgmv_workspace_bytes(T, H1, H2, r)) return SGMV_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return SGMV_ERR_ALIGNMENT;
+    if (T == 0 || S == 0) return SGMV_OK;
+    if (!y || !x || !A || !B) return SGMV_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(A) || !aligned16(B))
+        return SGMV_ERR_ALIGNMENT;
+
+    CCLaunch l = {};
+    CCParams &p = l.p;
+    p.y = y;
+    p.x = x;
+    p.A = A;
+    p.B = B;
+    p.perm = perm;
+    p.seg_ptr = seg_ptr;
+    p.idx = idx;
+    p.S = S;
+    p.T = T;
+    p.L = L;
+    p.H1 = H1;
+    p.H2 = H2;
+    p.r = r;
+    const int32_t mx = longest(seg_ptr_host, S);
+    p.rows = mx > 0 ? std::min(kRowsMax, mx) : kRowsMax;
+    p.min_len = 1;
+    p.max_len = INT_MAX;
+    p.scale = scale;
+    const int cl = choose_cluster(H1, H2);
+    p.hc = round8(ceil_div(H1, cl));
+    p.jc = round8(ceil_div(H2, cl));
+    stage_sizes(p, kFused, elem_size(in_dtype));
+    const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
+    if (slots == 0) return SGMV_OK;
+    if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
+    if (!(p.err = error_word())) return SGMV_ERR_CUDA;
+    l.mode = kFused;
+    l.y_dtype = y_dtype;
+    l.rmax = rmax_of(r);
+    l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
+    l.cluster = cl;
+    p.cl = cl;
+    l.stream = static_cast<cudaStream_t>(stream);
+    l.pdl = true;
+    return cuda_status("fused kernel", cc_launch(in_dtype, l));
+}
+
+int sgmv_get_device_error(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        note("cudaStreamSynchronize", e);
+        return SGMV_ERR_CUDA;
+    }
+    int v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_sgmv_error, sizeof(int))) != cudaSuccess) {
+        note("read error word", e);
+        return SGMV_ERR_CUDA;
+    }
+    if (v != 0) {
+        const int zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_sgmv_error, &zero, sizeof(int))) != cudaSuccess) {
+            note("clear error word", e);
+            return SGMV_ERR_CUDA;
+        }
+    }
+    return v;
+}
+
+}  // extern "C"

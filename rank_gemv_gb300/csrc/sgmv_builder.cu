@@ -1,0 +1,158 @@
+// sgmv_builder.cu -- device kernel that groups a batch's rows by adapter id.
+//
+// The batch builder groups requests by LoRA id ("Punica: when LoRA
+// fine-tuned models need multi-tenant serving", omica.com.cn article, §5.1)
+// and SGMV runs over the resulting contiguous segments ("Punica: Multi-Tenant
+// LoRA Serving", nubint.ai review, "Proposed method").  Here the grouping is
+// a stable counting sort on the GPU: ascending id with -1 (no adapter) first,
+// original row order inside an id.
+//
+// One CTA of 1024 threads:
+//   1. histogram of ids in shared memory (bin b holds id b-1);
+//   2. block scan of the bins: start position of each id and segment number
+//      of each id that occurs;
+//   3. griddepcontrol.wait -- the outputs may still be read by the SGMV kernel
+//      launched before on the stream -- then write seg_ptr / idx and pad them
+//      with empty segments up to S_max;
+//   4. stable scatter of row numbers into perm by one warp, 32 rows per step,
+//      ranking equal ids inside a step with __match_any_sync.
+// The kernel never triggers its dependents early, so the next kernel on the
+// stream starts only after the metadata is complete.
+#include "sgmv_device.cuh"
+#include "sgmv_internal.h"
+
+namespace sgmv {
+
+constexpr int kBuilderThreads = 1024;
+
+__global__ void __launch_bounds__(kBuilderThreads)
+    build_segments_kernel(const int32_t *__restrict__ ra, int32_t T, int32_t L,
+                          int32_t *__restrict__ perm, int32_t *__restrict__ seg_ptr,
+                          int32_t *__restrict__ idx, int32_t *__restrict__ S_out, int32_t S_max,
+                          int *err) {
+    extern __shared__ int cnt[];  // L + 1 bins
+    __shared__ int w_c[32], w_n[32];
+    __shared__ int s_total;
+    const int nb = L + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+
+    for (int b = tid; b < nb; b += blockDim.x) cnt[b] = 0;
+    __syncthreads();
+    for (int t = tid; t < T; t += blockDim.x) {
+        int key = ra[t] + 1;
+        if (key < 0 || key > L) {
+            set_error(err, kErrBadIndex);
+            key = 0;
+        }
+        atomicAdd(&cnt[key], 1);
+    }
+    __syncthreads();
+
+    // Each thread owns a contiguous run of bins.
+    const int per = (nb + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
+    int c_own = 0, n_own = 0;
+    for (int b = b0; b < b1; ++b) {
+        c_own += cnt[b];
+        n_own += cnt[b] > 0;
+    }
+    int c_in = c_own, n_in = n_own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int c = __shfl_up_sync(0xffffffffu, c_in, off);
+        const int n = __shfl_up_sync(0xffffffffu, n_in, off);
+        if (lane >= off) {
+            c_in += c;
+            n_in += n;
+        }
+    }
+    if (lane == 31) {
+        w_c[warp] = c_in;
+        w_n[warp] = n_in;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int c = lane < nwarps ? w_c[lane] : 0;
+        const int n = lane < nwarps ? w_n[lane] : 0;
+        int ci = c, ni = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int cc = __shfl_up_sync(0xffffffffu, ci, off);
+            const int nn = __shfl_up_sync(0xffffffffu, ni, off);
+            if (lane >= off) {
+                ci += cc;
+                ni += nn;
+            }
+        }
+        w_c[lane] = ci - c;
+        w_n[lane] = ni - n;
+        if (lane == 31) s_total = ni;
+    }
+    __syncthreads();
+    int pos = w_c[warp] + c_in - c_own;  // first sorted position of this thread's bins
+    int sid = w_n[warp] + n_in - n_own;  // segment number of its first non-empty bin
+    const int S = s_total;
+
+    pdl_wait();
+
+    for (int b = b0; b < b1; ++b) {
+        const int c = cnt[b];
+        if (c > 0) {
+            seg_ptr[sid] = pos;
+            idx[sid] = b - 1;
+            ++sid;
+        }
+        cnt[b] = pos;  // from here on: next free position of the bin
+        pos += c;
+    }
+    if (tid == 0) {
+        seg_ptr[S] = T;
+        *S_out = S;
+    }
+    for (int s = S + tid; s < S_max; s += blockDim.x) {
+        idx[s] = -1;
+        seg_ptr[s + 1] = T;
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        for (int base = 0; base < T; base += 32) {
+            const int t = base + lane;
+            int key = -1;  // lanes past T get a key no real row has
+            if (t < T) {
+                key = ra[t] + 1;
+                if (key < 0 || key > L) key = 0;
+            }
+            const unsigned grp = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(grp & ((1u << lane) - 1u));
+            if (t < T) perm[cnt[key] + rank] = t;
+            __syncwarp();
+            if (t < T && rank == 0) cnt[key] += __popc(grp);
+            __syncwarp();
+        }
+    }
+}
+
+int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
+                          int32_t *seg_ptr, int32_t *idx, int32_t *S, int32_t S_max, int *err,
+                          cudaStream_t stream) {
+    const size_t smem = (size_t)(L + 1) * sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(build_segments_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kBuilderThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&cfg, build_segments_kernel, row_adapter, T, L, perm, seg_ptr,
+                                   idx, S, S_max, err);
+}
+
+}  // namespace sgmv

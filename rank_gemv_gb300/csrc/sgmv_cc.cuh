@@ -1,0 +1,408 @@
+// sgmv_cc.cuh -- CUDA-core SGMV kernels for decode-sized segments.
+//
+// Method ("Punica: when LoRA fine-tuned models need multi-tenant serving",
+// omica.com.cn article, §2.2): for every row of a segment, shrink
+// v = x . A[idx] (A gathered out of the stacked adapters), then expand
+// y += scale * v . B[idx].  Both steps stream one adapter's weights and do
+// about one flop per byte, so they are bound by HBM bandwidth and run on the
+// CUDA cores; the tensor-core path takes long segments.
+//
+// Work decomposition (one launch, no device-memory intermediate in kFused):
+//   * a tile is up to kRowsMax consecutive rows of one segment; tiles are
+//     numbered on the device from seg_ptr (grid.y = tile slot), so the same
+//     kernel serves metadata built on the host or on the device;
+//   * the CL CTAs of one tile form a thread-block cluster; CTA c owns the
+//     H1 slice [c*hc, (c+1)*hc) for the shrink and the H2 slice [c*jc, ...)
+//     for the expand;
+//   * each CTA issues 1-D bulk (TMA) copies of its A slice (one contiguous
+//     block), its B slice (r rows) and the tile's X rows into shared memory,
+//     all at kernel start, so the whole working set is in flight at once;
+//   * partial v from the CTA's H1 slice is summed over the cluster through
+//     distributed shared memory in a fixed order (deterministic, identical in
+//     every CTA), then each CTA expands its H2 slice and updates y in place.
+// Programmatic dependent launch: A, B and the segment metadata are requested
+// before griddepcontrol.wait; x, y and v only after it.
+#pragma once
+
+#include "sgmv_device.cuh"
+#include "sgmv_internal.h"
+
+namespace sgmv {
+
+// Warp 0 finds the tile with number `tile` among the segments that this launch
+// handles.  out = {segment or -1, first position, rows, adapter}.  With
+// `report`, the warp scans every segment and records malformed ones in the
+// error word (one CTA per launch reports).
+__device__ __forceinline__ void find_tile(const CCParams &P, int tile, bool with_no_adapter,
+                                          bool report, int *out) {
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    int f_s = -1, f_p0 = 0, f_n = 0, f_a = -1;
+    for (int s0 = 0; s0 < P.S; s0 += 32) {
+        const int s = s0 + lane;
+        int n = 0, b = 0, e = 0, a = -1;
+        if (s < P.S) {
+            b = P.seg_ptr[s];
+            e = P.seg_ptr[s + 1];
+            a = P.idx[s];
+            const bool seg_ok = b >= 0 && e >= b && e <= P.T;
+            const bool idx_ok = a >= -1 && a < P.L;
+            if (report && !seg_ok) set_error(P.err, kErrBadSegments);
+            if (report && seg_ok && !idx_ok) set_error(P.err, kErrBadIndex);
+            const int len = e - b;
+            if (seg_ok && idx_ok && len > 0 && (a >= 0 || with_no_adapter) && len >= P.min_len &&
+                len <= P.max_len)
+                n = (len + P.rows - 1) / P.rows;
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const int excl = incl - n;
+        const bool mine = f_s < 0 && n > 0 && tile >= base + excl && tile < base + incl;
+        const unsigned m = __ballot_sync(0xffffffffu, mine);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            int p0 = 0, nr = 0;
+            if (lane == src) {
+                p0 = b + (tile - base - excl) * P.rows;
+                nr = min(P.rows, e - p0);
+            }
+            f_s = __shfl_sync(0xffffffffu, s, src);
+            f_p0 = __shfl_sync(0xffffffffu, p0, src);
+            f_n = __shfl_sync(0xffffffffu, nr, src);
+            f_a = __shfl_sync(0xffffffffu, a, src);
+            if (!report) break;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        out[0] = f_s;
+        out[1] = f_p0;
+        out[2] = f_n;
+        out[3] = f_a;
+    }
+}
+
+template <typename Tin, typename Ty, int RMAX, int MODE>
+__global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant__ CCParams P) {
+    extern __shared__ __align__(128) uint8_t dsmem[];
+    constexpr int WG = RMAX >= 32 ? RMAX : 32;  // threads sharing one warp-group of k values
+    constexpr int NWG = kThreads / WG;
+    constexpr int G = kThreads / RMAX;          // h-groups in the shrink
+    __shared__ __align__(8) uint64_t bars[4];   // 0,1: (A,X) stages; 2,3: B stages
+    __shared__ int s_info[4];
+    __shared__ int s_row[kRowsMax];
+    __shared__ __align__(16) float s_vpart[kRowsMax * RMAX];
+    __shared__ __align__(16) float s_v[kRowsMax * RMAX];
+    __shared__ float s_red[(MODE == kExpand) ? 1 : NWG * kRowsMax * RMAX];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const bool report = blockIdx.x == 0 && blockIdx.y == 0;
+
+    if (tid < 32) find_tile(P, blockIdx.y, MODE == kShrink, report, s_info);
+    __syncthreads();
+    if (s_info[0] < 0) return;  // no tile for this slot (same for the whole cluster)
+    const int p0 = s_info[1];
+    const int nrows = s_info[2];
+    const int a = s_info[3];
+
+    // Physical rows of the tile; invalid perm entries are skipped and reported.
+    if (tid < nrows) {
+        const int p = p0 + tid;
+        int row = P.perm ? P.perm[p] : p;
+        if (row < 0 || row >= P.T) {
+            set_error(P.err, kErrBadIndex);
+            row = -1;
+        }
+        s_row[tid] = row;
+    }
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (MODE == kShrink && a < 0) {  // no adapter: v = 0 for these rows
+        pdl_wait();
+        pdl_trigger();
+        if (blockIdx.x == 0)
+            for (int e = tid; e < nrows * P.r; e += kThreads)
+                P.v_out[(size_t)(p0 + e / P.r) * P.r + e % P.r] = 0.f;
+        return;
+    }
+
+    unsigned vmask = 0;  // tile rows with a valid physical row
+    int nvalid = 0;
+#pragma unroll
+    for (int t = 0; t < kRowsMax; ++t)
+        if (t < nrows && s_row[t] >= 0) {
+            vmask |= 1u << t;
+            ++nvalid;
+        }
+
+    const CCSmem lay = cc_smem_layout(P, (int)sizeof(Tin), MODE);
+    const Tin *gA = static_cast<const Tin *>(P.A);
+    const Tin *gB = static_cast<const Tin *>(P.B);
+    const Tin *gX = static_cast<const Tin *>(P.x);
+
+    // Slices owned by this CTA.
+    int h0 = 0, h1 = 0, j0 = 0, j1 = 0;
+    if (MODE != kExpand) {
+        h0 = min(P.H1, (int)blockIdx.x * P.hc);
+        h1 = min(P.H1, h0 + P.hc);
+    }
+    if (MODE != kShrink) {
+        j0 = min(P.H2, (int)blockIdx.x * P.jc);
+        j1 = min(P.H2, j0 + P.jc);
+    }
+    const int nA = (MODE != kExpand && h1 > h0) ? (h1 - h0 + P.hs - 1) / P.hs : 0;
+    const int nB = (MODE != kShrink && j1 > j0) ? (j1 - j0 + P.js - 1) / P.js : 0;
+
+    auto ax_buf = [&](int st) {
+        return reinterpret_cast<Tin *>(dsmem + lay.ax_off + st * lay.ax_stage_bytes);
+    };
+    auto b_buf = [&](int st) {
+        return reinterpret_cast<Tin *>(dsmem + lay.b_off + st * lay.b_stage_bytes);
+    };
+    // Chunk i of A (and its byte count in the expectation, X added by issue_x).
+    auto issue_a = [&](int i) {  // lane 0 of warp 0
+        const int st = i % P.ax_stages;
+        const int hlo = h0 + i * P.hs;
+        const int hn = min(P.hs, h1 - hlo);
+        const uint32_t ab = (uint32_t)(hn * P.r) * sizeof(Tin);
+        const uint32_t xb = (uint32_t)(nvalid * hn) * sizeof(Tin);
+        mbar_arrive_expect_tx(&bars[st], ab + xb);
+        bulk_g2s(ax_buf(st), gA + ((size_t)a * P.H1 + hlo) * P.r, ab, &bars[st]);
+    };
+    auto issue_x = [&](int i) {  // lanes of warp 0, one row each
+        const int st = i % P.ax_stages;
+        const int hlo = h0 + i * P.hs;
+        const int hn = min(P.hs, h1 - hlo);
+        Tin *xs = ax_buf(st) + P.hs * P.r;
+        if (lane < nrows && s_row[lane] >= 0)
+            bulk_g2s(xs + lane * P.hs, gX + (size_t)s_row[lane] * P.H1 + hlo,
+                     (uint32_t)hn * sizeof(Tin), &bars[st]);
+    };
+    auto issue_b = [&](int i) {  // all lanes of warp 0
+        const int st = i % P.b_stages;
+        const int jlo = j0 + i * P.js;
+        const int jn = min(P.js, j1 - jlo);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[2 + st], (uint32_t)(P.r * jn) * sizeof(Tin));
+        __syncwarp();
+        for (int k = lane; k < P.r; k += 32)
+            bulk_g2s(b_buf(st) + k * P.js, gB + ((size_t)a * P.r + k) * P.H2 + jlo,
+                     (uint32_t)jn * sizeof(Tin), &bars[2 + st]);
+    };
+
+    // Weights first: they do not depend on the previous kernel on the stream.
+    if (tid < 32) {
+        if (lane == 0)
+            for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_a(i);
+        for (int i = 0; i < min(nB, P.b_stages); ++i) issue_b(i);
+    }
+    pdl_wait();
+    if (tid < 32) {
+        __syncwarp();
+        for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_x(i);
+    }
+    pdl_trigger();
+
+    bool lost = false;  // a bounded wait ran out: write nothing
+    if (MODE == kExpand) {
+        for (int e = tid; e < nrows * P.r; e += kThreads) {
+            const int t = e / P.r, k = e - (e / P.r) * P.r;
+            s_v[t * RMAX + k] = P.v_in[(size_t)(p0 + t) * P.r + k];
+        }
+    } else {
+        // ---- shrink: partial v over this CTA's H1 slice -----------------
+        float acc[kRowsMax];
+#pragma unroll
+        for (int t = 0; t < kRowsMax; ++t) acc[t] = 0.f;
+        const int k = tid % RMAX;
+        const int g = tid / RMAX;
+        for (int i = 0; i < nA; ++i) {
+            const int st = i % P.ax_stages;
+            const uint32_t par = (uint32_t)((i / P.ax_stages) & 1);
+            if (!mbar_wait(&bars[st], par)) {
+                lost = true;
+                set_error(P.err, kErrTimeout);
+                mbar_wait(&bars[st], par);
+            }
+            const int hn = min(P.hs, h1 - (h0 + i * P.hs));
+            const Tin *As = ax_buf(st);
+            const Tin *Xs = As + P.hs * P.r;
+            if (k < P.r) {
+                for (int h = g; h < hn; h += G) {
+                    const float av = to_f<Tin>(As[h * P.r + k]);
+#pragma unroll
+                    for (int t = 0; t < kRowsMax; ++t)
+                        if (vmask & (1u << t)) acc[t] = fmaf(to_f<Tin>(Xs[t * P.hs + h]), av, acc[t]);
+                }
+            }
+            __syncthreads();
+            if (tid < 32 && i + P.ax_stages < nA) {
+                if (lane == 0) issue_a(i + P.ax_stages);
+                __syncwarp();
+                issue_x(i + P.ax_stages);
+            }
+        }
+        // groups holding the same k inside one warp sit RMAX lanes apart
+        if (RMAX < 32) {
+#pragma unroll
+            for (int off = RMAX; off < 32; off <<= 1)
+#pragma unroll
+                for (int t = 0; t < kRowsMax; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+        }
+        if ((tid % WG) < RMAX) {
+            const int wg = tid / WG;
+#pragma unroll
+            for (int t = 0; t < kRowsMax; ++t)
+                if (t < nrows) s_red[(wg * kRowsMax + t) * RMAX + k] = acc[t];
+        }
+        __syncthreads();
+        for (int e = tid; e < nrows * RMAX; e += kThreads) {
+            const int t = e / RMAX, kk = e % RMAX;
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < NWG; ++w) s += s_red[(w * kRowsMax + t) * RMAX + kk];
+            s_vpart[t * RMAX + kk] = s;
+        }
+        // ---- sum the partials of the cluster's CTAs, in rank order ------
+        if (P.cl > 1) {
+            cluster_sync();
+            for (int e = tid; e < nrows * P.r; e += kThreads) {
+                const int t = e / P.r, kk = e - (e / P.r) * P.r;
+                float s = 0.f;
+                for (int c = 0; c < P.cl; ++c)
+                    s += ld_peer(peer_addr(&s_vpart[t * RMAX + kk], (uint32_t)c));
+                s_v[t * RMAX + kk] = s;
+            }
+            cluster_sync();  // peers are done reading this CTA's partials
+        } else {
+            __syncthreads();
+            for (int e = tid; e < nrows * P.r; e += kThreads) {
+                const int t = e / P.r, kk = e - (e / P.r) * P.r;
+                s_v[t * RMAX + kk] = s_vpart[t * RMAX + kk];
+            }
+        }
+        if (MODE == kShrink) {
+            if (blockIdx.x == 0 && !lost)
+                for (int e = tid; e < nrows * P.r; e += kThreads) {
+                    const int t = e / P.r, kk = e - (e / P.r) * P.r;
+                    P.v_out[(size_t)(p0 + t) * P.r + kk] = s_v[t * RMAX + kk];
+                }
+            return;
+        }
+    }
+    __syncthreads();
+
+    // ---- expand: y[row, j] += scale * v . B[a][:, j] for this CTA's slice ----
+    Ty *gY = static_cast<Ty *>(P.y);
+    for (int i = 0; i < nB; ++i) {
+        const int st = i % P.b_stages;
+        const uint32_t par = (uint32_t)((i / P.b_stages) & 1);
+        if (!mbar_wait(&bars[2 + st], par)) {
+            lost = true;
+            set_error(P.err, kErrTimeout);
+            mbar_wait(&bars[2 + st], par);
+        }
+        const int jlo = j0 + i * P.js;
+        const int ncv = min(P.js, j1 - jlo) >> 3;
+        const Tin *Bs = b_buf(st);
+        if (!lost) {
+            for (int w = tid; w < nrows * ncv; w += kThreads) {
+                const int t = w / ncv;
+                const int cv = w - t * ncv;
+                const int row = s_row[t];
+                if (row < 0) continue;
+                float acc8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc8[q] = 0.f;
+                const float *vt = s_v + t * RMAX;
+#pragma unroll 8
+                for (int kk = 0; kk < P.r; ++kk) {
+                    const float vk = vt[kk];
+                    float bf[8];
+                    unpack8<Tin>(*reinterpret_cast<const uint4 *>(Bs + kk * P.js + cv * 8), bf);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc8[q] = fmaf(vk, bf[q], acc8[q]);
+                }
+                Ty *yp = gY + (size_t)row * P.H2 + jlo + cv * 8;
+                float yv[8];
+                load8<Ty>(yp, yv);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) yv[q] = fmaf(P.scale, acc8[q], yv[q]);
+                store8<Ty>(yp, yv);
+            }
+        }
+        __syncthreads();
+        if (tid < 32 && i + P.b_stages < nB) issue_b(i + P.b_stages);
+    }
+}
+
+// ---- host-side launcher for one input type ----------------------------------
+template <typename Tin, typename Ty, int RMAX>
+static void *pick_mode(int mode) {
+    switch (mode) {
+        case kFused: return (void *)sgmv_cc_kernel<Tin, Ty, RMAX, kFused>;
+        case kExpand: return (void *)sgmv_cc_kernel<Tin, Ty, RMAX, kExpand>;
+        default: return (void *)sgmv_cc_kernel<Tin, float, RMAX, kShrink>;
+    }
+}
+
+template <typename Tin, typename Ty>
+static void *pick_rmax(int mode, int rmax) {
+    switch (rmax) {
+        case 16: return pick_mode<Tin, Ty, 16>(mode);
+        case 32: return pick_mode<Tin, Ty, 32>(mode);
+        case 64: return pick_mode<Tin, Ty, 64>(mode);
+        default: return pick_mode<Tin, Ty, 128>(mode);
+    }
+}
+
+template <typename Tin>
+static int cc_launch_impl(const CCLaunch &l) {
+    void *fn;
+    switch (l.y_dtype) {
+        case 0: fn = pick_rmax<Tin, __half>(l.mode, l.rmax); break;
+        case 1: fn = pick_rmax<Tin, __nv_bfloat16>(l.mode, l.rmax); break;
+        default: fn = pick_rmax<Tin, float>(l.mode, l.rmax); break;
+    }
+    const CCSmem lay = cc_smem_layout(l.p, (int)sizeof(Tin), l.mode);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);
+    if (e != cudaSuccess) return (int)e;
+    if (l.cluster > 8) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return (int)e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = l.grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = lay.total;
+    cfg.stream = l.stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (l.cluster > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)l.cluster;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (l.pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    void *args[] = {(void *)&l.p};
+    return (int)cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace sgmv

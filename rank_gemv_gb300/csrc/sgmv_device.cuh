@@ -1,0 +1,158 @@
+// sgmv_device.cuh -- device helpers shared by the SGMV kernels: inline PTX for
+// mbarriers, 1-D bulk (TMA) copies, thread-block clusters and distributed
+// shared memory, and programmatic dependent launch; plus f16/bf16/f32 loads,
+// stores and conversions.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sgmv {
+
+// Status codes written into the device error word (same values as sgmv.h).
+constexpr int kErrBadIndex = 4;
+constexpr int kErrTimeout = 7;
+constexpr int kErrBadSegments = 8;
+
+// Bound on mbarrier polls before a wait is declared lost.  Each try_wait may
+// suspend the thread for a while, so this is on the order of a second.
+constexpr uint32_t kMaxPolls = 1u << 20;
+
+__device__ __forceinline__ void set_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---- programmatic dependent launch -------------------------------------
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+// Makes barrier initialisation visible to the async (TMA) proxy and the cluster.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Arrive (count 1) and add `bytes` to the expected transaction count.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for phase `parity` to complete.  Returns false if it did not.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kMaxPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// ---- 1-D bulk copy global -> shared, completes on an mbarrier --------------
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---- clusters / distributed shared memory ---------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// Full cluster barrier: every thread of every CTA in the cluster arrives;
+// release/acquire orders shared-memory writes before it with reads after it.
+// The non-.aligned forms are used so that warps need not be converged here.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_peer(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ---- element conversions ---------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+
+// Eight consecutive 16-bit values (one 16-byte vector) widened to fp32.
+template <typename T> __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
+    const T *h = reinterpret_cast<const T *>(&u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) f[q] = to_f<T>(h[q]);
+}
+
+// Read 8 consecutive output elements at p (16 B for 16-bit types, 32 B for f32).
+template <typename Ty> __device__ __forceinline__ void load8(const Ty *p, float (&f)[8]) {
+    uint4 u = *reinterpret_cast<const uint4 *>(p);
+    unpack8<Ty>(u, f);
+}
+template <> __device__ __forceinline__ void load8<float>(const float *p, float (&f)[8]) {
+    float4 a = reinterpret_cast<const float4 *>(p)[0];
+    float4 b = reinterpret_cast<const float4 *>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+template <typename Ty> __device__ __forceinline__ void store8(Ty *p, const float (&f)[8]) {
+    uint4 u;
+    Ty *h = reinterpret_cast<Ty *>(&u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = from_f<Ty>(f[q]);
+    *reinterpret_cast<uint4 *>(p) = u;
+}
+template <> __device__ __forceinline__ void store8<float>(float *p, const float (&f)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+}  // namespace sgmv

@@ -1,0 +1,86 @@
+// sgmv_internal.h -- parameters shared by the C-ABI host code and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sgmv {
+
+// Which part of SGMV a CUDA-core launch runs.
+enum Mode : int {
+    kFused = 0,   // shrink + expand, v kept in shared memory of a cluster
+    kShrink = 1,  // shrink only, v written to device memory
+    kExpand = 2,  // expand only, v read from device memory
+};
+
+constexpr int kThreads = 256;   // threads per CTA of the CUDA-core kernels
+constexpr int kRowsMax = 8;     // rows of one segment handled by one tile
+constexpr int kStageBytes = 32768;  // bytes of one staged chunk (A+X or B)
+
+// One CUDA-core launch.  Grid: x = slice of H1 (and H2) owned by one CTA, or
+// of H2 alone in kExpand; y = tile slot.  A tile is up to `rows` consecutive
+// sorted positions of one segment.  In kFused / kShrink the CTAs along x form
+// one thread-block cluster and reduce their partial v through distributed
+// shared memory.
+struct CCParams {
+    void *y;
+    const void *x;
+    const void *A;
+    const void *B;
+    const float *v_in;   // kExpand: v [T][r]
+    float *v_out;        // kShrink: v [T][r]
+    const int32_t *perm;
+    const int32_t *seg_ptr;
+    const int32_t *idx;
+    int *err;            // sticky device error word
+    int32_t S, T, L, H1, H2, r;
+    int32_t rows;        // rows per tile, 1..kRowsMax
+    int32_t hc, jc;      // columns of H1 / H2 owned by one CTA (multiples of 8)
+    int32_t hs, js;      // columns staged in shared memory at once (multiples of 8)
+    int32_t ax_stages;   // 1 or 2 buffers for (A, X) chunks
+    int32_t b_stages;    // 1 or 2 buffers for B chunks
+    int32_t cl;          // CTAs per cluster along x (1 = no cluster)
+    int32_t min_len;     // only segments with min_len <= length <= max_len
+    int32_t max_len;
+    float scale;
+};
+
+struct CCSmem {
+    uint32_t ax_stage_bytes, b_stage_bytes, ax_off, b_off, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// Dynamic shared memory of a CUDA-core launch; identical on host and device.
+__host__ __device__ inline CCSmem cc_smem_layout(const CCParams &p, int elem, int mode) {
+    CCSmem s;
+    const bool ax = mode != kExpand, b = mode != kShrink;
+    s.ax_stage_bytes = ax ? align_up((uint32_t)(p.hs * p.r + p.rows * p.hs) * elem, 128) : 0;
+    s.b_stage_bytes = b ? align_up((uint32_t)(p.r * p.js) * elem, 128) : 0;
+    s.ax_off = 0;
+    s.b_off = ax ? s.ax_stage_bytes * p.ax_stages : 0;
+    s.total = s.b_off + (b ? s.b_stage_bytes * p.b_stages : 0);
+    return s;
+}
+
+struct CCLaunch {
+    CCParams p;
+    int mode;
+    int y_dtype;   // SGMV_F16 / SGMV_BF16 / SGMV_F32
+    int rmax;      // 16, 32, 64 or 128: compile-time bound on r
+    dim3 grid;
+    int cluster;   // CTAs per cluster along x (1 = plain launch)
+    cudaStream_t stream;
+    bool pdl;
+};
+
+// Launch one CUDA-core kernel; returns a cudaError_t value.
+int cc_launch_f16(const CCLaunch &l);
+int cc_launch_bf16(const CCLaunch &l);
+
+// Launch the device grouping kernel; returns a cudaError_t value.
+int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
+                          int32_t *seg_ptr, int32_t *idx, int32_t *S, int32_t S_max, int *err,
+                          cudaStream_t stream);
+
+}  // namespace sgmv

@@ -1,0 +1,198 @@
+"""Thin ctypes binding of libsgmv.so (C ABI in include/sgmv.h).
+
+Argument marshalling only: every step of SGMV runs in the library's CUDA
+kernels.  Tensors are torch tensors (PyTorch provides device memory and the
+current stream); each function passes their data pointers, sizes and
+``torch.cuda.current_stream()`` to the C function of the same name and raises
+:class:`SgmvError` on a non-zero status.  If the library has not been built
+(``__graft_entry__.build()`` or ``python -m rank_gemv_gb300.build``), loading
+it raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+LIB_PATH = Path(__file__).resolve().parent / "libsgmv.so"
+
+SGMV_F16, SGMV_BF16, SGMV_F32 = 0, 1, 2
+_DTYPES = {torch.float16: SGMV_F16, torch.bfloat16: SGMV_BF16, torch.float32: SGMV_F32}
+
+STATUS = {0: "SGMV_OK", 1: "SGMV_ERR_INVALID_ARG", 2: "SGMV_ERR_UNSUPPORTED",
+          3: "SGMV_ERR_ALIGNMENT", 4: "SGMV_ERR_BAD_INDEX", 5: "SGMV_ERR_CUDA",
+          6: "SGMV_ERR_WORKSPACE", 7: "SGMV_ERR_TIMEOUT", 8: "SGMV_ERR_BAD_SEGMENTS"}
+
+# Every function include/sgmv.h declares, with its ctypes signature.
+_vp, _i32, _i32p = ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)
+_int, _f32, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "sgmv_status_string": (ctypes.c_char_p, [_int]),
+    "sgmv_last_error_string": (ctypes.c_char_p, []),
+    "sgmv_max_segments": (_i32, [_i32, _i32]),
+    "sgmv_build_segments": (_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "sgmv_build_segments_device": (_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "sgmv_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "sgmv_shrink": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                           _i32, _vp]),
+    "sgmv_expand": (_int, [_vp, _int, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp, _i32,
+                           _i32, _i32, _i32, _vp]),
+    "sgmv_apply": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp, _i32,
+                          _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "sgmv_get_device_error": (_int, [_vp]),
+}
+
+_lib = None
+
+
+class SgmvError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
+
+
+def load_library(path: str | Path | None = None) -> ctypes.CDLL:
+    """Load libsgmv.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path is not None else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"{p} is not built: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(str(p))
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        detail = ""
+        if rc == 5:
+            detail = (load_library().sgmv_last_error_string() or b"").decode()
+        raise SgmvError(rc, where, detail)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _meta(t, name):
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous int32 tensor")
+    return t
+
+
+def _host_i32(a):
+    if a is None:
+        return None
+    t = torch.as_tensor(a, dtype=torch.int32, device="cpu").contiguous()
+    return t
+
+
+def sgmv_status_string(status: int) -> str:
+    return load_library().sgmv_status_string(status).decode()
+
+
+def sgmv_max_segments(T: int, L: int) -> int:
+    return int(load_library().sgmv_max_segments(T, L))
+
+
+def sgmv_workspace_bytes(T: int, H1: int, H2: int, r: int) -> int:
+    return int(load_library().sgmv_workspace_bytes(T, H1, H2, r))
+
+
+def sgmv_build_segments(row_adapter, L: int):
+    """Host grouping -> (perm, seg_ptr, idx) as CPU int32 tensors."""
+    ra = _host_i32(row_adapter).reshape(-1)
+    T = ra.numel()
+    perm = torch.empty(max(T, 1), dtype=torch.int32)
+    seg_ptr = torch.empty(T + 1, dtype=torch.int32)
+    idx = torch.empty(max(T, 1), dtype=torch.int32)
+    S = ctypes.c_int32(0)
+    _check(load_library().sgmv_build_segments(ra.data_ptr(), T, L, perm.data_ptr(),
+                                              seg_ptr.data_ptr(), idx.data_ptr(),
+                                              ctypes.addressof(S)), "sgmv_build_segments")
+    s = S.value
+    return perm[:T].clone(), seg_ptr[: s + 1].clone(), idx[:s].clone()
+
+
+def sgmv_build_segments_device(row_adapter: torch.Tensor, L: int, out=None):
+    """Device grouping -> (perm, seg_ptr, idx, S) device int32 tensors, padded to
+    sgmv_max_segments(T, L) segments (S holds the real count on the device)."""
+    ra = _meta(row_adapter, "row_adapter")
+    T = ra.numel()
+    smax = sgmv_max_segments(T, L)
+    if out is None:
+        dev = ra.device
+        out = (torch.empty(max(T, 1), dtype=torch.int32, device=dev),
+               torch.empty(smax + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(smax, 1), dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev))
+    perm, seg_ptr, idx, S = out
+    _check(load_library().sgmv_build_segments_device(
+        ra.data_ptr(), T, L, perm.data_ptr(), seg_ptr.data_ptr(), idx.data_ptr(), S.data_ptr(),
+        _stream(ra.device)), "sgmv_build_segments_device")
+    return perm, seg_ptr, idx, S
+
+
+def _nseg(idx, S):
+    return idx.numel() if S is None else int(S)
+
+
+def sgmv_shrink(v, x, A, seg_ptr, idx, perm=None, seg_ptr_host=None, S=None):
+    """v[p] = x[row(p)] @ A[idx[s]] (fp32), in place; returns v."""
+    T, H1 = x.shape
+    L, _, r = A.shape
+    sph = _host_i32(seg_ptr_host)
+    _check(load_library().sgmv_shrink(
+        _ptr(v), _ptr(x), _ptr(A), _DTYPES[x.dtype], _ptr(_meta(perm, "perm")),
+        _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")), _nseg(idx, S), _ptr(sph),
+        T, L, H1, r, _stream(x.device)), "sgmv_shrink")
+    return v
+
+
+def sgmv_expand(y, v, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_host=None, S=None):
+    """y[row(p)] += scale * v[p] @ B[idx[s]], in place; returns y."""
+    T, H2 = y.shape
+    L, r, _ = B.shape
+    sph = _host_i32(seg_ptr_host)
+    _check(load_library().sgmv_expand(
+        _ptr(y), _DTYPES[y.dtype], _ptr(v), _ptr(B), _DTYPES[B.dtype], float(scale),
+        _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")),
+        _nseg(idx, S), _ptr(sph), T, L, H2, r, _stream(y.device)), "sgmv_expand")
+    return y
+
+
+def sgmv_apply(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_host=None,
+               workspace=None, S=None):
+    """y[row(p)] += scale * (x[row(p)] @ A[idx[s]]) @ B[idx[s]], in place; returns y."""
+    T, H1 = x.shape
+    L, _, r = A.shape
+    H2 = y.shape[1]
+    sph = _host_i32(seg_ptr_host)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().sgmv_apply(
+        _ptr(y), _DTYPES[y.dtype], _ptr(x), _ptr(A), _ptr(B), _DTYPES[x.dtype], float(scale),
+        _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")),
+        _nseg(idx, S), _ptr(sph), T, L, H1, H2, r, _ptr(workspace), ws_bytes,
+        _stream(x.device)), "sgmv_apply")
+    return y
+
+
+def sgmv_get_device_error(device=None) -> int:
+    """Synchronise the current stream, read and clear the device error word."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return int(load_library().sgmv_get_device_error(_stream(dev)))

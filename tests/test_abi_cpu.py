@@ -1,0 +1,141 @@
+"""The C ABI without a GPU: the library loads, exports what include/sgmv.h
+declares, groups rows on the host exactly like the oracle, and rejects bad
+arguments with the documented status before touching CUDA."""
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.golden import load
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rank_gemv_gb300 import build, sgmv
+
+    build.build()
+    return sgmv.load_library()
+
+
+def declared_functions():
+    text = (ROOT / "include" / "sgmv.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sgmv_\w+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    from rank_gemv_gb300 import sgmv
+
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in sgmv.SIGNATURES, f"binding lacks {n}"
+    assert sorted(sgmv.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    from rank_gemv_gb300 import sgmv
+
+    for code, name in sgmv.STATUS.items():
+        assert sgmv.sgmv_status_string(code) == name
+    assert sgmv.sgmv_status_string(99) == "SGMV_ERR_UNKNOWN"
+
+
+def test_max_segments_and_workspace(lib):
+    from rank_gemv_gb300 import sgmv
+
+    assert sgmv.sgmv_max_segments(32, 32) == 32
+    assert sgmv.sgmv_max_segments(8, 3) == 4
+    assert sgmv.sgmv_max_segments(0, 5) == 0
+    assert sgmv.sgmv_workspace_bytes(100, 4096, 4096, 16) >= 100 * 16 * 4
+    assert sgmv.sgmv_workspace_bytes(0, 4096, 4096, 16) == 0
+
+
+def test_host_grouping_golden(lib):
+    from rank_gemv_gb300 import sgmv
+
+    d = load("segments_worked_example.txt")
+    perm, seg_ptr, idx = sgmv.sgmv_build_segments(d["row_adapter"], d["L"])
+    assert np.array_equal(perm.numpy(), d["perm"])
+    assert np.array_equal(seg_ptr.numpy(), d["seg_ptr"])
+    assert np.array_equal(idx.numpy(), d["idx"])
+
+
+@pytest.mark.parametrize("T,L", [(0, 1), (1, 1), (7, 3), (64, 128), (1000, 37), (5000, 2)])
+def test_host_grouping_matches_oracle(lib, T, L):
+    from rank_gemv_gb300 import sgmv
+
+    rng = np.random.default_rng(T * 31 + L)
+    ra = rng.integers(-1, L, size=T).astype(np.int32)
+    perm, seg_ptr, idx = sgmv.sgmv_build_segments(ra, L)
+    o_perm, o_seg, o_idx = oracle.build_segments(ra, L)
+    assert np.array_equal(perm.numpy(), o_perm)
+    assert np.array_equal(seg_ptr.numpy(), o_seg)
+    assert np.array_equal(idx.numpy(), o_idx)
+
+
+def test_host_grouping_rejects_bad_ids(lib):
+    from rank_gemv_gb300 import sgmv
+
+    for bad in ([0, 3], [-2, 0]):
+        with pytest.raises(sgmv.SgmvError) as e:
+            sgmv.sgmv_build_segments(bad, 3)
+        assert e.value.status == 4
+
+
+# Host validation happens before any CUDA call, so fake device addresses are
+# safe here: each case below must be rejected on the host.
+A16 = 0x10000          # 16-byte aligned fake device address
+MIS = 0x10008          # misaligned fake device address
+
+
+def _apply(lib, **kw):
+    args = dict(y=A16, y_dt=0, x=A16, A=A16, B=A16, in_dt=0, scale=1.0, perm=None,
+                seg_ptr=A16, idx=A16, S=1, sph=None, T=4, L=2, H1=64, H2=64, r=16,
+                ws=None, wsb=0, stream=None)
+    args.update(kw)
+    sph = args["sph"]
+    if sph is not None:
+        sph = np.ascontiguousarray(sph, dtype=np.int32)
+        sph_p = sph.ctypes.data
+    else:
+        sph_p = None
+    return lib.sgmv_apply(args["y"], args["y_dt"], args["x"], args["A"], args["B"], args["in_dt"],
+                          args["scale"], args["perm"], args["seg_ptr"], args["idx"], args["S"],
+                          sph_p, args["T"], args["L"], args["H1"], args["H2"], args["r"],
+                          args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(r=0), 1), (dict(r=129), 2), (dict(T=-1), 1), (dict(L=0), 1), (dict(S=-1), 1),
+    (dict(H1=12), 3), (dict(H2=100), 3), (dict(H1=0), 1), (dict(in_dt=2), 1), (dict(y_dt=7), 1),
+    (dict(x=MIS), 3), (dict(A=MIS), 3), (dict(B=MIS), 3), (dict(y=MIS), 3),
+    (dict(x=None), 1), (dict(seg_ptr=None), 1), (dict(idx=None), 1),
+    (dict(sph=[0, 5]), 8), (dict(sph=[3, 2]), 8), (dict(sph=[-1, 2]), 8),
+    (dict(ws=A16, wsb=16), 6),
+])
+def test_apply_rejects_bad_arguments(lib, kw, status):
+    assert _apply(lib, **kw) == status
+
+
+def test_empty_problems_are_no_ops(lib):
+    assert _apply(lib, T=0, S=0, x=None, y=None, A=None, B=None) == 0
+    assert _apply(lib, S=0, seg_ptr=None, idx=None) == 0
+
+
+def test_shrink_expand_reject_bad_arguments(lib):
+    assert lib.sgmv_shrink(A16, A16, A16, 0, None, A16, A16, 1, None, 4, 2, 20, 16, None) == 3
+    assert lib.sgmv_shrink(A16, MIS, A16, 0, None, A16, A16, 1, None, 4, 2, 64, 16, None) == 3
+    assert lib.sgmv_shrink(A16, A16, A16, 0, None, A16, A16, 1, None, 4, 2, 64, 200, None) == 2
+    assert lib.sgmv_expand(A16, 3, A16, A16, 0, 1.0, None, A16, A16, 1, None, 4, 2, 64, 16,
+                           None) == 1
+    assert lib.sgmv_expand(MIS, 0, A16, A16, 0, 1.0, None, A16, A16, 1, None, 4, 2, 64, 16,
+                           None) == 3
+    assert lib.sgmv_build_segments_device(A16, 4, 40000, A16, A16, A16, A16, None) == 2
+    assert lib.sgmv_build_segments_device(A16, -1, 4, A16, A16, A16, A16, None) == 1
