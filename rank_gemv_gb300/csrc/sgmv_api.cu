@@ -113,6 +113,17 @@ int choose_cluster(int32_t H1, int32_t H2) {
     return cl;
 }
 
+void stage_sizes(CCParams &p, int mode, int elem);
+
+// Fill the derived launch parameters once rows, r, cl, hc and jc are set.
+void finish(CCParams &p, int mode, int in_dtype, int y_dtype) {
+    p.rmax = rmax_of(p.r);
+    p.ysize = elem_size(y_dtype);
+    stage_sizes(p, mode, elem_size(in_dtype));
+    // prefetch y rows when the CTA's whole H2 slice is staged as one chunk
+    p.y_pref = (mode != kShrink && p.jc <= p.js) ? 1 : 0;
+}
+
 void stage_sizes(CCParams &p, int mode, int elem) {
     if (mode != kExpand) {
         // A multiple of 16 columns keeps the h -> thread assignment of the
@@ -237,7 +248,8 @@ int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype, const int3
     const int cl = choose_cluster(H1, 0);
     p.hc = round8(ceil_div(H1, cl));
     p.jc = 8;
-    stage_sizes(p, kShrink, elem_size(in_dtype));
+    p.cl = cl;
+    finish(p, kShrink, in_dtype, SGMV_F32);
     const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
     if (slots == 0) return SGMV_OK;
     if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
@@ -247,7 +259,6 @@ int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype, const int3
     l.rmax = rmax_of(r);
     l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
     l.cluster = cl;
-    p.cl = cl;
     l.stream = static_cast<cudaStream_t>(stream);
     l.pdl = true;
     return cuda_status("shrink kernel", cc_launch(in_dtype, l));
@@ -288,7 +299,8 @@ int sgmv_expand(void *y, int y_dtype, const float *v, const void *B, int in_dtyp
     const int nx = (int)std::max<int64_t>(1, ceil_div(H2, 512));
     p.jc = round8(ceil_div(H2, nx));
     p.hc = 8;
-    stage_sizes(p, kExpand, elem_size(in_dtype));
+    p.cl = 1;
+    finish(p, kExpand, in_dtype, y_dtype);
     const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
     if (slots == 0) return SGMV_OK;
     if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
@@ -298,7 +310,6 @@ int sgmv_expand(void *y, int y_dtype, const float *v, const void *B, int in_dtyp
     l.rmax = rmax_of(r);
     l.grid = dim3((unsigned)ceil_div(H2, p.jc), (unsigned)slots, 1);
     l.cluster = 1;
-    p.cl = 1;
     l.stream = static_cast<cudaStream_t>(stream);
     l.pdl = true;
     return cuda_status("expand kernel", cc_launch(in_dtype, l));
@@ -344,7 +355,8 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     const int cl = choose_cluster(H1, H2);
     p.hc = round8(ceil_div(H1, cl));
     p.jc = round8(ceil_div(H2, cl));
-    stage_sizes(p, kFused, elem_size(in_dtype));
+    p.cl = cl;
+    finish(p, kFused, in_dtype, y_dtype);
     const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
     if (slots == 0) return SGMV_OK;
     if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
@@ -354,7 +366,6 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     l.rmax = rmax_of(r);
     l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
     l.cluster = cl;
-    p.cl = cl;
     l.stream = static_cast<cudaStream_t>(stream);
     l.pdl = true;
     return cuda_status("fused kernel", cc_launch(in_dtype, l));

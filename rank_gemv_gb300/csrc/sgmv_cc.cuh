@@ -92,10 +92,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     constexpr int WG = RMAX >= 32 ? RMAX : 32;  // threads sharing one warp-group of k values
     constexpr int NWG = kThreads / WG;
     constexpr int G = kThreads / RMAX;          // h-groups in the shrink
-    __shared__ __align__(8) uint64_t bars[4];   // 0,1: (A,X) stages; 2,3: B stages
+    // 0,1: (A, X) stages, two arrivals each (A, then X); 2,3: B stages; 4: y rows
+    __shared__ __align__(8) uint64_t bars[5];
     __shared__ int s_info[4];
     __shared__ int s_row[kRowsMax];
-    __shared__ __align__(16) float s_vpart[kRowsMax * RMAX];
     __shared__ __align__(16) float s_v[kRowsMax * RMAX];
     __shared__ float s_red[(MODE == kExpand) ? 1 : NWG * kRowsMax * RMAX];
 
@@ -103,29 +103,22 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     const int lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
-    if (tid < 32) find_tile(P, blockIdx.y, MODE == kShrink, report, s_info);
+    if (tid < 32) {
+        find_tile(P, blockIdx.y, MODE == kShrink, report, s_info);
+        if (tid == 0) {
+            mbar_init(&bars[0], 2);
+            mbar_init(&bars[1], 2);
+            mbar_init(&bars[2], 1);
+            mbar_init(&bars[3], 1);
+            mbar_init(&bars[4], 1);
+            mbar_init_fence();
+        }
+    }
     __syncthreads();
     if (s_info[0] < 0) return;  // no tile for this slot (same for the whole cluster)
     const int p0 = s_info[1];
     const int nrows = s_info[2];
     const int a = s_info[3];
-
-    // Physical rows of the tile; invalid perm entries are skipped and reported.
-    if (tid < nrows) {
-        const int p = p0 + tid;
-        int row = P.perm ? P.perm[p] : p;
-        if (row < 0 || row >= P.T) {
-            set_error(P.err, kErrBadIndex);
-            row = -1;
-        }
-        s_row[tid] = row;
-    }
-    if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
 
     if (MODE == kShrink && a < 0) {  // no adapter: v = 0 for these rows
         pdl_wait();
@@ -135,20 +128,14 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 P.v_out[(size_t)(p0 + e / P.r) * P.r + e % P.r] = 0.f;
         return;
     }
-
-    unsigned vmask = 0;  // tile rows with a valid physical row
-    int nvalid = 0;
-#pragma unroll
-    for (int t = 0; t < kRowsMax; ++t)
-        if (t < nrows && s_row[t] >= 0) {
-            vmask |= 1u << t;
-            ++nvalid;
-        }
+    const bool clustered = MODE != kExpand && P.cl > 1;
+    if (clustered) cluster_arrive_relaxed();  // waited on just before the first peer access
 
     const CCSmem lay = cc_smem_layout(P, (int)sizeof(Tin), MODE);
     const Tin *gA = static_cast<const Tin *>(P.A);
     const Tin *gB = static_cast<const Tin *>(P.B);
     const Tin *gX = static_cast<const Tin *>(P.x);
+    Ty *gY = static_cast<Ty *>(P.y);
 
     // Slices owned by this CTA.
     int h0 = 0, h1 = 0, j0 = 0, j1 = 0;
@@ -162,6 +149,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     }
     const int nA = (MODE != kExpand && h1 > h0) ? (h1 - h0 + P.hs - 1) / P.hs : 0;
     const int nB = (MODE != kShrink && j1 > j0) ? (j1 - j0 + P.js - 1) / P.js : 0;
+    const bool y_pref = MODE != kShrink && P.y_pref && nB > 0;
 
     auto ax_buf = [&](int st) {
         return reinterpret_cast<Tin *>(dsmem + lay.ax_off + st * lay.ax_stage_bytes);
@@ -169,20 +157,25 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     auto b_buf = [&](int st) {
         return reinterpret_cast<Tin *>(dsmem + lay.b_off + st * lay.b_stage_bytes);
     };
-    // Chunk i of A (and its byte count in the expectation, X added by issue_x).
+    Ty *ybuf = reinterpret_cast<Ty *>(dsmem + lay.y_off);
+    float *recv = reinterpret_cast<float *>(dsmem + lay.recv_off);
+
+    // Chunk i of A: first of the two arrivals on its stage barrier.
     auto issue_a = [&](int i) {  // lane 0 of warp 0
         const int st = i % P.ax_stages;
         const int hlo = h0 + i * P.hs;
         const int hn = min(P.hs, h1 - hlo);
         const uint32_t ab = (uint32_t)(hn * P.r) * sizeof(Tin);
-        const uint32_t xb = (uint32_t)(nvalid * hn) * sizeof(Tin);
-        mbar_arrive_expect_tx(&bars[st], ab + xb);
+        mbar_arrive_expect_tx(&bars[st], ab);
         bulk_g2s(ax_buf(st), gA + ((size_t)a * P.H1 + hlo) * P.r, ab, &bars[st]);
     };
-    auto issue_x = [&](int i) {  // lanes of warp 0, one row each
+    // Chunk i of the tile's X rows: second arrival.  Needs s_row and nvalid.
+    auto issue_x = [&](int i, int nvalid) {  // all lanes of warp 0
         const int st = i % P.ax_stages;
         const int hlo = h0 + i * P.hs;
         const int hn = min(P.hs, h1 - hlo);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)(nvalid * hn) * sizeof(Tin));
+        __syncwarp();
         Tin *xs = ax_buf(st) + P.hs * P.r;
         if (lane < nrows && s_row[lane] >= 0)
             bulk_g2s(xs + lane * P.hs, gX + (size_t)s_row[lane] * P.H1 + hlo,
@@ -199,16 +192,42 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                      (uint32_t)jn * sizeof(Tin), &bars[2 + st]);
     };
 
-    // Weights first: they do not depend on the previous kernel on the stream.
+    // Weights first: they do not depend on the previous kernel on the stream,
+    // and nothing waits for the row permutation before they are requested.
     if (tid < 32) {
         if (lane == 0)
             for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_a(i);
         for (int i = 0; i < min(nB, P.b_stages); ++i) issue_b(i);
+    } else if (tid < 32 + nrows) {
+        // Physical rows of the tile; invalid perm entries are skipped and reported.
+        const int t = tid - 32;
+        int row = P.perm ? P.perm[p0 + t] : p0 + t;
+        if (row < 0 || row >= P.T) {
+            set_error(P.err, kErrBadIndex);
+            row = -1;
+        }
+        s_row[t] = row;
     }
     pdl_wait();
+    __syncthreads();
+    unsigned vmask = 0;  // tile rows with a valid physical row
+    int nvalid = 0;
+#pragma unroll
+    for (int t = 0; t < kRowsMax; ++t)
+        if (t < nrows && s_row[t] >= 0) {
+            vmask |= 1u << t;
+            ++nvalid;
+        }
+    // Activations and outputs: only after the previous kernel has finished.
     if (tid < 32) {
-        __syncwarp();
-        for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_x(i);
+        for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_x(i, nvalid);
+        if (y_pref) {
+            const uint32_t yb = (uint32_t)(j1 - j0) * sizeof(Ty);
+            if (lane == 0) mbar_arrive_expect_tx(&bars[4], yb * nvalid);
+            __syncwarp();
+            if (lane < nrows && s_row[lane] >= 0)
+                bulk_g2s(ybuf + lane * P.jc, gY + (size_t)s_row[lane] * P.H2 + j0, yb, &bars[4]);
+        }
     }
     pdl_trigger();
 
@@ -248,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             if (tid < 32 && i + P.ax_stages < nA) {
                 if (lane == 0) issue_a(i + P.ax_stages);
                 __syncwarp();
-                issue_x(i + P.ax_stages);
+                issue_x(i + P.ax_stages, nvalid);
             }
         }
         // groups holding the same k inside one warp sit RMAX lanes apart
@@ -265,29 +284,37 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 if (t < nrows) s_red[(wg * kRowsMax + t) * RMAX + k] = acc[t];
         }
         __syncthreads();
-        for (int e = tid; e < nrows * RMAX; e += kThreads) {
-            const int t = e / RMAX, kk = e % RMAX;
+        // This CTA's partial of v[t][k]: the warp-groups summed in order.
+        auto partial = [&](int t, int kk) {
             float s = 0.f;
 #pragma unroll
             for (int w = 0; w < NWG; ++w) s += s_red[(w * kRowsMax + t) * RMAX + kk];
-            s_vpart[t * RMAX + kk] = s;
-        }
-        // ---- sum the partials of the cluster's CTAs, in rank order ------
-        if (P.cl > 1) {
+            return s;
+        };
+        if (clustered) {
+            // Push the partial into slot `rank` of every CTA's receive buffer,
+            // then sum the slots locally in rank order: the same bits in every
+            // CTA, one cluster barrier, no remote loads.
+            const int rank = (int)blockIdx.x;
+            const int per = nrows * P.r;
+            cluster_wait();
+            for (int e = tid; e < P.cl * per; e += kThreads) {
+                const int c = e / per, rem = e - (e / per) * per;
+                const int t = rem / P.r, kk = rem - (rem / P.r) * P.r;
+                st_peer(peer_addr(&recv[(rank * kRowsMax + t) * RMAX + kk], (uint32_t)c),
+                        partial(t, kk));
+            }
             cluster_sync();
-            for (int e = tid; e < nrows * P.r; e += kThreads) {
+            for (int e = tid; e < per; e += kThreads) {
                 const int t = e / P.r, kk = e - (e / P.r) * P.r;
                 float s = 0.f;
-                for (int c = 0; c < P.cl; ++c)
-                    s += ld_peer(peer_addr(&s_vpart[t * RMAX + kk], (uint32_t)c));
+                for (int c = 0; c < P.cl; ++c) s += recv[(c * kRowsMax + t) * RMAX + kk];
                 s_v[t * RMAX + kk] = s;
             }
-            cluster_sync();  // peers are done reading this CTA's partials
         } else {
-            __syncthreads();
             for (int e = tid; e < nrows * P.r; e += kThreads) {
                 const int t = e / P.r, kk = e - (e / P.r) * P.r;
-                s_v[t * RMAX + kk] = s_vpart[t * RMAX + kk];
+                s_v[t * RMAX + kk] = partial(t, kk);
             }
         }
         if (MODE == kShrink) {
@@ -300,9 +327,13 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         }
     }
     __syncthreads();
+    if (y_pref && !mbar_wait(&bars[4], 0)) {
+        lost = true;
+        set_error(P.err, kErrTimeout);
+        mbar_wait(&bars[4], 0);
+    }
 
     // ---- expand: y[row, j] += scale * v . B[a][:, j] for this CTA's slice ----
-    Ty *gY = static_cast<Ty *>(P.y);
     for (int i = 0; i < nB; ++i) {
         const int st = i % P.b_stages;
         const uint32_t par = (uint32_t)((i / P.b_stages) & 1);
@@ -334,7 +365,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 }
                 Ty *yp = gY + (size_t)row * P.H2 + jlo + cv * 8;
                 float yv[8];
-                load8<Ty>(yp, yv);
+                if (y_pref)
+                    load8<Ty>(ybuf + t * P.jc + (jlo - j0) + cv * 8, yv);
+                else
+                    load8<Ty>(yp, yv);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) yv[q] = fmaf(P.scale, acc8[q], yv[q]);
                 store8<Ty>(yp, yv);

@@ -40,13 +40,16 @@ struct CCParams {
     int32_t ax_stages;   // 1 or 2 buffers for (A, X) chunks
     int32_t b_stages;    // 1 or 2 buffers for B chunks
     int32_t cl;          // CTAs per cluster along x (1 = no cluster)
+    int32_t rmax;        // compile-time bound on r of the launched kernel
+    int32_t ysize;       // bytes per element of y
+    int32_t y_pref;      // 1: the CTA's y rows are prefetched into shared memory
     int32_t min_len;     // only segments with min_len <= length <= max_len
     int32_t max_len;
     float scale;
 };
 
 struct CCSmem {
-    uint32_t ax_stage_bytes, b_stage_bytes, ax_off, b_off, total;
+    uint32_t ax_stage_bytes, b_stage_bytes, ax_off, b_off, y_off, recv_off, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -59,7 +62,13 @@ __host__ __device__ inline CCSmem cc_smem_layout(const CCParams &p, int elem, in
     s.b_stage_bytes = b ? align_up((uint32_t)(p.r * p.js) * elem, 128) : 0;
     s.ax_off = 0;
     s.b_off = ax ? s.ax_stage_bytes * p.ax_stages : 0;
-    s.total = s.b_off + (b ? s.b_stage_bytes * p.b_stages : 0);
+    // y rows of the tile: [rows][jc] when the CTA's whole H2 slice is one chunk
+    s.y_off = s.b_off + (b ? s.b_stage_bytes * p.b_stages : 0);
+    const uint32_t y_bytes = (b && p.y_pref) ? align_up((uint32_t)(p.rows * p.jc * p.ysize), 128) : 0;
+    // partial v of every CTA of the cluster: [cl][kRowsMax][rmax] fp32
+    s.recv_off = s.y_off + y_bytes;
+    const uint32_t recv_bytes = (ax && p.cl > 1) ? (uint32_t)(p.cl * kRowsMax * p.rmax) * 4u : 0;
+    s.total = s.recv_off + recv_bytes;
     return s;
 }
 

@@ -1,0 +1,39 @@
+"""Full-size llama7b-stack workload (32 layers x 7 projections, 128 decode rows
+on 128 adapters, about 10 GB of stacked adapters) in the benchmark's launch
+configuration: one device grouping, then 224 fused updates.  Sampled
+projections are checked against the oracle element by element."""
+import pytest
+import torch
+
+import oracle
+from rank_gemv_gb300 import workloads as wl
+from tests.gpu_helpers import assert_close, check_error_word
+
+pytestmark = pytest.mark.gpu
+
+SAMPLES = [(0, 0), (9, 3), (17, 4), (24, 5), (31, 6)]  # (layer, projection)
+
+
+def test_llama7b_stack_sampled_projections():
+    from rank_gemv_gb300 import build, sgmv
+
+    build.build()
+    dev = torch.device("cuda")
+    seed = 0
+    projs = [wl.stack_projection(seed, layer, p, device=dev)
+             for layer in range(wl.LLAMA7B_LAYERS) for p in range(len(wl.LLAMA7B_PROJ))]
+    ra = wl.stack_row_adapter(128)
+    perm, seg_ptr, idx, S = sgmv.sgmv_build_segments_device(ra.to(dev), 128)
+    smax = sgmv.sgmv_max_segments(128, 128)
+    for X, A, B, Y in projs:
+        sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=smax)
+    check_error_word(0)
+    o_perm, o_seg, o_idx = oracle.build_segments(ra, 128)
+    n_proj = len(wl.LLAMA7B_PROJ)
+    for layer, p in SAMPLES:
+        X, A, B, Y = projs[layer * n_proj + p]
+        Y0 = torch.zeros(Y.shape, dtype=torch.float16)
+        ref = oracle.sgmv_apply(Y0, X, A, B, o_seg, o_idx, 1.0, perm=o_perm)
+        assert_close(Y, ref, f"layer {layer} proj {wl.LLAMA7B_PROJ[p][0]}")
+    del projs
+    torch.cuda.empty_cache()
