@@ -101,6 +101,11 @@ const char *sgmv_status_string(int status);
  * owned by the library, valid until the thread's next failing call. */
 const char *sgmv_last_error_string(void);
 
+/* Number of kernels the calling thread's last sgmv_shrink / sgmv_expand /
+ * sgmv_apply / sgmv_build_segments_device call launched (0 when it returned
+ * before launching anything). */
+int sgmv_last_launch_count(void);
+
 /* Upper bound on the number of segments that grouping T rows over L adapters
  * (ids -1..L-1) can produce: min(T, L + 1).  Size seg_ptr (bound + 1) and idx
  * (bound) with it for sgmv_build_segments_device. */

@@ -18,6 +18,7 @@ namespace {
 using namespace sgmv;
 
 thread_local char g_last_error[256] = "";
+thread_local int g_launches = 0;  // kernels launched by this thread's last call
 
 void note(const char *what, cudaError_t e) {
     snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, cudaGetErrorString(e));
@@ -98,7 +99,13 @@ int64_t tile_slots(int32_t T, int32_t S, const int32_t *sp, int rows, int min_le
         }
         return n;
     }
-    return ((int64_t)T + (int64_t)S * (rows - 1)) / rows;
+    // sum over segments of ceil(len / rows) <= (T + S (rows - 1)) / rows
+    int64_t b = ((int64_t)T + (int64_t)S * (rows - 1)) / rows;
+    // short segments only: at most ceil(max_len / rows) tiles each
+    if (max_len < INT_MAX) b = std::min<int64_t>(b, (int64_t)S * ceil_div(max_len, rows));
+    // long segments only: at most T / min_len of them, one partial tile each
+    if (min_len > 1) b = std::min<int64_t>(b, (int64_t)T / rows + (int64_t)T / min_len);
+    return b;
 }
 
 int cc_launch(int in_dtype, const CCLaunch &l) {
@@ -126,10 +133,10 @@ void finish(CCParams &p, int mode, int in_dtype, int y_dtype) {
 
 void stage_sizes(CCParams &p, int mode, int elem) {
     if (mode != kExpand) {
-        // A multiple of 16 columns keeps the h -> thread assignment of the
-        // shrink independent of the chunking, so every row's v is bitwise the
-        // same whatever the tile shape.
-        p.hs = std::min(p.hc, floor16(kStageBytes / ((int64_t)(p.r + p.rows) * elem)));
+        // Sized for kRowsMax rows whatever the tile height, so the chunking of
+        // H1 (and with it the summation order of every row's v) does not
+        // depend on how segments are cut into tiles.
+        p.hs = std::min(p.hc, floor16(kStageBytes / ((int64_t)(p.r + kRowsMax) * elem)));
         p.ax_stages = ceil_div(p.hc, p.hs) > 1 ? 2 : 1;
     } else {
         p.hs = 8;
@@ -165,6 +172,8 @@ const char *sgmv_status_string(int status) {
 
 const char *sgmv_last_error_string(void) { return g_last_error; }
 
+int sgmv_last_launch_count(void) { return g_launches; }
+
 int32_t sgmv_max_segments(int32_t T, int32_t L) {
     if (T <= 0 || L < 0) return 0;
     return (int32_t)std::min<int64_t>(T, (int64_t)L + 1);
@@ -198,27 +207,33 @@ int sgmv_build_segments(const int32_t *row_adapter, int32_t T, int32_t L, int32_
 
 int sgmv_build_segments_device(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
                                int32_t *seg_ptr, int32_t *idx, int32_t *S, void *stream) {
+    g_launches = 0;
     if (T < 0 || L < 1 || !seg_ptr || !S) return SGMV_ERR_INVALID_ARG;
     if (T > 0 && (!row_adapter || !perm || !idx)) return SGMV_ERR_INVALID_ARG;
     if (L > 32767) return SGMV_ERR_UNSUPPORTED;
     int *err = error_word();
     if (!err) return SGMV_ERR_CUDA;
-    return cuda_status("build_segments kernel",
-                       build_segments_launch(row_adapter, T, L, perm, seg_ptr, idx, S,
-                                             sgmv_max_segments(T, L), err,
-                                             static_cast<cudaStream_t>(stream)));
+    const int st = cuda_status("build_segments kernel",
+                               build_segments_launch(row_adapter, T, L, perm, seg_ptr, idx, S,
+                                                     sgmv_max_segments(T, L), err,
+                                                     static_cast<cudaStream_t>(stream)));
+    if (st == SGMV_OK) g_launches = 1;
+    return st;
 }
 
 size_t sgmv_workspace_bytes(int32_t T, int32_t H1, int32_t H2, int32_t r) {
     (void)H1;
     (void)H2;
     if (T <= 0 || r <= 0) return 0;
-    return (size_t)T * (size_t)r * 4u + 256u;
+    // v as two 16-bit halves, [T][r] each, the second one 256-byte aligned
+    const size_t half = ((size_t)T * (size_t)r * 2u + 255u) / 256u * 256u;
+    return 2u * half;
 }
 
 int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype, const int32_t *perm,
                 const int32_t *seg_ptr, const int32_t *idx, int32_t S, const int32_t *seg_ptr_host,
                 int32_t T, int32_t L, int32_t H1, int32_t r, void *stream) {
+    g_launches = 0;
     int st = check_common(T, L, r, S, seg_ptr, idx, seg_ptr_host, in_dtype);
     if (st != SGMV_OK) return st;
     if ((st = check_dim(H1)) != SGMV_OK) return st;
@@ -261,13 +276,16 @@ int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype, const int3
     l.cluster = cl;
     l.stream = static_cast<cudaStream_t>(stream);
     l.pdl = true;
-    return cuda_status("shrink kernel", cc_launch(in_dtype, l));
+    st = cuda_status("shrink kernel", cc_launch(in_dtype, l));
+    if (st == SGMV_OK) g_launches = 1;
+    return st;
 }
 
 int sgmv_expand(void *y, int y_dtype, const float *v, const void *B, int in_dtype, float scale,
                 const int32_t *perm, const int32_t *seg_ptr, const int32_t *idx, int32_t S,
                 const int32_t *seg_ptr_host, int32_t T, int32_t L, int32_t H2, int32_t r,
                 void *stream) {
+    g_launches = 0;
     int st = check_common(T, L, r, S, seg_ptr, idx, seg_ptr_host, in_dtype);
     if (st != SGMV_OK) return st;
     if ((st = check_dim(H2)) != SGMV_OK) return st;
@@ -312,13 +330,16 @@ int sgmv_expand(void *y, int y_dtype, const float *v, const void *B, int in_dtyp
     l.cluster = 1;
     l.stream = static_cast<cudaStream_t>(stream);
     l.pdl = true;
-    return cuda_status("expand kernel", cc_launch(in_dtype, l));
+    st = cuda_status("expand kernel", cc_launch(in_dtype, l));
+    if (st == SGMV_OK) g_launches = 1;
+    return st;
 }
 
 int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B, int in_dtype,
                float scale, const int32_t *perm, const int32_t *seg_ptr, const int32_t *idx,
                int32_t S, const int32_t *seg_ptr_host, int32_t T, int32_t L, int32_t H1,
                int32_t H2, int32_t r, void *workspace, size_t workspace_bytes, void *stream) {
+    g_launches = 0;
     int st = check_common(T, L, r, S, seg_ptr, idx, seg_ptr_host, in_dtype);
     if (st != SGMV_OK) return st;
     if ((st = check_dim(H1)) != SGMV_OK) return st;
@@ -331,6 +352,19 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     if (!y || !x || !A || !B) return SGMV_ERR_INVALID_ARG;
     if (!aligned16(y) || !aligned16(x) || !aligned16(A) || !aligned16(B))
         return SGMV_ERR_ALIGNMENT;
+
+    int *err = error_word();
+    if (!err) return SGMV_ERR_CUDA;
+    // Dispatch: segments of at least kTcMinLen rows to the tensor cores when a
+    // workspace holds their v and r suits the tensor-core tiles.
+    bool use_tc = workspace != nullptr && (r == 64 || r == 128) && T >= kTcMinLen;
+    int64_t tc_slots = 0;
+    if (use_tc) {
+        tc_slots = tile_slots(T, S, seg_ptr_host, 128, kTcMinLen, INT_MAX);
+        if (tc_slots > 65535) return SGMV_ERR_UNSUPPORTED;
+        use_tc = tc_slots > 0;
+    }
+    const int32_t cc_max_len = use_tc ? kTcMinLen - 1 : INT_MAX;
 
     CCLaunch l = {};
     CCParams &p = l.p;
@@ -350,25 +384,58 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     const int32_t mx = longest(seg_ptr_host, S);
     p.rows = mx > 0 ? std::min(kRowsMax, mx) : kRowsMax;
     p.min_len = 1;
-    p.max_len = INT_MAX;
+    p.max_len = cc_max_len;
     p.scale = scale;
     const int cl = choose_cluster(H1, H2);
     p.hc = round8(ceil_div(H1, cl));
     p.jc = round8(ceil_div(H2, cl));
     p.cl = cl;
     finish(p, kFused, in_dtype, y_dtype);
-    const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, INT_MAX);
-    if (slots == 0) return SGMV_OK;
+    const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, cc_max_len);
     if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
-    if (!(p.err = error_word())) return SGMV_ERR_CUDA;
-    l.mode = kFused;
-    l.y_dtype = y_dtype;
-    l.rmax = rmax_of(r);
-    l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
-    l.cluster = cl;
-    l.stream = static_cast<cudaStream_t>(stream);
-    l.pdl = true;
-    return cuda_status("fused kernel", cc_launch(in_dtype, l));
+    p.err = err;
+    if (slots > 0) {
+        l.mode = kFused;
+        l.y_dtype = y_dtype;
+        l.rmax = rmax_of(r);
+        l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
+        l.cluster = cl;
+        l.stream = static_cast<cudaStream_t>(stream);
+        l.pdl = true;
+        st = cuda_status("fused kernel", cc_launch(in_dtype, l));
+        if (st != SGMV_OK) return st;
+        g_launches = 1;
+    }
+    if (!use_tc) return SGMV_OK;
+
+    TCArgs g = {};
+    g.y = y;
+    g.x = x;
+    g.A = A;
+    g.B = B;
+    g.perm = perm;
+    g.seg_ptr = seg_ptr;
+    g.idx = idx;
+    g.err = err;
+    const size_t half = sgmv_workspace_bytes(T, H1, H2, r) / 2;
+    g.vhi = workspace;
+    g.vlo = static_cast<uint8_t *>(workspace) + half;
+    g.S = S;
+    g.T = T;
+    g.L = L;
+    g.H1 = H1;
+    g.H2 = H2;
+    g.r = r;
+    g.min_len = kTcMinLen;
+    g.max_len = INT_MAX;
+    g.scale = scale;
+    g.in_dtype = in_dtype;
+    g.y_dtype = y_dtype;
+    g.slots = tc_slots;
+    g.stream = static_cast<cudaStream_t>(stream);
+    st = cuda_status("tensor-core kernels", tc_launch(g));
+    if (st == SGMV_OK) g_launches += 2;
+    return st;
 }
 
 int sgmv_get_device_error(void *stream) {

@@ -26,85 +26,27 @@
 
 #include "sgmv_device.cuh"
 #include "sgmv_internal.h"
+#include "sgmv_tiles.cuh"
 
 namespace sgmv {
-
-// Warp 0 finds the tile with number `tile` among the segments that this launch
-// handles.  out = {segment or -1, first position, rows, adapter}.  With
-// `report`, the warp scans every segment and records malformed ones in the
-// error word (one CTA per launch reports).
-__device__ __forceinline__ void find_tile(const CCParams &P, int tile, bool with_no_adapter,
-                                          bool report, int *out) {
-    const int lane = threadIdx.x & 31;
-    int base = 0;
-    int f_s = -1, f_p0 = 0, f_n = 0, f_a = -1;
-    for (int s0 = 0; s0 < P.S; s0 += 32) {
-        const int s = s0 + lane;
-        int n = 0, b = 0, e = 0, a = -1;
-        if (s < P.S) {
-            b = P.seg_ptr[s];
-            e = P.seg_ptr[s + 1];
-            a = P.idx[s];
-            const bool seg_ok = b >= 0 && e >= b && e <= P.T;
-            const bool idx_ok = a >= -1 && a < P.L;
-            if (report && !seg_ok) set_error(P.err, kErrBadSegments);
-            if (report && seg_ok && !idx_ok) set_error(P.err, kErrBadIndex);
-            const int len = e - b;
-            if (seg_ok && idx_ok && len > 0 && (a >= 0 || with_no_adapter) && len >= P.min_len &&
-                len <= P.max_len)
-                n = (len + P.rows - 1) / P.rows;
-        }
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        const int excl = incl - n;
-        const bool mine = f_s < 0 && n > 0 && tile >= base + excl && tile < base + incl;
-        const unsigned m = __ballot_sync(0xffffffffu, mine);
-        if (m) {
-            const int src = __ffs(m) - 1;
-            int p0 = 0, nr = 0;
-            if (lane == src) {
-                p0 = b + (tile - base - excl) * P.rows;
-                nr = min(P.rows, e - p0);
-            }
-            f_s = __shfl_sync(0xffffffffu, s, src);
-            f_p0 = __shfl_sync(0xffffffffu, p0, src);
-            f_n = __shfl_sync(0xffffffffu, nr, src);
-            f_a = __shfl_sync(0xffffffffu, a, src);
-            if (!report) break;
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-        out[0] = f_s;
-        out[1] = f_p0;
-        out[2] = f_n;
-        out[3] = f_a;
-    }
-}
 
 template <typename Tin, typename Ty, int RMAX, int MODE>
 __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant__ CCParams P) {
     extern __shared__ __align__(128) uint8_t dsmem[];
-    constexpr int WG = RMAX >= 32 ? RMAX : 32;  // threads sharing one warp-group of k values
-    constexpr int NWG = kThreads / WG;
-    constexpr int G = kThreads / RMAX;          // h-groups in the shrink
     // 0,1: (A, X) stages, two arrivals each (A, then X); 2,3: B stages; 4: y rows
     __shared__ __align__(8) uint64_t bars[5];
     __shared__ int s_info[4];
     __shared__ int s_row[kRowsMax];
     __shared__ __align__(16) float s_v[kRowsMax * RMAX];
-    __shared__ float s_red[(MODE == kExpand) ? 1 : NWG * kRowsMax * RMAX];
+    __shared__ float s_red[(MODE == kExpand) ? 1 : kRowsMax * RMAX * (kThreads / (RMAX / 16)) / 32];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
     if (tid < 32) {
-        find_tile(P, blockIdx.y, MODE == kShrink, report, s_info);
+        find_tile(P.seg_ptr, P.idx, P.S, P.T, P.L, P.rows, P.min_len, P.max_len, P.err,
+                  blockIdx.y, MODE == kShrink, report, s_info);
         if (tid == 0) {
             mbar_init(&bars[0], 2);
             mbar_init(&bars[1], 2);
@@ -239,11 +181,19 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         }
     } else {
         // ---- shrink: partial v over this CTA's H1 slice -----------------
-        float acc[kRowsMax];
-#pragma unroll
-        for (int t = 0; t < kRowsMax; ++t) acc[t] = 0.f;
-        const int k = tid % RMAX;
-        const int g = tid / RMAX;
+        // Thread -> (k-group of 16 columns of r, h-group); each thread reads
+        // two 16-byte vectors of A per h and one X value per row, and the
+        // 32 h-groups of a warp are summed by a reduce-scatter butterfly.
+        constexpr int KG = RMAX / 16;        // k-groups: 1, 2, 4, 8
+        constexpr int HG = kThreads / KG;    // h-groups per k-group (>= 32)
+        constexpr int WPG = HG / 32;         // warps per k-group
+        const int kg = tid / HG, hg = tid - (tid / HG) * HG;
+        const int kbase = kg * 16;
+        const int wig = hg >> 5;             // warp within the k-group
+        const bool kact = kbase < P.r;       // same for the whole warp
+        const bool vec = (P.r & 7) == 0;     // A rows are 16-byte aligned in smem
+        for (int e = tid; e < kRowsMax * RMAX * WPG; e += kThreads) s_red[e] = 0.f;
+        __syncthreads();
         for (int i = 0; i < nA; ++i) {
             const int st = i % P.ax_stages;
             const uint32_t par = (uint32_t)((i / P.ax_stages) & 1);
@@ -255,12 +205,47 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             const int hn = min(P.hs, h1 - (h0 + i * P.hs));
             const Tin *As = ax_buf(st);
             const Tin *Xs = As + P.hs * P.r;
-            if (k < P.r) {
-                for (int h = g; h < hn; h += G) {
-                    const float av = to_f<Tin>(As[h * P.r + k]);
+            if (kact) {
+                for (int t = 0; t < nrows; ++t) {
+                    if (!(vmask & (1u << t))) continue;
+                    float acc[16];
 #pragma unroll
-                    for (int t = 0; t < kRowsMax; ++t)
-                        if (vmask & (1u << t)) acc[t] = fmaf(to_f<Tin>(Xs[t * P.hs + h]), av, acc[t]);
+                    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+                    for (int h = hg; h < hn; h += HG) {
+                        const float x = to_f<Tin>(Xs[t * P.hs + h]);
+                        float av[16];
+                        const Tin *arow = As + h * P.r + kbase;
+                        if (vec) {
+                            float lo[8], hi[8];
+                            unpack8<Tin>(*reinterpret_cast<const uint4 *>(arow), lo);
+                            unpack8<Tin>(*reinterpret_cast<const uint4 *>(arow + 8), hi);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                av[j] = lo[j];
+                                av[8 + j] = hi[j];
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                av[j] = kbase + j < P.r ? to_f<Tin>(arow[j]) : 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] = fmaf(x, av[j], acc[j]);
+                    }
+                    // reduce-scatter over the warp: lane l ends with k = kbase + l/2
+#pragma unroll
+                    for (int half = 8; half >= 1; half >>= 1) {
+                        const bool upper = (lane & (half * 2)) != 0;
+#pragma unroll
+                        for (int j = 0; j < half; ++j) {
+                            const float keep = upper ? acc[half + j] : acc[j];
+                            const float give = upper ? acc[j] : acc[half + j];
+                            acc[j] = keep + __shfl_xor_sync(0xffffffffu, give, half * 2);
+                        }
+                    }
+                    acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+                    if ((lane & 1) == 0)
+                        s_red[(t * RMAX + kbase + (lane >> 1)) * WPG + wig] += acc[0];
                 }
             }
             __syncthreads();
@@ -270,25 +255,11 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 issue_x(i + P.ax_stages, nvalid);
             }
         }
-        // groups holding the same k inside one warp sit RMAX lanes apart
-        if (RMAX < 32) {
-#pragma unroll
-            for (int off = RMAX; off < 32; off <<= 1)
-#pragma unroll
-                for (int t = 0; t < kRowsMax; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
-        }
-        if ((tid % WG) < RMAX) {
-            const int wg = tid / WG;
-#pragma unroll
-            for (int t = 0; t < kRowsMax; ++t)
-                if (t < nrows) s_red[(wg * kRowsMax + t) * RMAX + k] = acc[t];
-        }
-        __syncthreads();
-        // This CTA's partial of v[t][k]: the warp-groups summed in order.
+        // This CTA's partial of v[t][k]: the warps of the k-group summed in order.
         auto partial = [&](int t, int kk) {
             float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < NWG; ++w) s += s_red[(w * kRowsMax + t) * RMAX + kk];
+            for (int w = 0; w < WPG; ++w) s += s_red[(t * RMAX + kk) * WPG + w];
             return s;
         };
         if (clustered) {

@@ -16,9 +16,12 @@ constexpr int kErrBadIndex = 4;
 constexpr int kErrTimeout = 7;
 constexpr int kErrBadSegments = 8;
 
-// Bound on mbarrier polls before a wait is declared lost.  Each try_wait may
-// suspend the thread for a while, so this is on the order of a second.
-constexpr uint32_t kMaxPolls = 1u << 20;
+// Bounds of every mbarrier wait: about one second of %globaltimer, and at most
+// kMaxPolls polls.  Each poll may suspend the thread for up to kSuspendNs
+// (it resumes as soon as the phase completes).
+constexpr uint32_t kMaxPolls = 1u << 22;
+constexpr uint32_t kSuspendNs = 20000;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ void set_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
@@ -55,17 +58,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 // Bounded wait for phase `parity` to complete.  Returns false if it did not.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) break;
+    }
     return false;
 }
 

@@ -83,6 +83,33 @@ struct CCLaunch {
     bool pdl;
 };
 
+// Tensor-core launch pair (shrink then expand) for segments of at least
+// min_len rows.  v is kept in the workspace as two 16-bit halves, vhi and vlo.
+struct TCArgs {
+    void *y;
+    const void *x;
+    const void *A;
+    const void *B;
+    const int32_t *perm;
+    const int32_t *seg_ptr;
+    const int32_t *idx;
+    int *err;
+    void *vhi;
+    void *vlo;
+    int32_t S, T, L, H1, H2, r;
+    int32_t min_len, max_len;
+    float scale;
+    int in_dtype, y_dtype;
+    int64_t slots;   // 128-row tile slots
+    cudaStream_t stream;
+};
+
+// Segments at least this long go to the tensor cores (when a workspace is
+// given and r is 64 or 128).
+constexpr int kTcMinLen = 64;
+
+int tc_launch(const TCArgs &g);
+
 // Launch one CUDA-core kernel; returns a cudaError_t value.
 int cc_launch_f16(const CCLaunch &l);
 int cc_launch_bf16(const CCLaunch &l);

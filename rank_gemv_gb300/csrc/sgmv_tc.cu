@@ -1,0 +1,607 @@
+// sgmv_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) SGMV for long segments.
+//
+// A prefill segment of hundreds of rows turns each SGMV step into a real
+// dense contraction ("Punica: when LoRA fine-tuned models need multi-tenant
+// serving", omica.com.cn article, §2.2: shrink x.A, then expand v.B, per
+// adapter): X[rows, H1] . A[a] is [rows, r], and v[rows, r] . B[a] is
+// [rows, H2].  These kernels run both on the 5th-generation tensor cores.
+//
+// Shrink (sgmv_tc_shrink_kernel): one 128-row tile of a segment per cluster;
+//   the cluster's CL CTAs split H1.  Each CTA streams 64-column k-blocks
+//   through a 3-stage ring: X rows are gathered through perm with 16-byte
+//   cp.async writes into the 128-byte-swizzled K-major layout, A[a] k-blocks
+//   come by TMA (N-major, same swizzle).  One thread issues
+//   tcgen05.mma (M=128, N=r, K=16) into a TMEM accumulator; commits free the
+//   stages.  The partial v is read out of TMEM, pushed to the CTA that owns
+//   its rows through distributed shared memory, summed in rank order and
+//   written as two 16-bit halves, hi = round(v) and lo = round(v - hi), so
+//   the expand can run on 16-bit tensor cores and still see v to about
+//   16 significant bits.
+// Expand (sgmv_tc_expand_kernel): one CTA per (128-row tile, 128 columns of
+//   H2).  TMA brings B[a][:, j0:j0+128] (N-major) and the tile's v hi/lo
+//   (K-major); 2 x r/16 MMAs accumulate v_hi.B + v_lo.B in TMEM; each thread
+//   then owns one row: tcgen05.ld 32 columns at a time, y += scale * acc in
+//   fp32, rounded once to y's type.
+// Every mbarrier wait is bounded; TMEM is freed on every path.
+#include <cuda.h>  // CUtensorMap and the encoder's signature (no libcuda link)
+
+#include <cstring>
+#include <type_traits>
+
+#include "sgmv_device.cuh"
+#include "sgmv_internal.h"
+#include "sgmv_tiles.cuh"
+
+namespace sgmv {
+
+constexpr int kTcThreads = 128;  // 4 warps: one TMEM lane (tile row) per thread
+constexpr int kTcRows = 128;     // M of one tile
+constexpr int kKB = 64;          // k-block: 64 16-bit elements = one 128-byte swizzle row
+constexpr int kStages = 3;       // shrink ring depth
+constexpr int kTcN = 128;        // columns of H2 per expand CTA
+
+struct TCShrinkParams {
+    CUtensorMap tmap_a;  // A as [L][H1][r], box {64, 64, 1}
+    const void *x;
+    const int32_t *perm, *seg_ptr, *idx;
+    int *err;
+    void *vhi, *vlo;     // [T][r] each, input type
+    int32_t S, T, L, H1, r, hk, cl, min_len, max_len;
+};
+
+struct TCExpandParams {
+    CUtensorMap tmap_b;    // B as [L][r][H2], box {64, r, 1}
+    CUtensorMap tmap_vhi;  // v hi as [T][r], box {64, 128}
+    CUtensorMap tmap_vlo;
+    void *y;
+    const int32_t *perm, *seg_ptr, *idx;
+    int *err;
+    int32_t S, T, L, H2, r, min_len, max_len;
+    float scale;
+};
+
+// ---- tcgen05, TMA and cp.async wrappers -------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] . B[smem], 16-bit inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+// 32 TMEM lanes (one per thread of the warp) x 32 consecutive fp32 columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// 16-byte asynchronous copy; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// Arrive on `bar` when this thread's cp.async copies so far have landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void st_peer4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: version 1
+// at bit 46, layout 2 at bits 61-63).  lbo / sbo in bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, A K-major, B N-major.
+__device__ __forceinline__ uint32_t idesc_f16(bool bf16, int M, int N) {
+    const uint32_t f = bf16 ? 1u : 0u;
+    return (1u << 4) | (f << 7) | (f << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+// Byte offset of the 16-byte chunk c (0..7) of row m in a 128-byte-swizzled,
+// K-major [rows][64] 16-bit tile: 8-row atoms of 1024 bytes, chunk index XOR
+// row-in-atom.
+__device__ __forceinline__ uint32_t sw128_offset(int m, int c) {
+    return (uint32_t)((m >> 3) * 1024 + (m & 7) * 128 + ((c ^ (m & 7)) << 4));
+}
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    const uint32_t a = smem_addr(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// ---------------------------------------------------------------- shrink
+template <typename Tin>
+__global__ void __launch_bounds__(kTcThreads)
+    sgmv_tc_shrink_kernel(const __grid_constant__ TCShrinkParams P) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
+    __shared__ int s_info[4];
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool report = blockIdx.x == 0 && blockIdx.y == 0;
+
+    if (warp == 0) {
+        find_tile(P.seg_ptr, P.idx, P.S, P.T, P.L, kTcRows, P.min_len, P.max_len, P.err,
+                  blockIdx.y, false, report, s_info);
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(&full[s], kTcThreads + 1);  // 128 cp.async arrivals + the TMA one
+                mbar_init(&empty[s], 1);
+            }
+            mbar_init(&done, 1);
+            mbar_init_fence();
+        }
+    }
+    __syncthreads();
+    if (s_info[0] < 0) return;  // same decision in every CTA of the cluster
+    const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
+    const bool clustered = P.cl > 1;
+    if (clustered) cluster_arrive_relaxed();
+    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)P.r);
+
+    uint8_t *base = align1024(dsm);
+    const uint32_t x_bytes = kTcRows * kKB * sizeof(Tin);  // 16 KB
+    const uint32_t a_bytes = kKB * P.r * sizeof(Tin);       // 8 or 16 KB
+    auto stage_x = [&](int st) { return base + st * (x_bytes + a_bytes); };
+    auto stage_a = [&](int st) { return base + st * (x_bytes + a_bytes) + x_bytes; };
+    float *recv = reinterpret_cast<float *>(base + kStages * (x_bytes + a_bytes));
+    const Tin *gX = static_cast<const Tin *>(P.x);
+
+    const int k0 = (int)blockIdx.x * P.hk;
+    const int k1 = min(P.H1, k0 + P.hk);
+    const int nkb = k1 > k0 ? (k1 - k0 + kKB - 1) / kKB : 0;
+
+    auto issue_a = [&](int kb) {  // thread 0
+        const int st = kb % kStages;
+        mbar_arrive_expect_tx(&full[st], a_bytes);
+        for (int c = 0; c < P.r; c += 64)
+            tma_load_3d(stage_a(st) + c * kKB * sizeof(Tin), &P.tmap_a, c, k0 + kb * kKB, a,
+                        &full[st]);
+    };
+    if (tid == 0)
+        for (int kb = 0; kb < min(nkb, kStages); ++kb) issue_a(kb);
+
+    // Physical row of this thread's tile row (metadata is complete before launch).
+    int row = -1;
+    if (tid < nrows) {
+        row = P.perm ? P.perm[p0 + tid] : p0 + tid;
+        if (row < 0 || row >= P.T) {
+            set_error(P.err, kErrBadIndex);
+            row = -1;
+        }
+    }
+    auto issue_x = [&](int kb) {  // every thread: the 8 chunks of its own row
+        const int st = kb % kStages;
+        uint8_t *xs = stage_x(st);
+        const int kk0 = k0 + kb * kKB;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int k = kk0 + c * 8;
+            const bool ok = row >= 0 && k < k1;
+            cp_async16(xs + sw128_offset(tid, c), ok ? gX + (size_t)row * P.H1 + k : gX,
+                       ok ? 16u : 0u);
+        }
+        cp_async_arrive(&full[st]);
+    };
+    pdl_wait();
+    for (int kb = 0; kb < min(nkb, kStages); ++kb) issue_x(kb);
+    pdl_trigger();
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, P.r);
+    bool lost = false;
+    for (int kb = 0; kb < nkb; ++kb) {
+        const int st = kb % kStages;
+        const uint32_t ph = (uint32_t)((kb / kStages) & 1);
+        if (tid == 0) {
+            if (!mbar_wait(&full[st], ph)) {
+                lost = true;
+                set_error(P.err, kErrTimeout);
+                mbar_wait(&full[st], ph);
+            }
+            fence_proxy_async();  // cp.async (generic proxy) data -> tensor core (async proxy)
+            tc_fence_after();
+            const uint32_t xa = smem_addr(stage_x(st)), aa = smem_addr(stage_a(st));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_f16(tmem, sw128_desc(xa + kk * 32, 16, 1024),
+                        sw128_desc(aa + kk * 2048, kKB * 128, 1024), idesc, (kb | kk) != 0);
+            mma_commit(&empty[st]);
+        }
+        if (kb + kStages < nkb) {
+            if (!mbar_wait(&empty[st], ph)) {
+                lost = true;
+                set_error(P.err, kErrTimeout);
+                mbar_wait(&empty[st], ph);
+            }
+            if (tid == 0) issue_a(kb + kStages);
+            issue_x(kb + kStages);
+        }
+    }
+    if (tid == 0) mma_commit(&done);
+    if (!mbar_wait(&done, 0)) {
+        lost = true;
+        set_error(P.err, kErrTimeout);
+        mbar_wait(&done, 0);
+    }
+    tc_fence_after();
+
+    // Partial v of this CTA's H1 slice -> the CTA that owns the row.
+    const int rpc = kTcRows / P.cl;  // rows summed by each CTA of the cluster
+    const int rank = (int)blockIdx.x;
+    if (clustered) cluster_wait();
+    for (int c0 = 0; c0 < P.r; c0 += 32) {
+        float v[32];
+        if (nkb > 0) {
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        if (tid < nrows) {
+            const int owner = tid / rpc, mr = tid - (tid / rpc) * rpc;
+            float *dst = recv + (size_t)(rank * rpc + mr) * P.r + c0;
+            if (clustered) {
+                const uint32_t pa = peer_addr(dst, (uint32_t)owner);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) st_peer4(pa + j * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dst[j] = v[j];
+            }
+        }
+    }
+    if (clustered)
+        cluster_sync();
+    else
+        __syncthreads();
+    Tin *vhi = static_cast<Tin *>(P.vhi);
+    Tin *vlo = static_cast<Tin *>(P.vlo);
+    for (int e = tid; e < rpc * P.r; e += kTcThreads) {
+        const int mr = e / P.r, col = e - (e / P.r) * P.r;
+        const int m = rank * rpc + mr;
+        if (m >= nrows || lost) continue;
+        float s = 0.f;
+        for (int c = 0; c < P.cl; ++c) s += recv[(size_t)(c * rpc + mr) * P.r + col];
+        const Tin hi = from_f<Tin>(s);
+        const size_t o = (size_t)(p0 + m) * P.r + col;
+        vhi[o] = hi;
+        vlo[o] = from_f<Tin>(s - to_f<Tin>(hi));
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, (uint32_t)P.r);
+}
+
+// ---------------------------------------------------------------- expand
+template <typename Tin, typename Ty>
+__global__ void __launch_bounds__(kTcThreads)
+    sgmv_tc_expand_kernel(const __grid_constant__ TCExpandParams P) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t bar_b, bar_v, bar_mma;
+    __shared__ int s_info[4];
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool report = blockIdx.x == 0 && blockIdx.y == 0;
+
+    if (warp == 0) {
+        find_tile(P.seg_ptr, P.idx, P.S, P.T, P.L, kTcRows, P.min_len, P.max_len, P.err,
+                  blockIdx.y, false, report, s_info);
+        if (lane == 0) {
+            mbar_init(&bar_b, 1);
+            mbar_init(&bar_v, 1);
+            mbar_init(&bar_mma, 1);
+            mbar_init_fence();
+        }
+    }
+    __syncthreads();
+    if (s_info[0] < 0) return;
+    const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
+    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)kTcN);
+
+    uint8_t *base = align1024(dsm);
+    const uint32_t tile_bytes = (uint32_t)P.r * 256u;  // [r][128] and [128][r] 16-bit tiles
+    uint8_t *b_tile = base;                  // two N-atoms of [r rows][64 columns]
+    uint8_t *vhi_tile = base + tile_bytes;   // r/64 K-blocks of [128 rows][64]
+    uint8_t *vlo_tile = base + 2 * tile_bytes;
+    const int j0 = (int)blockIdx.x * kTcN;
+
+    if (tid == 0) {  // weights: independent of the previous kernel
+        mbar_arrive_expect_tx(&bar_b, tile_bytes);
+        tma_load_3d(b_tile, &P.tmap_b, j0, 0, a, &bar_b);
+        tma_load_3d(b_tile + P.r * 128, &P.tmap_b, j0 + 64, 0, a, &bar_b);
+    }
+    int row = -1;
+    if (tid < nrows) {
+        row = P.perm ? P.perm[p0 + tid] : p0 + tid;
+        if (row < 0 || row >= P.T) {
+            set_error(P.err, kErrBadIndex);
+            row = -1;
+        }
+    }
+    pdl_wait();
+    if (tid == 0) {  // v of the tile, written by the shrink kernel
+        mbar_arrive_expect_tx(&bar_v, 2 * tile_bytes);
+        for (int kb = 0; kb < P.r / kKB; ++kb) {
+            tma_load_2d(vhi_tile + kb * 16384, &P.tmap_vhi, kb * kKB, p0, &bar_v);
+            tma_load_2d(vlo_tile + kb * 16384, &P.tmap_vlo, kb * kKB, p0, &bar_v);
+        }
+    }
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    bool lost = false;
+    if (tid == 0) {
+        const bool ok = mbar_wait(&bar_b, 0) && mbar_wait(&bar_v, 0);
+        if (!ok) {
+            set_error(P.err, kErrTimeout);
+            mbar_wait(&bar_b, 0);
+            mbar_wait(&bar_v, 0);
+        }
+        tc_fence_after();
+        const uint32_t idesc =
+            idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, kTcN);
+        const uint32_t ba = smem_addr(b_tile);
+        uint32_t acc = 0;
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t va = smem_addr(h ? vlo_tile : vhi_tile);
+            for (int kb = 0; kb < P.r / kKB; ++kb)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_f16(tmem, sw128_desc(va + kb * 16384 + kk * 32, 16, 1024),
+                            sw128_desc(ba + (kb * 4 + kk) * 2048, (uint32_t)P.r * 128, 1024),
+                            idesc, acc);
+                    acc = 1;
+                }
+        }
+        mma_commit(&bar_mma);
+    }
+    if (!mbar_wait(&bar_mma, 0)) {
+        lost = true;
+        set_error(P.err, kErrTimeout);
+        mbar_wait(&bar_mma, 0);
+    }
+    tc_fence_after();
+
+    Ty *yrow = static_cast<Ty *>(P.y) + (size_t)(row < 0 ? 0 : row) * P.H2;
+    for (int c0 = 0; c0 < kTcN; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        if (row >= 0 && !lost) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + c0 + q * 8;
+                if (j < P.H2) {
+                    float y[8];
+                    load8<Ty>(yrow + j, y);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = fmaf(P.scale, v[q * 8 + i], y[i]);
+                    store8<Ty>(yrow + j, y);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, (uint32_t)kTcN);
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap *m, bool bf16, int rank, const void *ptr, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box) {
+    EncodeTiled fn = encoder();
+    if (!fn) return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+              (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K, typename P>
+int launch(K kernel, const P &params, dim3 grid, int cluster, size_t smem, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (cluster > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)cluster;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    return (int)cudaLaunchKernelEx(&cfg, kernel, params);
+}
+
+template <typename Tin, typename Ty>
+int tc_launch_t(const TCArgs &g) {
+    const bool bf16 = std::is_same<Tin, __nv_bfloat16>::value;
+    const size_t es = sizeof(Tin);
+    // -- shrink: CL CTAs split H1 in multiples of 64 columns, each with >= 1 k-block
+    int cl = 8;
+    while (cl > 1 && (g.H1 + kKB - 1) / kKB < cl) cl >>= 1;
+    int hk = (int)(((g.H1 + cl - 1) / cl + kKB - 1) / kKB * kKB);
+    while (cl > 1 && (cl - 1) * hk >= g.H1) {
+        cl >>= 1;
+        hk = (int)(((g.H1 + cl - 1) / cl + kKB - 1) / kKB * kKB);
+    }
+    TCShrinkParams sp;
+    memset(&sp, 0, sizeof sp);
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.r, (cuuint64_t)g.H1, (cuuint64_t)g.L};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.r * es, (cuuint64_t)g.H1 * g.r * es};
+        const cuuint32_t box[3] = {64, 64, 1};
+        if (!encode(&sp.tmap_a, bf16, 3, g.A, dims, strides, box)) return (int)cudaErrorInvalidValue;
+    }
+    sp.x = g.x;
+    sp.perm = g.perm;
+    sp.seg_ptr = g.seg_ptr;
+    sp.idx = g.idx;
+    sp.err = g.err;
+    sp.vhi = g.vhi;
+    sp.vlo = g.vlo;
+    sp.S = g.S;
+    sp.T = g.T;
+    sp.L = g.L;
+    sp.H1 = g.H1;
+    sp.r = g.r;
+    sp.hk = hk;
+    sp.cl = cl;
+    sp.min_len = g.min_len;
+    sp.max_len = g.max_len;
+    const size_t shrink_smem = 1024 + (size_t)kStages * (kTcRows * kKB + kKB * g.r) * es +
+                               (size_t)kTcRows * g.r * 4;
+    int rc = launch(sgmv_tc_shrink_kernel<Tin>, sp, dim3((unsigned)cl, (unsigned)g.slots, 1), cl,
+                    shrink_smem, g.stream);
+    if (rc != 0) return rc;
+
+    // -- expand
+    TCExpandParams ep;
+    memset(&ep, 0, sizeof ep);
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.H2, (cuuint64_t)g.r, (cuuint64_t)g.L};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.H2 * es, (cuuint64_t)g.r * g.H2 * es};
+        const cuuint32_t box[3] = {64, (cuuint32_t)g.r, 1};
+        if (!encode(&ep.tmap_b, bf16, 3, g.B, dims, strides, box)) return (int)cudaErrorInvalidValue;
+        const cuuint64_t vd[2] = {(cuuint64_t)g.r, (cuuint64_t)g.T};
+        const cuuint64_t vs[1] = {(cuuint64_t)g.r * es};
+        const cuuint32_t vb[2] = {64, (cuuint32_t)kTcRows};
+        if (!encode(&ep.tmap_vhi, bf16, 2, g.vhi, vd, vs, vb)) return (int)cudaErrorInvalidValue;
+        if (!encode(&ep.tmap_vlo, bf16, 2, g.vlo, vd, vs, vb)) return (int)cudaErrorInvalidValue;
+    }
+    ep.y = g.y;
+    ep.perm = g.perm;
+    ep.seg_ptr = g.seg_ptr;
+    ep.idx = g.idx;
+    ep.err = g.err;
+    ep.S = g.S;
+    ep.T = g.T;
+    ep.L = g.L;
+    ep.H2 = g.H2;
+    ep.r = g.r;
+    ep.min_len = g.min_len;
+    ep.max_len = g.max_len;
+    ep.scale = g.scale;
+    const size_t expand_smem = 1024 + (size_t)3 * g.r * 256;
+    return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep,
+                  dim3((unsigned)((g.H2 + kTcN - 1) / kTcN), (unsigned)g.slots, 1), 1, expand_smem,
+                  g.stream);
+}
+
+template <typename Tin>
+int tc_launch_in(const TCArgs &g) {
+    switch (g.y_dtype) {
+        case 0: return tc_launch_t<Tin, __half>(g);
+        case 1: return tc_launch_t<Tin, __nv_bfloat16>(g);
+        default: return tc_launch_t<Tin, float>(g);
+    }
+}
+
+}  // namespace
+
+int tc_launch(const TCArgs &g) {
+    return g.in_dtype == 0 ? tc_launch_in<__half>(g) : tc_launch_in<__nv_bfloat16>(g);
+}
+
+}  // namespace sgmv

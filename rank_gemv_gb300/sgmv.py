@@ -30,6 +30,7 @@ _int, _f32, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "sgmv_status_string": (ctypes.c_char_p, [_int]),
     "sgmv_last_error_string": (ctypes.c_char_p, []),
+    "sgmv_last_launch_count": (_int, []),
     "sgmv_max_segments": (_i32, [_i32, _i32]),
     "sgmv_build_segments": (_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
     "sgmv_build_segments_device": (_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -104,6 +105,11 @@ def _host_i32(a):
 
 def sgmv_status_string(status: int) -> str:
     return load_library().sgmv_status_string(status).decode()
+
+
+def sgmv_last_launch_count() -> int:
+    """Kernels launched by this thread's last launching call."""
+    return int(load_library().sgmv_last_launch_count())
 
 
 def sgmv_max_segments(T: int, L: int) -> int:

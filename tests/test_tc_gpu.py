@@ -1,0 +1,145 @@
+"""Tensor-core (tcgen05) path for long segments against the fp64 oracle.
+
+sgmv_apply sends segments of at least 64 rows to the tensor cores when it is
+given a workspace and r is 64 or 128; shorter segments stay on the CUDA-core
+kernel in the same call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rank_gemv_gb300 import workloads as wl
+from tests.gpu_helpers import assert_close, check_error_word, oracle_apply_rows
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+def sg():
+    from rank_gemv_gb300 import sgmv
+
+    return sgmv
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from rank_gemv_gb300 import build
+
+    build.build()
+    sg().load_library()
+    sg().sgmv_get_device_error()
+    yield
+
+
+def workspace(w):
+    n = sg().sgmv_workspace_bytes(w.T, w.H1, w.H2, w.r)
+    return torch.empty(n, dtype=torch.uint8, device=DEV)
+
+
+def run(w, host_meta=False, ws=True):
+    y = w.Y0.to(DEV).clone()
+    X, A, B = w.X.to(DEV), w.A.to(DEV), w.B.to(DEV)
+    if host_meta:
+        perm, seg_ptr, idx = sg().sgmv_build_segments(w.row_adapter, w.L)
+        sg().sgmv_apply(y, X, A, B, seg_ptr.to(DEV), idx.to(DEV), w.scale, perm=perm.to(DEV),
+                        seg_ptr_host=seg_ptr, workspace=workspace(w) if ws else None)
+    else:
+        perm, seg_ptr, idx, _ = sg().sgmv_build_segments_device(w.row_adapter.to(DEV), w.L)
+        sg().sgmv_apply(y, X, A, B, seg_ptr, idx, w.scale, perm=perm,
+                        workspace=workspace(w) if ws else None)
+    return y
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("y_dtype", [torch.float32, torch.bfloat16])
+def test_prefill_workload(seed, y_dtype):
+    w = wl.make("prefill", seed, y_dtype=y_dtype, y0="randn" if seed else "zeros",
+                shuffle_rows=seed == 2)
+    y = run(w)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y, ref, f"prefill seed {seed} y {y_dtype}")
+
+
+@pytest.mark.parametrize("r", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_ranks_and_input_types(r, dtype):
+    lens = [130, 64, 257, 90]
+    ra = torch.arange(4, dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    w = wl.draw(int(sum(lens)), 5, 1024, 1032, r, ra, dtype=dtype, y_dtype=torch.float32,
+                y0="randn", seed=r, scale=0.75)
+    y = run(w)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y, ref, f"r={r} {dtype}")
+
+
+def test_short_and_long_segments_in_one_call():
+    # lengths straddle the 64-row threshold; ids unsorted in storage; one
+    # long segment without an adapter
+    lens = [3, 70, 1, 200, 64, 63, 129, 5, 80]
+    ids = [0, 1, 2, 3, 4, 5, 6, 7, -1]
+    ra = torch.tensor(ids, dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    g = torch.Generator().manual_seed(3)
+    ra = ra[torch.randperm(ra.numel(), generator=g)]
+    w = wl.draw(ra.numel(), 8, 1536, 520, 64, ra, dtype=torch.bfloat16, y_dtype=torch.float32,
+                y0="randn", seed=9, scale=1.5)
+    y_dev = run(w)
+    y_host = run(w, host_meta=True)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y_dev, ref, "device metadata")
+    assert torch.equal(y_dev, y_host)
+    untouched = (ra == -1).nonzero().flatten()
+    assert torch.equal(y_dev[untouched].cpu(), w.Y0[untouched])
+
+
+@pytest.mark.parametrize("H1,H2", [(4104, 11016), (64, 136), (11008, 4096), (192, 8)])
+def test_ragged_dims(H1, H2):
+    lens = [150, 66]
+    ra = torch.tensor([1, 0], dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    w = wl.draw(216, 2, H1, H2, 64, ra, dtype=torch.bfloat16, y_dtype=torch.float32, y0="randn",
+                seed=H1)
+    y = run(w)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y, ref, f"H1={H1} H2={H2}")
+
+
+def test_tensor_and_cuda_core_paths_agree():
+    w = wl.make("prefill", 5, y0="randn")
+    y_tc = run(w, ws=True)
+    y_cc = run(w, ws=False)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y_tc, ref, "tensor cores")
+    assert_close(y_cc, ref, "CUDA cores")
+
+
+def test_bad_adapter_in_long_segment_is_reported():
+    lens = [100, 90]
+    ra = torch.tensor([0, 1], dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    w = wl.draw(190, 2, 512, 256, 64, ra, dtype=torch.bfloat16, y_dtype=torch.float32,
+                y0="randn", seed=4)
+    y = w.Y0.to(DEV).clone()
+    seg_ptr = torch.tensor([0, 100, 190], dtype=torch.int32, device=DEV)
+    idx = torch.tensor([0, 9], dtype=torch.int32, device=DEV)
+    sg().sgmv_apply(y, w.X.to(DEV), w.A.to(DEV), w.B.to(DEV), seg_ptr, idx, w.scale,
+                    workspace=workspace(w))
+    check_error_word(4)
+    assert torch.equal(y[100:].cpu(), w.Y0[100:])
+    ref = oracle.sgmv_apply(w.Y0, w.X, w.A, w.B, [0, 100, 190], [0, -1], w.scale)
+    assert_close(y, ref, "segment before the bad one")
+
+
+def test_workspace_too_small_is_rejected():
+    w = wl.draw(128, 1, 256, 256, 64, torch.zeros(128, dtype=torch.int32),
+                dtype=torch.bfloat16)
+    y = w.Y0.to(DEV)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(sg().SgmvError) as e:
+        sg().sgmv_apply(y, w.X.to(DEV), w.A.to(DEV), w.B.to(DEV),
+                        torch.tensor([0, 128], dtype=torch.int32, device=DEV),
+                        torch.tensor([0], dtype=torch.int32, device=DEV), 1.0, workspace=ws)
+    assert e.value.status == 6
