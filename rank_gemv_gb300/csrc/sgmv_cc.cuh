@@ -174,6 +174,18 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     pdl_trigger();
 
     bool lost = false;  // a bounded wait ran out: write nothing
+    // One thread waits on the mbarrier (waiters that sleep in try_wait wake
+    // late); the others wait at the CTA barrier, which also tells every
+    // thread whether the wait ran out.
+    auto cta_wait = [&](uint64_t *bar, uint32_t par) {
+        int bad = 0;
+        if (tid == 0 && !mbar_wait(bar, par)) {
+            set_error(P.err, kErrTimeout);
+            mbar_wait(bar, par);
+            bad = 1;
+        }
+        if (__syncthreads_or(bad)) lost = true;
+    };
     if (MODE == kExpand) {
         for (int e = tid; e < nrows * P.r; e += kThreads) {
             const int t = e / P.r, k = e - (e / P.r) * P.r;
@@ -197,11 +209,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         for (int i = 0; i < nA; ++i) {
             const int st = i % P.ax_stages;
             const uint32_t par = (uint32_t)((i / P.ax_stages) & 1);
-            if (!mbar_wait(&bars[st], par)) {
-                lost = true;
-                set_error(P.err, kErrTimeout);
-                mbar_wait(&bars[st], par);
-            }
+            cta_wait(&bars[st], par);
             const int hn = min(P.hs, h1 - (h0 + i * P.hs));
             const Tin *As = ax_buf(st);
             const Tin *Xs = As + P.hs * P.r;
@@ -298,42 +306,48 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         }
     }
     __syncthreads();
-    if (y_pref && !mbar_wait(&bars[4], 0)) {
-        lost = true;
-        set_error(P.err, kErrTimeout);
-        mbar_wait(&bars[4], 0);
-    }
+    if (y_pref) cta_wait(&bars[4], 0);
 
     // ---- expand: y[row, j] += scale * v . B[a][:, j] for this CTA's slice ----
+    // Work item = (tile row, 8 consecutive columns); the r-sum of an item is
+    // split over ks neighbouring lanes (ks from the chunk width only, so a
+    // row's result never depends on how many rows share its tile) and summed
+    // by an xor tree.
     for (int i = 0; i < nB; ++i) {
         const int st = i % P.b_stages;
-        const uint32_t par = (uint32_t)((i / P.b_stages) & 1);
-        if (!mbar_wait(&bars[2 + st], par)) {
-            lost = true;
-            set_error(P.err, kErrTimeout);
-            mbar_wait(&bars[2 + st], par);
-        }
+        cta_wait(&bars[2 + st], (uint32_t)((i / P.b_stages) & 1));
         const int jlo = j0 + i * P.js;
         const int ncv = min(P.js, j1 - jlo) >> 3;
+        int ks = 1;
+        while (ks < 8 && ncv * ks * 2 <= kThreads) ks <<= 1;
+        const int items = nrows * ncv * ks;
+        const int span = (items + 31) & ~31;  // whole warps take part in the shuffles
         const Tin *Bs = b_buf(st);
-        if (!lost) {
-            for (int w = tid; w < nrows * ncv; w += kThreads) {
-                const int t = w / ncv;
-                const int cv = w - t * ncv;
-                const int row = s_row[t];
-                if (row < 0) continue;
-                float acc8[8];
+        for (int w = tid; w < span; w += kThreads) {
+            const bool live = w < items;
+            const int item = live ? w / ks : 0;
+            const int part = w & (ks - 1);
+            const int t = item / ncv;
+            const int cv = item - t * ncv;
+            float acc8[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc8[q] = 0.f;
+            for (int q = 0; q < 8; ++q) acc8[q] = 0.f;
+            if (live) {
                 const float *vt = s_v + t * RMAX;
-#pragma unroll 8
-                for (int kk = 0; kk < P.r; ++kk) {
+#pragma unroll 4
+                for (int kk = part; kk < P.r; kk += ks) {
                     const float vk = vt[kk];
                     float bf[8];
                     unpack8<Tin>(*reinterpret_cast<const uint4 *>(Bs + kk * P.js + cv * 8), bf);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) acc8[q] = fmaf(vk, bf[q], acc8[q]);
                 }
+            }
+            for (int off = 1; off < ks; off <<= 1)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc8[q] += __shfl_xor_sync(0xffffffffu, acc8[q], off);
+            const int row = live ? s_row[t] : -1;
+            if (part == 0 && row >= 0 && !lost) {
                 Ty *yp = gY + (size_t)row * P.H2 + jlo + cv * 8;
                 float yv[8];
                 if (y_pref)

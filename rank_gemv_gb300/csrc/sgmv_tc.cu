@@ -274,20 +274,29 @@ __global__ void __launch_bounds__(kTcThreads)
             mma_commit(&empty[st]);
         }
         if (kb + kStages < nkb) {
-            if (!mbar_wait(&empty[st], ph)) {
-                lost = true;
+            // one waiter, then the CTA barrier (sleeping waiters wake late)
+            int bad = 0;
+            if (tid == 0 && !mbar_wait(&empty[st], ph)) {
                 set_error(P.err, kErrTimeout);
                 mbar_wait(&empty[st], ph);
+                bad = 1;
             }
+            if (__syncthreads_or(bad)) lost = true;
             if (tid == 0) issue_a(kb + kStages);
             issue_x(kb + kStages);
         }
     }
-    if (tid == 0) mma_commit(&done);
-    if (!mbar_wait(&done, 0)) {
-        lost = true;
-        set_error(P.err, kErrTimeout);
-        mbar_wait(&done, 0);
+    {
+        int bad = 0;
+        if (tid == 0) {
+            mma_commit(&done);
+            if (!mbar_wait(&done, 0)) {
+                set_error(P.err, kErrTimeout);
+                mbar_wait(&done, 0);
+                bad = 1;
+            }
+        }
+        if (__syncthreads_or(bad)) lost = true;
     }
     tc_fence_after();
 
@@ -423,10 +432,14 @@ __global__ void __launch_bounds__(kTcThreads)
         }
         mma_commit(&bar_mma);
     }
-    if (!mbar_wait(&bar_mma, 0)) {
-        lost = true;
-        set_error(P.err, kErrTimeout);
-        mbar_wait(&bar_mma, 0);
+    {
+        int bad = 0;
+        if (tid == 0 && !mbar_wait(&bar_mma, 0)) {
+            set_error(P.err, kErrTimeout);
+            mbar_wait(&bar_mma, 0);
+            bad = 1;
+        }
+        if (__syncthreads_or(bad)) lost = true;
     }
     tc_fence_after();
 
