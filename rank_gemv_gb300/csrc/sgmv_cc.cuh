@@ -32,6 +32,26 @@ namespace sgmv {
 
 template <typename Tin, typename Ty, int RMAX, int MODE>
 __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant__ CCParams P) {
+    // Kernel parameters, read once into registers: touching the parameter
+    // struct inside loops or lambdas makes the compiler address it in memory
+    // and reload its fields on every use.
+    const int nseg = P.S, nrows_all = P.T, nadapters = P.L, H1 = P.H1, H2 = P.H2, rk = P.r;
+    const int tile_rows = P.rows, hc = P.hc, jc = P.jc, hs = P.hs, js = P.js;
+    const int ax_stages = P.ax_stages, b_stages = P.b_stages, ncl = P.cl;
+    const int min_len = P.min_len, max_len = P.max_len, y_pref_on = P.y_pref;
+    const float scale = P.scale;
+    int *const err = P.err;
+    const int32_t *const perm = P.perm;
+    const int32_t *const seg_ptr = P.seg_ptr;
+    const int32_t *const idx = P.idx;
+    const float *const v_in = P.v_in;
+    float *const v_out = P.v_out;
+    const void *const xptr = P.x;
+    const void *const Aptr = P.A;
+    const void *const Bptr = P.B;
+    void *const yptr = P.y;
+    const CCSmem lay = cc_smem_layout(P, (int)sizeof(Tin), MODE);
+
     extern __shared__ __align__(128) uint8_t dsmem[];
     // 0,1: (A, X) stages, two arrivals each (A, then X); 2,3: B stages; 4: y rows
     __shared__ __align__(8) uint64_t bars[5];
@@ -45,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
     if (tid < 32) {
-        find_tile(P.seg_ptr, P.idx, P.S, P.T, P.L, P.rows, P.min_len, P.max_len, P.err,
+        find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, tile_rows, min_len, max_len, err,
                   blockIdx.y, MODE == kShrink, report, s_info);
         if (tid == 0) {
             mbar_init(&bars[0], 2);
@@ -66,32 +86,31 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         pdl_wait();
         pdl_trigger();
         if (blockIdx.x == 0)
-            for (int e = tid; e < nrows * P.r; e += kThreads)
-                P.v_out[(size_t)(p0 + e / P.r) * P.r + e % P.r] = 0.f;
+            for (int e = tid; e < nrows * rk; e += kThreads)
+                v_out[(size_t)(p0 + e / rk) * rk + e % rk] = 0.f;
         return;
     }
-    const bool clustered = MODE != kExpand && P.cl > 1;
+    const bool clustered = MODE != kExpand && ncl > 1;
     if (clustered) cluster_arrive_relaxed();  // waited on just before the first peer access
 
-    const CCSmem lay = cc_smem_layout(P, (int)sizeof(Tin), MODE);
-    const Tin *gA = static_cast<const Tin *>(P.A);
-    const Tin *gB = static_cast<const Tin *>(P.B);
-    const Tin *gX = static_cast<const Tin *>(P.x);
-    Ty *gY = static_cast<Ty *>(P.y);
+    const Tin *gA = static_cast<const Tin *>(Aptr);
+    const Tin *gB = static_cast<const Tin *>(Bptr);
+    const Tin *gX = static_cast<const Tin *>(xptr);
+    Ty *gY = static_cast<Ty *>(yptr);
 
     // Slices owned by this CTA.
     int h0 = 0, h1 = 0, j0 = 0, j1 = 0;
     if (MODE != kExpand) {
-        h0 = min(P.H1, (int)blockIdx.x * P.hc);
-        h1 = min(P.H1, h0 + P.hc);
+        h0 = min(H1, (int)blockIdx.x * hc);
+        h1 = min(H1, h0 + hc);
     }
     if (MODE != kShrink) {
-        j0 = min(P.H2, (int)blockIdx.x * P.jc);
-        j1 = min(P.H2, j0 + P.jc);
+        j0 = min(H2, (int)blockIdx.x * jc);
+        j1 = min(H2, j0 + jc);
     }
-    const int nA = (MODE != kExpand && h1 > h0) ? (h1 - h0 + P.hs - 1) / P.hs : 0;
-    const int nB = (MODE != kShrink && j1 > j0) ? (j1 - j0 + P.js - 1) / P.js : 0;
-    const bool y_pref = MODE != kShrink && P.y_pref && nB > 0;
+    const int nA = (MODE != kExpand && h1 > h0) ? (h1 - h0 + hs - 1) / hs : 0;
+    const int nB = (MODE != kShrink && j1 > j0) ? (j1 - j0 + js - 1) / js : 0;
+    const bool y_pref = MODE != kShrink && y_pref_on && nB > 0;
 
     auto ax_buf = [&](int st) {
         return reinterpret_cast<Tin *>(dsmem + lay.ax_off + st * lay.ax_stage_bytes);
@@ -104,33 +123,33 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
 
     // Chunk i of A: first of the two arrivals on its stage barrier.
     auto issue_a = [&](int i) {  // lane 0 of warp 0
-        const int st = i % P.ax_stages;
-        const int hlo = h0 + i * P.hs;
-        const int hn = min(P.hs, h1 - hlo);
-        const uint32_t ab = (uint32_t)(hn * P.r) * sizeof(Tin);
+        const int st = i % ax_stages;
+        const int hlo = h0 + i * hs;
+        const int hn = min(hs, h1 - hlo);
+        const uint32_t ab = (uint32_t)(hn * rk) * sizeof(Tin);
         mbar_arrive_expect_tx(&bars[st], ab);
-        bulk_g2s(ax_buf(st), gA + ((size_t)a * P.H1 + hlo) * P.r, ab, &bars[st]);
+        bulk_g2s(ax_buf(st), gA + ((size_t)a * H1 + hlo) * rk, ab, &bars[st]);
     };
     // Chunk i of the tile's X rows: second arrival.  Needs s_row and nvalid.
     auto issue_x = [&](int i, int nvalid) {  // all lanes of warp 0
-        const int st = i % P.ax_stages;
-        const int hlo = h0 + i * P.hs;
-        const int hn = min(P.hs, h1 - hlo);
+        const int st = i % ax_stages;
+        const int hlo = h0 + i * hs;
+        const int hn = min(hs, h1 - hlo);
         if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)(nvalid * hn) * sizeof(Tin));
         __syncwarp();
-        Tin *xs = ax_buf(st) + P.hs * P.r;
+        Tin *xs = ax_buf(st) + hs * rk;
         if (lane < nrows && s_row[lane] >= 0)
-            bulk_g2s(xs + lane * P.hs, gX + (size_t)s_row[lane] * P.H1 + hlo,
+            bulk_g2s(xs + lane * hs, gX + (size_t)s_row[lane] * H1 + hlo,
                      (uint32_t)hn * sizeof(Tin), &bars[st]);
     };
     auto issue_b = [&](int i) {  // all lanes of warp 0
-        const int st = i % P.b_stages;
-        const int jlo = j0 + i * P.js;
-        const int jn = min(P.js, j1 - jlo);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[2 + st], (uint32_t)(P.r * jn) * sizeof(Tin));
+        const int st = i % b_stages;
+        const int jlo = j0 + i * js;
+        const int jn = min(js, j1 - jlo);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[2 + st], (uint32_t)(rk * jn) * sizeof(Tin));
         __syncwarp();
-        for (int k = lane; k < P.r; k += 32)
-            bulk_g2s(b_buf(st) + k * P.js, gB + ((size_t)a * P.r + k) * P.H2 + jlo,
+        for (int k = lane; k < rk; k += 32)
+            bulk_g2s(b_buf(st) + k * js, gB + ((size_t)a * rk + k) * H2 + jlo,
                      (uint32_t)jn * sizeof(Tin), &bars[2 + st]);
     };
 
@@ -138,14 +157,14 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     // and nothing waits for the row permutation before they are requested.
     if (tid < 32) {
         if (lane == 0)
-            for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_a(i);
-        for (int i = 0; i < min(nB, P.b_stages); ++i) issue_b(i);
+            for (int i = 0; i < min(nA, ax_stages); ++i) issue_a(i);
+        for (int i = 0; i < min(nB, b_stages); ++i) issue_b(i);
     } else if (tid < 32 + nrows) {
         // Physical rows of the tile; invalid perm entries are skipped and reported.
         const int t = tid - 32;
-        int row = P.perm ? P.perm[p0 + t] : p0 + t;
-        if (row < 0 || row >= P.T) {
-            set_error(P.err, kErrBadIndex);
+        int row = perm ? perm[p0 + t] : p0 + t;
+        if (row < 0 || row >= nrows_all) {
+            set_error(err, kErrBadIndex);
             row = -1;
         }
         s_row[t] = row;
@@ -162,13 +181,13 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         }
     // Activations and outputs: only after the previous kernel has finished.
     if (tid < 32) {
-        for (int i = 0; i < min(nA, P.ax_stages); ++i) issue_x(i, nvalid);
+        for (int i = 0; i < min(nA, ax_stages); ++i) issue_x(i, nvalid);
         if (y_pref) {
             const uint32_t yb = (uint32_t)(j1 - j0) * sizeof(Ty);
             if (lane == 0) mbar_arrive_expect_tx(&bars[4], yb * nvalid);
             __syncwarp();
             if (lane < nrows && s_row[lane] >= 0)
-                bulk_g2s(ybuf + lane * P.jc, gY + (size_t)s_row[lane] * P.H2 + j0, yb, &bars[4]);
+                bulk_g2s(ybuf + lane * jc, gY + (size_t)s_row[lane] * H2 + j0, yb, &bars[4]);
         }
     }
     pdl_trigger();
@@ -180,16 +199,16 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     auto cta_wait = [&](uint64_t *bar, uint32_t par) {
         int bad = 0;
         if (tid == 0 && !mbar_wait(bar, par)) {
-            set_error(P.err, kErrTimeout);
+            set_error(err, kErrTimeout);
             mbar_wait(bar, par);
             bad = 1;
         }
         if (__syncthreads_or(bad)) lost = true;
     };
     if (MODE == kExpand) {
-        for (int e = tid; e < nrows * P.r; e += kThreads) {
-            const int t = e / P.r, k = e - (e / P.r) * P.r;
-            s_v[t * RMAX + k] = P.v_in[(size_t)(p0 + t) * P.r + k];
+        for (int e = tid; e < nrows * rk; e += kThreads) {
+            const int t = e / rk, k = e - (e / rk) * rk;
+            s_v[t * RMAX + k] = v_in[(size_t)(p0 + t) * rk + k];
         }
     } else {
         // ---- shrink: partial v over this CTA's H1 slice -----------------
@@ -202,17 +221,17 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         const int kg = tid / HG, hg = tid - (tid / HG) * HG;
         const int kbase = kg * 16;
         const int wig = hg >> 5;             // warp within the k-group
-        const bool kact = kbase < P.r;       // same for the whole warp
-        const bool vec = (P.r & 7) == 0;     // A rows are 16-byte aligned in smem
+        const bool kact = kbase < rk;       // same for the whole warp
+        const bool vec = (rk & 7) == 0;     // A rows are 16-byte aligned in smem
         for (int e = tid; e < kRowsMax * RMAX * WPG; e += kThreads) s_red[e] = 0.f;
         __syncthreads();
         for (int i = 0; i < nA; ++i) {
-            const int st = i % P.ax_stages;
-            const uint32_t par = (uint32_t)((i / P.ax_stages) & 1);
+            const int st = i % ax_stages;
+            const uint32_t par = (uint32_t)((i / ax_stages) & 1);
             cta_wait(&bars[st], par);
-            const int hn = min(P.hs, h1 - (h0 + i * P.hs));
+            const int hn = min(hs, h1 - (h0 + i * hs));
             const Tin *As = ax_buf(st);
-            const Tin *Xs = As + P.hs * P.r;
+            const Tin *Xs = As + hs * rk;
             if (kact) {
                 for (int t = 0; t < nrows; ++t) {
                     if (!(vmask & (1u << t))) continue;
@@ -220,9 +239,9 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
                     for (int h = hg; h < hn; h += HG) {
-                        const float x = to_f<Tin>(Xs[t * P.hs + h]);
+                        const float x = to_f<Tin>(Xs[t * hs + h]);
                         float av[16];
-                        const Tin *arow = As + h * P.r + kbase;
+                        const Tin *arow = As + h * rk + kbase;
                         if (vec) {
                             float lo[8], hi[8];
                             unpack8<Tin>(*reinterpret_cast<const uint4 *>(arow), lo);
@@ -235,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                         } else {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                av[j] = kbase + j < P.r ? to_f<Tin>(arow[j]) : 0.f;
+                                av[j] = kbase + j < rk ? to_f<Tin>(arow[j]) : 0.f;
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc[j] = fmaf(x, av[j], acc[j]);
@@ -257,10 +276,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 }
             }
             __syncthreads();
-            if (tid < 32 && i + P.ax_stages < nA) {
-                if (lane == 0) issue_a(i + P.ax_stages);
+            if (tid < 32 && i + ax_stages < nA) {
+                if (lane == 0) issue_a(i + ax_stages);
                 __syncwarp();
-                issue_x(i + P.ax_stages, nvalid);
+                issue_x(i + ax_stages, nvalid);
             }
         }
         // This CTA's partial of v[t][k]: the warps of the k-group summed in order.
@@ -275,32 +294,32 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             // then sum the slots locally in rank order: the same bits in every
             // CTA, one cluster barrier, no remote loads.
             const int rank = (int)blockIdx.x;
-            const int per = nrows * P.r;
+            const int per = nrows * rk;
             cluster_wait();
-            for (int e = tid; e < P.cl * per; e += kThreads) {
+            for (int e = tid; e < ncl * per; e += kThreads) {
                 const int c = e / per, rem = e - (e / per) * per;
-                const int t = rem / P.r, kk = rem - (rem / P.r) * P.r;
+                const int t = rem / rk, kk = rem - (rem / rk) * rk;
                 st_peer(peer_addr(&recv[(rank * kRowsMax + t) * RMAX + kk], (uint32_t)c),
                         partial(t, kk));
             }
             cluster_sync();
             for (int e = tid; e < per; e += kThreads) {
-                const int t = e / P.r, kk = e - (e / P.r) * P.r;
+                const int t = e / rk, kk = e - (e / rk) * rk;
                 float s = 0.f;
-                for (int c = 0; c < P.cl; ++c) s += recv[(c * kRowsMax + t) * RMAX + kk];
+                for (int c = 0; c < ncl; ++c) s += recv[(c * kRowsMax + t) * RMAX + kk];
                 s_v[t * RMAX + kk] = s;
             }
         } else {
-            for (int e = tid; e < nrows * P.r; e += kThreads) {
-                const int t = e / P.r, kk = e - (e / P.r) * P.r;
+            for (int e = tid; e < nrows * rk; e += kThreads) {
+                const int t = e / rk, kk = e - (e / rk) * rk;
                 s_v[t * RMAX + kk] = partial(t, kk);
             }
         }
         if (MODE == kShrink) {
             if (blockIdx.x == 0 && !lost)
-                for (int e = tid; e < nrows * P.r; e += kThreads) {
-                    const int t = e / P.r, kk = e - (e / P.r) * P.r;
-                    P.v_out[(size_t)(p0 + t) * P.r + kk] = s_v[t * RMAX + kk];
+                for (int e = tid; e < nrows * rk; e += kThreads) {
+                    const int t = e / rk, kk = e - (e / rk) * rk;
+                    v_out[(size_t)(p0 + t) * rk + kk] = s_v[t * RMAX + kk];
                 }
             return;
         }
@@ -314,10 +333,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     // row's result never depends on how many rows share its tile) and summed
     // by an xor tree.
     for (int i = 0; i < nB; ++i) {
-        const int st = i % P.b_stages;
-        cta_wait(&bars[2 + st], (uint32_t)((i / P.b_stages) & 1));
-        const int jlo = j0 + i * P.js;
-        const int ncv = min(P.js, j1 - jlo) >> 3;
+        const int st = i % b_stages;
+        cta_wait(&bars[2 + st], (uint32_t)((i / b_stages) & 1));
+        const int jlo = j0 + i * js;
+        const int ncv = min(js, j1 - jlo) >> 3;
         int ks = 1;
         while (ks < 8 && ncv * ks * 2 <= kThreads) ks <<= 1;
         const int items = nrows * ncv * ks;
@@ -335,10 +354,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             if (live) {
                 const float *vt = s_v + t * RMAX;
 #pragma unroll 4
-                for (int kk = part; kk < P.r; kk += ks) {
+                for (int kk = part; kk < rk; kk += ks) {
                     const float vk = vt[kk];
                     float bf[8];
-                    unpack8<Tin>(*reinterpret_cast<const uint4 *>(Bs + kk * P.js + cv * 8), bf);
+                    unpack8<Tin>(*reinterpret_cast<const uint4 *>(Bs + kk * js + cv * 8), bf);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) acc8[q] = fmaf(vk, bf[q], acc8[q]);
                 }
@@ -348,19 +367,19 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 for (int q = 0; q < 8; ++q) acc8[q] += __shfl_xor_sync(0xffffffffu, acc8[q], off);
             const int row = live ? s_row[t] : -1;
             if (part == 0 && row >= 0 && !lost) {
-                Ty *yp = gY + (size_t)row * P.H2 + jlo + cv * 8;
+                Ty *yp = gY + (size_t)row * H2 + jlo + cv * 8;
                 float yv[8];
                 if (y_pref)
-                    load8<Ty>(ybuf + t * P.jc + (jlo - j0) + cv * 8, yv);
+                    load8<Ty>(ybuf + t * jc + (jlo - j0) + cv * 8, yv);
                 else
                     load8<Ty>(yp, yv);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) yv[q] = fmaf(P.scale, acc8[q], yv[q]);
+                for (int q = 0; q < 8; ++q) yv[q] = fmaf(scale, acc8[q], yv[q]);
                 store8<Ty>(yp, yv);
             }
         }
         __syncthreads();
-        if (tid < 32 && i + P.b_stages < nB) issue_b(i + P.b_stages);
+        if (tid < 32 && i + b_stages < nB) issue_b(i + b_stages);
     }
 }
 

@@ -175,6 +175,19 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 template <typename Tin>
 __global__ void __launch_bounds__(kTcThreads)
     sgmv_tc_shrink_kernel(const __grid_constant__ TCShrinkParams P) {
+    // Parameters read once into registers (see the CUDA-core kernel); the
+    // tensor map stays in the parameter buffer, where TMA reads it.
+    const int32_t *const seg_ptr = P.seg_ptr;
+    const int32_t *const idx = P.idx;
+    const int32_t *const perm = P.perm;
+    int *const err = P.err;
+    const int nseg = P.S, nrows_all = P.T, nadapters = P.L, min_len = P.min_len,
+              max_len = P.max_len, ncl = P.cl, rk = P.r, hk = P.hk, H1 = P.H1;
+    const void *const xptr = P.x;
+    void *const vhi_ptr = P.vhi;
+    void *const vlo_ptr = P.vlo;
+    const CUtensorMap *const tmap_a = &P.tmap_a;
+
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
     __shared__ int s_info[4];
@@ -183,7 +196,7 @@ __global__ void __launch_bounds__(kTcThreads)
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
     if (warp == 0) {
-        find_tile(P.seg_ptr, P.idx, P.S, P.T, P.L, kTcRows, P.min_len, P.max_len, P.err,
+        find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, min_len, max_len, err,
                   blockIdx.y, false, report, s_info);
         if (lane == 0) {
             for (int s = 0; s < kStages; ++s) {
@@ -197,27 +210,27 @@ __global__ void __launch_bounds__(kTcThreads)
     __syncthreads();
     if (s_info[0] < 0) return;  // same decision in every CTA of the cluster
     const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
-    const bool clustered = P.cl > 1;
+    const bool clustered = ncl > 1;
     if (clustered) cluster_arrive_relaxed();
-    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)P.r);
+    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)rk);
 
     uint8_t *base = align1024(dsm);
     const uint32_t x_bytes = kTcRows * kKB * sizeof(Tin);  // 16 KB
-    const uint32_t a_bytes = kKB * P.r * sizeof(Tin);       // 8 or 16 KB
+    const uint32_t a_bytes = kKB * rk * sizeof(Tin);       // 8 or 16 KB
     auto stage_x = [&](int st) { return base + st * (x_bytes + a_bytes); };
     auto stage_a = [&](int st) { return base + st * (x_bytes + a_bytes) + x_bytes; };
     float *recv = reinterpret_cast<float *>(base + kStages * (x_bytes + a_bytes));
-    const Tin *gX = static_cast<const Tin *>(P.x);
+    const Tin *gX = static_cast<const Tin *>(xptr);
 
-    const int k0 = (int)blockIdx.x * P.hk;
-    const int k1 = min(P.H1, k0 + P.hk);
+    const int k0 = (int)blockIdx.x * hk;
+    const int k1 = min(H1, k0 + hk);
     const int nkb = k1 > k0 ? (k1 - k0 + kKB - 1) / kKB : 0;
 
     auto issue_a = [&](int kb) {  // thread 0
         const int st = kb % kStages;
         mbar_arrive_expect_tx(&full[st], a_bytes);
-        for (int c = 0; c < P.r; c += 64)
-            tma_load_3d(stage_a(st) + c * kKB * sizeof(Tin), &P.tmap_a, c, k0 + kb * kKB, a,
+        for (int c = 0; c < rk; c += 64)
+            tma_load_3d(stage_a(st) + c * kKB * sizeof(Tin), tmap_a, c, k0 + kb * kKB, a,
                         &full[st]);
     };
     if (tid == 0)
@@ -226,9 +239,9 @@ __global__ void __launch_bounds__(kTcThreads)
     // Physical row of this thread's tile row (metadata is complete before launch).
     int row = -1;
     if (tid < nrows) {
-        row = P.perm ? P.perm[p0 + tid] : p0 + tid;
-        if (row < 0 || row >= P.T) {
-            set_error(P.err, kErrBadIndex);
+        row = perm ? perm[p0 + tid] : p0 + tid;
+        if (row < 0 || row >= nrows_all) {
+            set_error(err, kErrBadIndex);
             row = -1;
         }
     }
@@ -240,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads)
         for (int c = 0; c < 8; ++c) {
             const int k = kk0 + c * 8;
             const bool ok = row >= 0 && k < k1;
-            cp_async16(xs + sw128_offset(tid, c), ok ? gX + (size_t)row * P.H1 + k : gX,
+            cp_async16(xs + sw128_offset(tid, c), ok ? gX + (size_t)row * H1 + k : gX,
                        ok ? 16u : 0u);
         }
         cp_async_arrive(&full[st]);
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(kTcThreads)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, P.r);
+    const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, rk);
     bool lost = false;
     for (int kb = 0; kb < nkb; ++kb) {
         const int st = kb % kStages;
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads)
         if (tid == 0) {
             if (!mbar_wait(&full[st], ph)) {
                 lost = true;
-                set_error(P.err, kErrTimeout);
+                set_error(err, kErrTimeout);
                 mbar_wait(&full[st], ph);
             }
             fence_proxy_async();  // cp.async (generic proxy) data -> tensor core (async proxy)
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(kTcThreads)
             // one waiter, then the CTA barrier (sleeping waiters wake late)
             int bad = 0;
             if (tid == 0 && !mbar_wait(&empty[st], ph)) {
-                set_error(P.err, kErrTimeout);
+                set_error(err, kErrTimeout);
                 mbar_wait(&empty[st], ph);
                 bad = 1;
             }
@@ -291,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads)
         if (tid == 0) {
             mma_commit(&done);
             if (!mbar_wait(&done, 0)) {
-                set_error(P.err, kErrTimeout);
+                set_error(err, kErrTimeout);
                 mbar_wait(&done, 0);
                 bad = 1;
             }
@@ -301,10 +314,10 @@ __global__ void __launch_bounds__(kTcThreads)
     tc_fence_after();
 
     // Partial v of this CTA's H1 slice -> the CTA that owns the row.
-    const int rpc = kTcRows / P.cl;  // rows summed by each CTA of the cluster
+    const int rpc = kTcRows / ncl;  // rows summed by each CTA of the cluster
     const int rank = (int)blockIdx.x;
     if (clustered) cluster_wait();
-    for (int c0 = 0; c0 < P.r; c0 += 32) {
+    for (int c0 = 0; c0 < rk; c0 += 32) {
         float v[32];
         if (nkb > 0) {
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
@@ -314,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads)
         }
         if (tid < nrows) {
             const int owner = tid / rpc, mr = tid - (tid / rpc) * rpc;
-            float *dst = recv + (size_t)(rank * rpc + mr) * P.r + c0;
+            float *dst = recv + (size_t)(rank * rpc + mr) * rk + c0;
             if (clustered) {
                 const uint32_t pa = peer_addr(dst, (uint32_t)owner);
 #pragma unroll
@@ -329,28 +342,40 @@ __global__ void __launch_bounds__(kTcThreads)
         cluster_sync();
     else
         __syncthreads();
-    Tin *vhi = static_cast<Tin *>(P.vhi);
-    Tin *vlo = static_cast<Tin *>(P.vlo);
-    for (int e = tid; e < rpc * P.r; e += kTcThreads) {
-        const int mr = e / P.r, col = e - (e / P.r) * P.r;
+    Tin *vhi = static_cast<Tin *>(vhi_ptr);
+    Tin *vlo = static_cast<Tin *>(vlo_ptr);
+    for (int e = tid; e < rpc * rk; e += kTcThreads) {
+        const int mr = e / rk, col = e - (e / rk) * rk;
         const int m = rank * rpc + mr;
         if (m >= nrows || lost) continue;
         float s = 0.f;
-        for (int c = 0; c < P.cl; ++c) s += recv[(size_t)(c * rpc + mr) * P.r + col];
+        for (int c = 0; c < ncl; ++c) s += recv[(size_t)(c * rpc + mr) * rk + col];
         const Tin hi = from_f<Tin>(s);
-        const size_t o = (size_t)(p0 + m) * P.r + col;
+        const size_t o = (size_t)(p0 + m) * rk + col;
         vhi[o] = hi;
         vlo[o] = from_f<Tin>(s - to_f<Tin>(hi));
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, (uint32_t)P.r);
+    if (warp == 0) tmem_dealloc(tmem, (uint32_t)rk);
 }
 
 // ---------------------------------------------------------------- expand
 template <typename Tin, typename Ty>
 __global__ void __launch_bounds__(kTcThreads)
     sgmv_tc_expand_kernel(const __grid_constant__ TCExpandParams P) {
+    const int32_t *const seg_ptr = P.seg_ptr;
+    const int32_t *const idx = P.idx;
+    const int32_t *const perm = P.perm;
+    int *const err = P.err;
+    const int nseg = P.S, nrows_all = P.T, nadapters = P.L, min_len = P.min_len,
+              max_len = P.max_len, rk = P.r, H2 = P.H2;
+    const float scale = P.scale;
+    void *const yptr = P.y;
+    const CUtensorMap *const tmap_b = &P.tmap_b;
+    const CUtensorMap *const tmap_vhi = &P.tmap_vhi;
+    const CUtensorMap *const tmap_vlo = &P.tmap_vlo;
+
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t bar_b, bar_v, bar_mma;
     __shared__ int s_info[4];
@@ -359,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads)
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
     if (warp == 0) {
-        find_tile(P.seg_ptr, P.idx, P.S, P.T, P.L, kTcRows, P.min_len, P.max_len, P.err,
+        find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, min_len, max_len, err,
                   blockIdx.y, false, report, s_info);
         if (lane == 0) {
             mbar_init(&bar_b, 1);
@@ -374,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads)
     if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)kTcN);
 
     uint8_t *base = align1024(dsm);
-    const uint32_t tile_bytes = (uint32_t)P.r * 256u;  // [r][128] and [128][r] 16-bit tiles
+    const uint32_t tile_bytes = (uint32_t)rk * 256u;  // [r][128] and [128][r] 16-bit tiles
     uint8_t *b_tile = base;                  // two N-atoms of [r rows][64 columns]
     uint8_t *vhi_tile = base + tile_bytes;   // r/64 K-blocks of [128 rows][64]
     uint8_t *vlo_tile = base + 2 * tile_bytes;
@@ -382,23 +407,23 @@ __global__ void __launch_bounds__(kTcThreads)
 
     if (tid == 0) {  // weights: independent of the previous kernel
         mbar_arrive_expect_tx(&bar_b, tile_bytes);
-        tma_load_3d(b_tile, &P.tmap_b, j0, 0, a, &bar_b);
-        tma_load_3d(b_tile + P.r * 128, &P.tmap_b, j0 + 64, 0, a, &bar_b);
+        tma_load_3d(b_tile, tmap_b, j0, 0, a, &bar_b);
+        tma_load_3d(b_tile + rk * 128, tmap_b, j0 + 64, 0, a, &bar_b);
     }
     int row = -1;
     if (tid < nrows) {
-        row = P.perm ? P.perm[p0 + tid] : p0 + tid;
-        if (row < 0 || row >= P.T) {
-            set_error(P.err, kErrBadIndex);
+        row = perm ? perm[p0 + tid] : p0 + tid;
+        if (row < 0 || row >= nrows_all) {
+            set_error(err, kErrBadIndex);
             row = -1;
         }
     }
     pdl_wait();
     if (tid == 0) {  // v of the tile, written by the shrink kernel
         mbar_arrive_expect_tx(&bar_v, 2 * tile_bytes);
-        for (int kb = 0; kb < P.r / kKB; ++kb) {
-            tma_load_2d(vhi_tile + kb * 16384, &P.tmap_vhi, kb * kKB, p0, &bar_v);
-            tma_load_2d(vlo_tile + kb * 16384, &P.tmap_vlo, kb * kKB, p0, &bar_v);
+        for (int kb = 0; kb < rk / kKB; ++kb) {
+            tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, p0, &bar_v);
+            tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, p0, &bar_v);
         }
     }
     pdl_trigger();
@@ -410,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads)
     if (tid == 0) {
         const bool ok = mbar_wait(&bar_b, 0) && mbar_wait(&bar_v, 0);
         if (!ok) {
-            set_error(P.err, kErrTimeout);
+            set_error(err, kErrTimeout);
             mbar_wait(&bar_b, 0);
             mbar_wait(&bar_v, 0);
         }
@@ -421,11 +446,11 @@ __global__ void __launch_bounds__(kTcThreads)
         uint32_t acc = 0;
         for (int h = 0; h < 2; ++h) {
             const uint32_t va = smem_addr(h ? vlo_tile : vhi_tile);
-            for (int kb = 0; kb < P.r / kKB; ++kb)
+            for (int kb = 0; kb < rk / kKB; ++kb)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     mma_f16(tmem, sw128_desc(va + kb * 16384 + kk * 32, 16, 1024),
-                            sw128_desc(ba + (kb * 4 + kk) * 2048, (uint32_t)P.r * 128, 1024),
+                            sw128_desc(ba + (kb * 4 + kk) * 2048, (uint32_t)rk * 128, 1024),
                             idesc, acc);
                     acc = 1;
                 }
@@ -435,7 +460,7 @@ __global__ void __launch_bounds__(kTcThreads)
     {
         int bad = 0;
         if (tid == 0 && !mbar_wait(&bar_mma, 0)) {
-            set_error(P.err, kErrTimeout);
+            set_error(err, kErrTimeout);
             mbar_wait(&bar_mma, 0);
             bad = 1;
         }
@@ -443,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads)
     }
     tc_fence_after();
 
-    Ty *yrow = static_cast<Ty *>(P.y) + (size_t)(row < 0 ? 0 : row) * P.H2;
+    Ty *yrow = static_cast<Ty *>(yptr) + (size_t)(row < 0 ? 0 : row) * H2;
     for (int c0 = 0; c0 < kTcN; c0 += 32) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
@@ -451,11 +476,11 @@ __global__ void __launch_bounds__(kTcThreads)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = j0 + c0 + q * 8;
-                if (j < P.H2) {
+                if (j < H2) {
                     float y[8];
                     load8<Ty>(yrow + j, y);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = fmaf(P.scale, v[q * 8 + i], y[i]);
+                    for (int i = 0; i < 8; ++i) y[i] = fmaf(scale, v[q * 8 + i], y[i]);
                     store8<Ty>(yrow + j, y);
                 }
             }
