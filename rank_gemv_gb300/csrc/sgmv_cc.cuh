@@ -239,13 +239,14 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
                     for (int h = hg; h < hn; h += HG) {
-                        const float x = to_f<Tin>(Xs[t * hs + h]);
+                        const unsigned short xb = lds16(Xs + t * hs + h);
+                        const float x = to_f<Tin>(*reinterpret_cast<const Tin *>(&xb));
                         float av[16];
                         const Tin *arow = As + h * rk + kbase;
                         if (vec) {
                             float lo[8], hi[8];
-                            unpack8<Tin>(*reinterpret_cast<const uint4 *>(arow), lo);
-                            unpack8<Tin>(*reinterpret_cast<const uint4 *>(arow + 8), hi);
+                            unpack8<Tin>(lds128(arow), lo);
+                            unpack8<Tin>(lds128(arow + 8), hi);
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 av[j] = lo[j];
@@ -253,8 +254,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                             }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                av[j] = kbase + j < rk ? to_f<Tin>(arow[j]) : 0.f;
+                            for (int j = 0; j < 16; ++j) {
+                                const unsigned short ab = kbase + j < rk ? lds16(arow + j) : 0;
+                                av[j] = to_f<Tin>(*reinterpret_cast<const Tin *>(&ab));
+                            }
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc[j] = fmaf(x, av[j], acc[j]);
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             for (int e = tid; e < per; e += kThreads) {
                 const int t = e / rk, kk = e - (e / rk) * rk;
                 float s = 0.f;
-                for (int c = 0; c < ncl; ++c) s += recv[(c * kRowsMax + t) * RMAX + kk];
+                for (int c = 0; c < ncl; ++c) s += ldsf(recv + (c * kRowsMax + t) * RMAX + kk);
                 s_v[t * RMAX + kk] = s;
             }
         } else {
@@ -355,9 +358,9 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 const float *vt = s_v + t * RMAX;
 #pragma unroll 4
                 for (int kk = part; kk < rk; kk += ks) {
-                    const float vk = vt[kk];
+                    const float vk = ldsf(vt + kk);
                     float bf[8];
-                    unpack8<Tin>(*reinterpret_cast<const uint4 *>(Bs + kk * js + cv * 8), bf);
+                    unpack8<Tin>(lds128(Bs + kk * js + cv * 8), bf);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) acc8[q] = fmaf(vk, bf[q], acc8[q]);
                 }
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                 Ty *yp = gY + (size_t)row * H2 + jlo + cv * 8;
                 float yv[8];
                 if (y_pref)
-                    load8<Ty>(ybuf + t * jc + (jlo - j0) + cv * 8, yv);
+                    lds8<Ty>(ybuf + t * jc + (jlo - j0) + cv * 8, yv);
                 else
                     load8<Ty>(yp, yv);
 #pragma unroll

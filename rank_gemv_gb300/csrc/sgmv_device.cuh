@@ -133,6 +133,38 @@ __device__ __forceinline__ void st_peer(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// ---- explicit shared-memory access ----------------------------------------
+// Pointers into dynamic shared memory that pass through lambdas or offset
+// arithmetic can lose their address space, and the generic loads the compiler
+// then emits are several times slower than ld.shared here.  Hot paths use
+// these instead.
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p))
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned short lds16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ldsf(const void *p) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void stsf(void *p, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_addr(p)), "f"(v) : "memory");
+}
+__device__ __forceinline__ void sts128(void *p, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // ---- element conversions ---------------------------------------------------
 template <typename T> __device__ __forceinline__ float to_f(T v);
 template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
@@ -176,6 +208,17 @@ template <typename Ty> __device__ __forceinline__ void store8(Ty *p, const float
 template <> __device__ __forceinline__ void store8<float>(float *p, const float (&f)[8]) {
     reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+// The same 8-element read from shared memory.
+template <typename Ty> __device__ __forceinline__ void lds8(const Ty *p, float (&f)[8]) {
+    unpack8<Ty>(lds128(p), f);
+}
+template <> __device__ __forceinline__ void lds8<float>(const float *p, float (&f)[8]) {
+    const uint4 a = lds128(p), b = lds128(p + 4);
+    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+    f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y);
+    f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
 }
 
 }  // namespace sgmv

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads)
                 for (int j = 0; j < 32; j += 4) st_peer4(pa + j * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dst[j] = v[j];
+                for (int j = 0; j < 32; ++j) stsf(dst + j, v[j]);
             }
         }
     }
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kTcThreads)
         const int m = rank * rpc + mr;
         if (m >= nrows || lost) continue;
         float s = 0.f;
-        for (int c = 0; c < ncl; ++c) s += recv[(size_t)(c * rpc + mr) * rk + col];
+        for (int c = 0; c < ncl; ++c) s += ldsf(recv + (size_t)(c * rpc + mr) * rk + col);
         const Tin hi = from_f<Tin>(s);
         const size_t o = (size_t)(p0 + m) * rk + col;
         vhi[o] = hi;
