@@ -1,10 +1,11 @@
 #!/usr/bin/env python3
 """Benchmark of the SGMV multi-LoRA hot path on GB300.
 
-One step = one pass of the whole path over one batch: group the batch's rows
-by adapter on the device (sgmv_build_segments_device), then the fused
-shrink+expand (sgmv_apply) with the row permutation -- both through the C ABI.
-The llama7b-stack workload groups once and applies all 224 projections.
+One step = one pass of the whole path over one batch through the C ABI:
+sgmv_apply_rows groups the batch's rows by adapter, gathers x, shrinks,
+expands and scatters into y (one kernel for decode batches; grouping kernel +
+CUDA-core + tensor-core kernels for prefill).  The llama7b-stack workload runs
+it for all 224 projections of one decode step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the fp64 oracle on the host cores
@@ -165,17 +166,15 @@ class Batch:
     def group(self, sgmv):
         sgmv.sgmv_build_segments_device(self.ra, self.w.L, out=self.meta)
 
-    n_apply = 1  # sgmv_apply calls per step
+    n_apply = 1  # update calls per step
 
     def apply(self, sgmv):
-        """One sgmv_apply; returns the number of kernels it launched."""
-        perm, seg_ptr, idx, _ = self.meta
-        sgmv.sgmv_apply(self.Y, self.X, self.A, self.B, seg_ptr, idx, self.w.scale, perm=perm,
-                        S=self.smax, workspace=self.ws)
+        """One sgmv_apply_rows (grouping + update); returns the kernels it launched."""
+        sgmv.sgmv_apply_rows(self.Y, self.X, self.A, self.B, self.ra, self.w.scale, out=self.meta,
+                             workspace=self.ws)
         return sgmv.sgmv_last_launch_count()
 
     def step(self, sgmv):
-        self.group(sgmv)
         self.apply(sgmv)
 
 
@@ -205,15 +204,15 @@ class StackBatch:
     n_apply = 224
 
     def apply(self, sgmv):
-        perm, seg_ptr, idx, _ = self.meta
+        """All 224 projections; the first call also writes the batch's grouping
+        out (as a serving loop would keep it)."""
         n = 0
-        for X, A, B, Y in self.projs:
-            sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
+        for i, (X, A, B, Y) in enumerate(self.projs):
+            sgmv.sgmv_apply_rows(Y, X, A, B, self.ra, 1.0, out=self.meta if i == 0 else None)
             n += sgmv.sgmv_last_launch_count()
         return n
 
     def step(self, sgmv):
-        self.group(sgmv)
         self.apply(sgmv)
 
     def bytes_moved(self):
@@ -293,19 +292,15 @@ def run_ours(args, rank, world, local):
     for i in range(W):
         batches[i % len(batches)].step(sgmv)
     # kernels per step, as reported by the library
-    batches[0].group(sgmv)
-    launches_group = sgmv.sgmv_last_launch_count()
     launches_apply = batches[0].apply(sgmv)
-    launches_step = launches_group + launches_apply
+    launches_step = launches_apply
     n_apply = batches[0].n_apply
     torch.cuda.synchronize()
     assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during warm-up"
     n = len(batches)
     g_full = capture([(lambda b=b: b.step(sgmv)) for b in batches])
     g_rem = capture([(lambda b=b: b.step(sgmv)) for b in batches[: K % n]]) if K % n else None
-    # kernel-only graphs (metadata already built) for the dominant kernel's duration
-    for b in batches:
-        b.group(sgmv)
+    # the update calls alone (here the same calls as a step)
     k_full = capture([(lambda b=b: b.apply(sgmv)) for b in batches])
     k_rem = capture([(lambda b=b: b.apply(sgmv)) for b in batches[: K % n]]) if K % n else None
 
@@ -338,8 +333,10 @@ def run_ours(args, rank, world, local):
     bytes_apply = bytes_step / n_apply
     achieved = bytes_apply / apply_s / 1e9
     per_call = launches_apply // n_apply
-    kname = ("sgmv_cc_kernel (fused shrink+expand, CUDA cores)" if per_call == 1 else
-             "sgmv_apply: sgmv_cc_kernel + sgmv_tc_shrink_kernel + sgmv_tc_expand_kernel")
+    kname = ("sgmv_cc_kernel (grouping + shrink + expand in one launch, CUDA cores)"
+             if per_call == 1 else
+             "sgmv_apply_rows: build_segments_kernel + sgmv_cc_kernel + sgmv_tc_shrink_kernel"
+             " + sgmv_tc_expand_kernel")
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak",

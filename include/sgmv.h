@@ -186,6 +186,29 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
                void *stream);
 
 /*
+ * Grouping and update in one call, from the batch's row -> adapter ids: the
+ * whole hot path (group rows by adapter, gather x, shrink, expand, scatter
+ * into y) for a batch whose rows arrive in any order.
+ *   row_adapter  device int32 [T], ids in [-1, L) (-1 = no adapter)
+ *   perm, seg_ptr, idx, S   device int32 arrays as for
+ *                sgmv_build_segments_device, receiving the grouping so later
+ *                calls on the same batch (other layers and projections) can
+ *                pass it to sgmv_apply; all four NULL or all four set.
+ * For T <= 256 without the tensor-core path (no workspace, r not 64/128, or
+ * T < 64) this is a single kernel: every CTA groups the rows itself, so no
+ * metadata is read from device memory (the arrays, if given, are still
+ * written).  Otherwise it runs the grouping kernel into the caller's arrays
+ * (then required: SGMV_ERR_INVALID_ARG if NULL) followed by sgmv_apply.  An id
+ * out of range is treated as -1 and reported as SGMV_ERR_BAD_INDEX in the
+ * device error word.
+ */
+int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const void *B,
+                    int in_dtype, float scale, const int32_t *row_adapter, int32_t T, int32_t L,
+                    int32_t H1, int32_t H2, int32_t r, int32_t *perm, int32_t *seg_ptr,
+                    int32_t *idx, int32_t *S, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's sticky
  * error word.  Returns SGMV_OK if no kernel reported an error since the last
  * read, else the first status code reported (SGMV_ERR_BAD_INDEX,

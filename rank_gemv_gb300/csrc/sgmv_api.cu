@@ -438,6 +438,87 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     return st;
 }
 
+int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const void *B,
+                    int in_dtype, float scale, const int32_t *row_adapter, int32_t T, int32_t L,
+                    int32_t H1, int32_t H2, int32_t r, int32_t *perm, int32_t *seg_ptr,
+                    int32_t *idx, int32_t *S, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+    g_launches = 0;
+    int st = check_common(T, L, r, 0, nullptr, nullptr, nullptr, in_dtype);
+    if (st != SGMV_OK) return st;
+    if ((st = check_dim(H1)) != SGMV_OK) return st;
+    if ((st = check_dim(H2)) != SGMV_OK) return st;
+    if (y_dtype != SGMV_F16 && y_dtype != SGMV_BF16 && y_dtype != SGMV_F32)
+        return SGMV_ERR_INVALID_ARG;
+    const bool meta = perm != nullptr;
+    if (meta != (seg_ptr != nullptr) || meta != (idx != nullptr) || meta != (S != nullptr))
+        return SGMV_ERR_INVALID_ARG;
+    if (workspace && workspace_bytes < sgmv_workspace_bytes(T, H1, H2, r)) return SGMV_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return SGMV_ERR_ALIGNMENT;
+    if (T == 0)
+        return meta ? sgmv_build_segments_device(row_adapter, T, L, perm, seg_ptr, idx, S, stream)
+                    : SGMV_OK;
+    if (!row_adapter || !y || !x || !A || !B) return SGMV_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(A) || !aligned16(B))
+        return SGMV_ERR_ALIGNMENT;
+    const int32_t smax = sgmv_max_segments(T, L);
+    const bool tc_possible = workspace != nullptr && (r == 64 || r == 128) && T >= kTcMinLen;
+
+    if (T <= kGroupMaxT && !tc_possible) {
+        // One launch: every CTA groups the rows itself.
+        int *err = error_word();
+        if (!err) return SGMV_ERR_CUDA;
+        CCLaunch l = {};
+        CCParams &p = l.p;
+        p.y = y;
+        p.x = x;
+        p.A = A;
+        p.B = B;
+        p.err = err;
+        p.row_adapter = row_adapter;
+        p.perm_out = perm;
+        p.seg_out = seg_ptr;
+        p.idx_out = idx;
+        p.S_out = S;
+        p.S_max = smax;
+        p.S = 0;
+        p.T = T;
+        p.L = L;
+        p.H1 = H1;
+        p.H2 = H2;
+        p.r = r;
+        p.rows = kRowsMax;
+        p.min_len = 1;
+        p.max_len = INT_MAX;
+        p.scale = scale;
+        const int cl = choose_cluster(H1, H2);
+        p.hc = round8(ceil_div(H1, cl));
+        p.jc = round8(ceil_div(H2, cl));
+        p.cl = cl;
+        finish(p, kFused, in_dtype, y_dtype);
+        const int64_t slots = ((int64_t)T + (int64_t)smax * (kRowsMax - 1)) / kRowsMax;
+        l.mode = kGrouped;
+        l.y_dtype = y_dtype;
+        l.rmax = rmax_of(r);
+        l.grid = dim3((unsigned)cl, (unsigned)slots, 1);
+        l.cluster = cl;
+        l.stream = static_cast<cudaStream_t>(stream);
+        l.pdl = true;
+        st = cuda_status("grouped fused kernel", cc_launch(in_dtype, l));
+        if (st == SGMV_OK) g_launches = 1;
+        return st;
+    }
+    // Larger batches, or long segments for the tensor cores: group into the
+    // caller's metadata arrays, then the general update.
+    if (!meta) return SGMV_ERR_INVALID_ARG;
+    st = sgmv_build_segments_device(row_adapter, T, L, perm, seg_ptr, idx, S, stream);
+    if (st != SGMV_OK) return st;
+    st = sgmv_apply(y, y_dtype, x, A, B, in_dtype, scale, perm, seg_ptr, idx, smax, nullptr, T, L,
+                    H1, H2, r, workspace, workspace_bytes, stream);
+    g_launches += 1;
+    return st;
+}
+
 int sgmv_get_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

@@ -59,15 +59,31 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     __shared__ int s_row[kRowsMax];
     __shared__ __align__(16) float s_v[kRowsMax * RMAX];
     __shared__ float s_red[(MODE == kExpand) ? 1 : kRowsMax * RMAX * (kThreads / (RMAX / 16)) / 32];
+    constexpr int kKeys = MODE == kGrouped ? kGroupMaxT : 1;
+    __shared__ int s_key[kKeys], s_cnt[kKeys], s_rank[kKeys];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
-    if (tid < 32) {
-        find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, tile_rows, min_len, max_len, err,
-                  blockIdx.y, MODE == kShrink, report, s_info);
+    // kGrouped: this thread's row (t = tid) in the stable grouping by adapter id
+    int g_key = -1, g_less = 0, g_rank = 0, g_dless = 0, g_nseg = 0;
+    if (MODE == kGrouped) {
+        // Every CTA groups the batch itself (T <= kGroupMaxT): no metadata to
+        // read from device memory and no separate grouping launch.  Sorted
+        // position of row t = (#rows with a smaller id) + (#earlier rows with
+        // the same id); tiles are numbered over ids in ascending order.
+        const int32_t *ra = P.row_adapter;
+        if (tid < nrows_all) {
+            g_key = ra[tid];
+            if (g_key < -1 || g_key >= nadapters) {
+                if (report) set_error(err, kErrBadIndex);
+                g_key = -1;
+            }
+            s_key[tid] = g_key;
+        }
         if (tid == 0) {
+            s_info[0] = -1;
             mbar_init(&bars[0], 2);
             mbar_init(&bars[1], 2);
             mbar_init(&bars[2], 1);
@@ -75,8 +91,75 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
             mbar_init(&bars[4], 1);
             mbar_init_fence();
         }
+        __syncthreads();
+        int cnt = 0;
+        if (tid < nrows_all) {
+            for (int u = 0; u < nrows_all; ++u) {
+                const int ku = s_key[u];
+                g_less += ku < g_key;
+                cnt += ku == g_key;
+                g_rank += (ku == g_key) & (u < tid);
+            }
+            s_cnt[tid] = cnt;
+            s_rank[tid] = g_rank;
+        }
+        __syncthreads();
+        if (tid < nrows_all) {
+            int tb = 0;  // tiles of the adapters with a smaller id
+            for (int u = 0; u < nrows_all; ++u) {
+                const int ku = s_key[u];
+                if (s_rank[u] == 0 && ku < g_key) {
+                    ++g_dless;
+                    if (ku >= 0) tb += (s_cnt[u] + kRowsMax - 1) / kRowsMax;
+                }
+            }
+            if (g_key >= 0 && tb + g_rank / kRowsMax == (int)blockIdx.y) {
+                const int slot = g_rank % kRowsMax;
+                s_row[slot] = tid;
+                if (slot == 0) {
+                    s_info[0] = 0;
+                    s_info[1] = g_less + g_rank;
+                    s_info[2] = min(kRowsMax, cnt - g_rank);
+                    s_info[3] = g_key;
+                }
+            }
+        }
+        g_nseg = __syncthreads_count(tid < nrows_all && g_rank == 0);
+    } else {
+        if (tid < 32) {
+            find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, tile_rows, min_len, max_len, err,
+                      blockIdx.y, MODE == kShrink, report, s_info);
+            if (tid == 0) {
+                mbar_init(&bars[0], 2);
+                mbar_init(&bars[1], 2);
+                mbar_init(&bars[2], 1);
+                mbar_init(&bars[3], 1);
+                mbar_init(&bars[4], 1);
+                mbar_init_fence();
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
+    if (MODE == kGrouped && report && P.perm_out) {
+        // CTA (0,0) writes the grouping out for later calls: after the
+        // previous kernel on the stream, which may still read these arrays.
+        pdl_wait();
+        if (tid < nrows_all) {
+            P.perm_out[g_less + g_rank] = tid;
+            if (g_rank == 0) {
+                P.seg_out[g_dless] = g_less;
+                P.idx_out[g_dless] = g_key;
+            }
+        }
+        if (tid == 0) {
+            P.seg_out[g_nseg] = nrows_all;
+            *P.S_out = g_nseg;
+        }
+        for (int sidx = g_nseg + tid; sidx < P.S_max; sidx += kThreads) {
+            P.idx_out[sidx] = -1;
+            P.seg_out[sidx + 1] = nrows_all;
+        }
+    }
     if (s_info[0] < 0) return;  // no tile for this slot (same for the whole cluster)
     const int p0 = s_info[1];
     const int nrows = s_info[2];
@@ -159,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         if (lane == 0)
             for (int i = 0; i < min(nA, ax_stages); ++i) issue_a(i);
         for (int i = 0; i < min(nB, b_stages); ++i) issue_b(i);
-    } else if (tid < 32 + nrows) {
+    } else if (MODE != kGrouped && tid < 32 + nrows) {
         // Physical rows of the tile; invalid perm entries are skipped and reported.
         const int t = tid - 32;
         int row = perm ? perm[p0 + t] : p0 + t;
@@ -392,6 +475,7 @@ static void *pick_mode(int mode) {
     switch (mode) {
         case kFused: return (void *)sgmv_cc_kernel<Tin, Ty, RMAX, kFused>;
         case kExpand: return (void *)sgmv_cc_kernel<Tin, Ty, RMAX, kExpand>;
+        case kGrouped: return (void *)sgmv_cc_kernel<Tin, Ty, RMAX, kGrouped>;
         default: return (void *)sgmv_cc_kernel<Tin, float, RMAX, kShrink>;
     }
 }

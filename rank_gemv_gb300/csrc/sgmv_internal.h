@@ -11,7 +11,11 @@ enum Mode : int {
     kFused = 0,   // shrink + expand, v kept in shared memory of a cluster
     kShrink = 1,  // shrink only, v written to device memory
     kExpand = 2,  // expand only, v read from device memory
+    kGrouped = 3, // kFused, each CTA grouping the rows itself from row_adapter
 };
+
+// Largest batch kGrouped handles (one row per thread of a CTA).
+constexpr int kGroupMaxT = 256;
 
 constexpr int kThreads = 256;   // threads per CTA of the CUDA-core kernels
 constexpr int kRowsMax = 8;     // rows of one segment handled by one tile
@@ -33,6 +37,12 @@ struct CCParams {
     const int32_t *seg_ptr;
     const int32_t *idx;
     int *err;            // sticky device error word
+    const int32_t *row_adapter;  // kGrouped: adapter id of every row
+    int32_t *perm_out;           // kGrouped, optional: grouping written out
+    int32_t *seg_out;
+    int32_t *idx_out;
+    int32_t *S_out;
+    int32_t S_max;
     int32_t S, T, L, H1, H2, r;
     int32_t rows;        // rows per tile, 1..kRowsMax
     int32_t hc, jc;      // columns of H1 / H2 owned by one CTA (multiples of 8)

@@ -41,6 +41,8 @@ SIGNATURES = {
                            _i32, _i32, _i32, _vp]),
     "sgmv_apply": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp, _i32,
                           _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "sgmv_apply_rows": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _i32, _i32, _i32, _i32,
+                               _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sgmv_get_device_error": (_int, [_vp]),
 }
 
@@ -195,6 +197,27 @@ def sgmv_apply(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_host=None
         _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")),
         _nseg(idx, S), _ptr(sph), T, L, H1, H2, r, _ptr(workspace), ws_bytes,
         _stream(x.device)), "sgmv_apply")
+    return y
+
+
+def sgmv_apply_rows(y, x, A, B, row_adapter, scale=1.0, out=None, workspace=None):
+    """Group the rows by adapter and apply SGMV in one call; returns y.
+
+    ``out`` = (perm, seg_ptr, idx, S) device int32 tensors (as returned by
+    sgmv_build_segments_device) to receive the grouping, or None.
+    """
+    T, H1 = x.shape
+    L, _, r = A.shape
+    H2 = y.shape[1]
+    ra = _meta(row_adapter, "row_adapter")
+    perm = seg_ptr = idx = S = None
+    if out is not None:
+        perm, seg_ptr, idx, S = (_meta(t, "out") for t in out)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().sgmv_apply_rows(
+        _ptr(y), _DTYPES[y.dtype], _ptr(x), _ptr(A), _ptr(B), _DTYPES[x.dtype], float(scale),
+        _ptr(ra), T, L, H1, H2, r, _ptr(perm), _ptr(seg_ptr), _ptr(idx), _ptr(S),
+        _ptr(workspace), ws_bytes, _stream(x.device)), "sgmv_apply_rows")
     return y
 
 

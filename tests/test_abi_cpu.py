@@ -139,3 +139,21 @@ def test_shrink_expand_reject_bad_arguments(lib):
                            None) == 3
     assert lib.sgmv_build_segments_device(A16, 4, 40000, A16, A16, A16, A16, None) == 2
     assert lib.sgmv_build_segments_device(A16, -1, 4, A16, A16, A16, A16, None) == 1
+
+
+def test_apply_rows_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(y=A16, y_dt=0, x=A16, A=A16, B=A16, in_dt=0, ra=A16, T=4, L=2, H1=64, H2=64, r=16,
+                 perm=None, seg=None, idx=None, S=None, ws=None, wsb=0)
+        a.update(kw)
+        return lib.sgmv_apply_rows(a["y"], a["y_dt"], a["x"], a["A"], a["B"], a["in_dt"], 1.0,
+                                   a["ra"], a["T"], a["L"], a["H1"], a["H2"], a["r"], a["perm"],
+                                   a["seg"], a["idx"], a["S"], a["ws"], a["wsb"], None)
+    assert call(r=0) == 1
+    assert call(r=129) == 2
+    assert call(H1=20) == 3
+    assert call(x=MIS) == 3
+    assert call(ra=None) == 1
+    assert call(perm=A16) == 1          # metadata outputs: all or none
+    assert call(ws=A16, wsb=8) == 6
+    assert call(y_dt=5) == 1
