@@ -204,11 +204,16 @@ class StackBatch:
     n_apply = 224
 
     def apply(self, sgmv):
-        """All 224 projections; the first call also writes the batch's grouping
-        out (as a serving loop would keep it)."""
+        """One decode step over all 224 projections, as a serving loop runs it:
+        the first call groups the batch (sgmv_apply_rows writes the grouping
+        out), the other 223 reuse it through sgmv_apply."""
+        perm, seg_ptr, idx, _ = self.meta
         n = 0
         for i, (X, A, B, Y) in enumerate(self.projs):
-            sgmv.sgmv_apply_rows(Y, X, A, B, self.ra, 1.0, out=self.meta if i == 0 else None)
+            if i == 0:
+                sgmv.sgmv_apply_rows(Y, X, A, B, self.ra, 1.0, out=self.meta)
+            else:
+                sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
             n += sgmv.sgmv_last_launch_count()
         return n
 

@@ -194,10 +194,9 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
  *                sgmv_build_segments_device, receiving the grouping so later
  *                calls on the same batch (other layers and projections) can
  *                pass it to sgmv_apply; all four NULL or all four set.
- * For T <= 256 without the tensor-core path (no workspace, r not 64/128, or
- * T < 64) this is a single kernel: every CTA groups the rows itself, so no
- * metadata is read from device memory (the arrays, if given, are still
- * written).  Otherwise it runs the grouping kernel into the caller's arrays
+ * For T <= 64 rows this is a single kernel: every CTA groups the rows
+ * itself, so no metadata is read from device memory (the arrays, if given,
+ * are still written).  Otherwise it runs the grouping kernel into the caller's arrays
  * (then required: SGMV_ERR_INVALID_ARG if NULL) followed by sgmv_apply.  An id
  * out of range is treated as -1 and reported as SGMV_ERR_BAD_INDEX in the
  * device error word.

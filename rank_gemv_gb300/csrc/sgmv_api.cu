@@ -462,9 +462,8 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
     if (!aligned16(y) || !aligned16(x) || !aligned16(A) || !aligned16(B))
         return SGMV_ERR_ALIGNMENT;
     const int32_t smax = sgmv_max_segments(T, L);
-    const bool tc_possible = workspace != nullptr && (r == 64 || r == 128) && T >= kTcMinLen;
-
-    if (T <= kGroupMaxT && !tc_possible) {
+    // T <= kGroupMaxT < kTcMinLen: no segment can reach the tensor cores
+    if (T <= kGroupMaxT) {
         // One launch: every CTA groups the rows itself.
         int *err = error_word();
         if (!err) return SGMV_ERR_CUDA;

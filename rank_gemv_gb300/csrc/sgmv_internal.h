@@ -14,8 +14,10 @@ enum Mode : int {
     kGrouped = 3, // kFused, each CTA grouping the rows itself from row_adapter
 };
 
-// Largest batch kGrouped handles (one row per thread of a CTA).
-constexpr int kGroupMaxT = 256;
+// Largest batch kGrouped handles.  Each CTA spends O(T) shared-memory steps
+// per row on the grouping, which stops paying off against reading
+// precomputed metadata beyond a few dozen rows.
+constexpr int kGroupMaxT = 64;
 
 constexpr int kThreads = 256;   // threads per CTA of the CUDA-core kernels
 constexpr int kRowsMax = 8;     // rows of one segment handled by one tile

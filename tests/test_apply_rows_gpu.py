@@ -1,8 +1,7 @@
 """sgmv_apply_rows (grouping + update in one call) against the oracle.
 
-Up to 256 rows without the tensor-core path it is one kernel in which every
-CTA groups the batch itself; otherwise it is the grouping kernel followed by
-sgmv_apply.  Both must give the oracle's result and its metadata bit-exact,
+Up to 64 rows it is one kernel in which every CTA groups the batch itself;
+otherwise it is the grouping kernel followed by sgmv_apply.  Both must give the oracle's result and its metadata bit-exact,
 and the single-kernel form must give the same bits as the two-call form.
 """
 import numpy as np
@@ -67,16 +66,17 @@ def check_meta(out, w):
 
 @pytest.mark.parametrize("shuffle", [False, True])
 @pytest.mark.parametrize("name", ["tiny", "decode-distinct", "decode-shared", "decode-zipf"])
-def test_decode_workloads_in_one_kernel(name, shuffle):
+def test_decode_workloads(name, shuffle):
     w = wl.make(name, 3, y0="randn", shuffle_rows=shuffle)
     y, out, launches = run_rows(w)
-    assert launches == 1
+    assert launches == (1 if w.T <= 64 else 2)
     check_error_word(0)
     check_meta(out, w)
     ref, *_ = oracle_apply_rows(w)
     assert_close(y, ref, name)
-    y2, _, _ = run_rows(w, with_meta=False)
-    assert torch.equal(y, y2)
+    if w.T <= 64:
+        y2, _, _ = run_rows(w, with_meta=False)
+        assert torch.equal(y, y2)
 
 
 def test_same_bits_as_grouping_then_apply():
@@ -90,7 +90,7 @@ def test_same_bits_as_grouping_then_apply():
     assert torch.equal(y_one, y_two)
 
 
-@pytest.mark.parametrize("T,expect_launches", [(255, 1), (256, 1), (257, 2), (600, 2)])
+@pytest.mark.parametrize("T,expect_launches", [(1, 1), (63, 1), (64, 1), (65, 2), (600, 2)])
 def test_batch_size_boundary(T, expect_launches):
     g = torch.Generator().manual_seed(T)
     ra = torch.randint(-1, 40, (T,), generator=g, dtype=torch.int32)  # adapters 40..47 unused
@@ -127,7 +127,7 @@ def test_bad_ids_are_no_adapter_and_reported():
 
 
 def test_large_batch_needs_metadata_buffers():
-    w = wl.draw(300, 4, 256, 128, 8, torch.zeros(300, dtype=torch.int32))
+    w = wl.draw(100, 4, 256, 128, 8, torch.zeros(100, dtype=torch.int32))
     with pytest.raises(sg().SgmvError) as e:
         run_rows(w, with_meta=False)
     assert e.value.status == 1
