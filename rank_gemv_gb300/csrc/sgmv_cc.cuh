@@ -275,18 +275,14 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     }
     pdl_trigger();
 
-    bool lost = false;  // a bounded wait ran out: write nothing
-    // One thread waits on the mbarrier (waiters that sleep in try_wait wake
-    // late); the others wait at the CTA barrier, which also tells every
-    // thread whether the wait ran out.
+    bool lost = false;  // a bounded wait ran out: this thread writes nothing
+    // Every thread polls the mbarrier itself: no CTA barrier per wait.
     auto cta_wait = [&](uint64_t *bar, uint32_t par) {
-        int bad = 0;
-        if (tid == 0 && !mbar_wait(bar, par)) {
+        if (!mbar_wait(bar, par)) {
             set_error(err, kErrTimeout);
             mbar_wait(bar, par);
-            bad = 1;
+            lost = true;
         }
-        if (__syncthreads_or(bad)) lost = true;
     };
     if (MODE == kExpand) {
         for (int e = tid; e < nrows * rk; e += kThreads) {
@@ -306,8 +302,6 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
         const int wig = hg >> 5;             // warp within the k-group
         const bool kact = kbase < rk;       // same for the whole warp
         const bool vec = (rk & 7) == 0;     // A rows are 16-byte aligned in smem
-        for (int e = tid; e < kRowsMax * RMAX * WPG; e += kThreads) s_red[e] = 0.f;
-        __syncthreads();
         for (int i = 0; i < nA; ++i) {
             const int st = i % ax_stages;
             const uint32_t par = (uint32_t)((i / ax_stages) & 1);
@@ -357,8 +351,10 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
                         }
                     }
                     acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
-                    if ((lane & 1) == 0)
-                        s_red[(t * RMAX + kbase + (lane >> 1)) * WPG + wig] += acc[0];
+                    if ((lane & 1) == 0) {
+                        float *dst = &s_red[(t * RMAX + kbase + (lane >> 1)) * WPG + wig];
+                        *dst = i == 0 ? acc[0] : *dst + acc[0];
+                    }
                 }
             }
             __syncthreads();
@@ -414,58 +410,45 @@ __global__ void __launch_bounds__(kThreads) sgmv_cc_kernel(const __grid_constant
     if (y_pref) cta_wait(&bars[4], 0);
 
     // ---- expand: y[row, j] += scale * v . B[a][:, j] for this CTA's slice ----
-    // Work item = (tile row, 8 consecutive columns); the r-sum of an item is
-    // split over ks neighbouring lanes (ks from the chunk width only, so a
-    // row's result never depends on how many rows share its tile) and summed
-    // by an xor tree.
+    // Each thread owns two adjacent columns and runs the whole r-sum, so a
+    // warp reads 128 contiguous bytes of a B row per step (no bank conflicts)
+    // and writes 128 contiguous bytes of y.
     for (int i = 0; i < nB; ++i) {
         const int st = i % b_stages;
         cta_wait(&bars[2 + st], (uint32_t)((i / b_stages) & 1));
         const int jlo = j0 + i * js;
-        const int ncv = min(js, j1 - jlo) >> 3;
-        int ks = 1;
-        while (ks < 8 && ncv * ks * 2 <= kThreads) ks <<= 1;
-        const int items = nrows * ncv * ks;
-        const int span = (items + 31) & ~31;  // whole warps take part in the shuffles
+        const int npair = min(js, j1 - jlo) >> 1;
         const Tin *Bs = b_buf(st);
-        for (int w = tid; w < span; w += kThreads) {
-            const bool live = w < items;
-            const int item = live ? w / ks : 0;
-            const int part = w & (ks - 1);
-            const int t = item / ncv;
-            const int cv = item - t * ncv;
-            float acc8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc8[q] = 0.f;
-            if (live) {
+        if (!lost) {
+            for (int t = 0; t < nrows; ++t) {
+                const int row = s_row[t];
+                if (row < 0) continue;
                 const float *vt = s_v + t * RMAX;
+                for (int cp = tid; cp < npair; cp += kThreads) {
+                    float a0 = 0.f, a1 = 0.f;
+                    const Tin *bcol = Bs + 2 * cp;
 #pragma unroll 4
-                for (int kk = part; kk < rk; kk += ks) {
-                    const float vk = ldsf(vt + kk);
-                    float bf[8];
-                    unpack8<Tin>(lds128(Bs + kk * js + cv * 8), bf);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc8[q] = fmaf(vk, bf[q], acc8[q]);
+                    for (int kk = 0; kk < rk; ++kk) {
+                        const float vk = ldsf(vt + kk);
+                        float b0, b1;
+                        unpack2<Tin>(lds32(bcol + kk * js), b0, b1);
+                        a0 = fmaf(vk, b0, a0);
+                        a1 = fmaf(vk, b1, a1);
+                    }
+                    Ty *yp = gY + (size_t)row * H2 + jlo + 2 * cp;
+                    float y0, y1;
+                    if (y_pref)
+                        lds2<Ty>(ybuf + t * jc + (jlo - j0) + 2 * cp, y0, y1);
+                    else
+                        ld2<Ty>(yp, y0, y1);
+                    st2<Ty>(yp, fmaf(scale, a0, y0), fmaf(scale, a1, y1));
                 }
             }
-            for (int off = 1; off < ks; off <<= 1)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc8[q] += __shfl_xor_sync(0xffffffffu, acc8[q], off);
-            const int row = live ? s_row[t] : -1;
-            if (part == 0 && row >= 0 && !lost) {
-                Ty *yp = gY + (size_t)row * H2 + jlo + cv * 8;
-                float yv[8];
-                if (y_pref)
-                    lds8<Ty>(ybuf + t * jc + (jlo - j0) + cv * 8, yv);
-                else
-                    load8<Ty>(yp, yv);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) yv[q] = fmaf(scale, acc8[q], yv[q]);
-                store8<Ty>(yp, yv);
-            }
         }
-        __syncthreads();
-        if (tid < 32 && i + b_stages < nB) issue_b(i + b_stages);
+        if (i + b_stages < nB) {  // the stage is refilled: everyone is done with it
+            __syncthreads();
+            if (tid < 32) issue_b(i + b_stages);
+        }
     }
 }
 

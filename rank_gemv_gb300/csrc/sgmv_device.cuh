@@ -165,6 +165,18 @@ __device__ __forceinline__ void sts128(void *p, uint4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ uint32_t lds32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(const void *p) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p))
+                 : "memory");
+    return v;
+}
+
 // ---- element conversions ---------------------------------------------------
 template <typename T> __device__ __forceinline__ float to_f(T v);
 template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
@@ -209,6 +221,41 @@ template <> __device__ __forceinline__ void store8<float>(float *p, const float 
     reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
+// Two consecutive elements widened to fp32: from 32 bits of a 16-bit pair, or
+// from 64 bits of an fp32 pair.
+template <typename T> __device__ __forceinline__ void unpack2(uint32_t u, float &a, float &b) {
+    const T *h = reinterpret_cast<const T *>(&u);
+    a = to_f<T>(h[0]);
+    b = to_f<T>(h[1]);
+}
+// y pairs: read / write two consecutive outputs (4 bytes, or 8 for fp32).
+template <typename Ty> __device__ __forceinline__ void ld2(const Ty *p, float &a, float &b) {
+    unpack2<Ty>(*reinterpret_cast<const uint32_t *>(p), a, b);
+}
+template <> __device__ __forceinline__ void ld2<float>(const float *p, float &a, float &b) {
+    const float2 v = *reinterpret_cast<const float2 *>(p);
+    a = v.x;
+    b = v.y;
+}
+template <typename Ty> __device__ __forceinline__ void lds2(const Ty *p, float &a, float &b) {
+    unpack2<Ty>(lds32(p), a, b);
+}
+template <> __device__ __forceinline__ void lds2<float>(const float *p, float &a, float &b) {
+    const uint2 v = lds64(p);
+    a = __uint_as_float(v.x);
+    b = __uint_as_float(v.y);
+}
+template <typename Ty> __device__ __forceinline__ void st2(Ty *p, float a, float b) {
+    uint32_t u;
+    Ty *h = reinterpret_cast<Ty *>(&u);
+    h[0] = from_f<Ty>(a);
+    h[1] = from_f<Ty>(b);
+    *reinterpret_cast<uint32_t *>(p) = u;
+}
+template <> __device__ __forceinline__ void st2<float>(float *p, float a, float b) {
+    *reinterpret_cast<float2 *>(p) = make_float2(a, b);
+}
+
 // The same 8-element read from shared memory.
 template <typename Ty> __device__ __forceinline__ void lds8(const Ty *p, float (&f)[8]) {
     unpack8<Ty>(lds128(p), f);
