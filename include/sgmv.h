@@ -208,6 +208,28 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
                     void *stream);
 
 /*
+ * sgmv_apply for callers that cannot allocate device memory: the pages
+ * describing SGMV have no counterpart of this call.  It is for code that may
+ * not call cudaMalloc where it runs SGMV -- a plugin that only gets the
+ * buffers its host engine planned at start-up, a serving loop that forbids
+ * allocation after warm-up, or code running while a CUDA graph is captured.
+ * Arguments and results are those of sgmv_apply, without the workspace: the
+ * scratch for the tensor-core path is a fixed 4 MiB array inside the
+ * library's device image, held by every GPU that loads the library until the
+ * process exits.  Problems whose sgmv_workspace_bytes(T, H1, H2, r) exceeds
+ * 4 MiB are refused with SGMV_ERR_WORKSPACE before anything is launched.
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress, no allocation); make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last call's
+ * contents (nothing in it has to start at zero), so calls that overlap on the
+ * GPU -- on different streams, or from different threads -- race on it.
+ */
+int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const void *B,
+                       int in_dtype, float scale, const int32_t *perm, const int32_t *seg_ptr,
+                       const int32_t *idx, int32_t S, const int32_t *seg_ptr_host, int32_t T,
+                       int32_t L, int32_t H1, int32_t H2, int32_t r, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's sticky
  * error word.  Returns SGMV_OK if no kernel reported an error since the last
  * read, else the first status code reported (SGMV_ERR_BAD_INDEX,

@@ -43,6 +43,8 @@ SIGNATURES = {
                           _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
     "sgmv_apply_rows": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _i32, _i32, _i32, _i32,
                                _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "sgmv_apply_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp,
+                                  _i32, _i32, _i32, _i32, _i32, _vp]),
     "sgmv_get_device_error": (_int, [_vp]),
 }
 
@@ -218,6 +220,22 @@ def sgmv_apply_rows(y, x, A, B, row_adapter, scale=1.0, out=None, workspace=None
         _ptr(y), _DTYPES[y.dtype], _ptr(x), _ptr(A), _ptr(B), _DTYPES[x.dtype], float(scale),
         _ptr(ra), T, L, H1, H2, r, _ptr(perm), _ptr(seg_ptr), _ptr(idx), _ptr(S),
         _ptr(workspace), ws_bytes, _stream(x.device)), "sgmv_apply_rows")
+    return y
+
+
+def sgmv_apply_noalloc(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_host=None, S=None):
+    """sgmv_apply without a caller-provided workspace: for callers that may not
+    allocate device memory, the tensor-core path uses a fixed 4 MiB scratch
+    array inside the library (see include/sgmv.h).  Calls that overlap on the
+    GPU share that array and race; returns y."""
+    T, H1 = x.shape
+    L, _, r = A.shape
+    H2 = y.shape[1]
+    sph = _host_i32(seg_ptr_host)
+    _check(load_library().sgmv_apply_noalloc(
+        _ptr(y), _DTYPES[y.dtype], _ptr(x), _ptr(A), _ptr(B), _DTYPES[x.dtype], float(scale),
+        _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")),
+        _nseg(idx, S), _ptr(sph), T, L, H1, H2, r, _stream(x.device)), "sgmv_apply_noalloc")
     return y
 
 
