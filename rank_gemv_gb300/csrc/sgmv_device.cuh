@@ -92,6 +92,20 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// ---- 1-D bulk copy shared -> global (bulk-group completion) ---------------
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until this thread's committed bulk copies have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ---- clusters / distributed shared memory ---------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -221,6 +235,21 @@ template <> __device__ __forceinline__ void store8<float>(float *p, const float 
     reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
+// Write 8 elements to shared memory (16 bytes, or 32 for fp32).
+template <typename Ty> __device__ __forceinline__ void sts8(Ty *p, const float (&f)[8]) {
+    uint4 u;
+    Ty *h = reinterpret_cast<Ty *>(&u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = from_f<Ty>(f[q]);
+    sts128(p, u);
+}
+template <> __device__ __forceinline__ void sts8<float>(float *p, const float (&f)[8]) {
+    sts128(p, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                         __float_as_uint(f[3])));
+    sts128(p + 4, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                             __float_as_uint(f[7])));
+}
+
 // Two consecutive elements widened to fp32: from 32 bits of a 16-bit pair, or
 // from 64 bits of an fp32 pair.
 template <typename T> __device__ __forceinline__ void unpack2(uint32_t u, float &a, float &b) {

@@ -38,7 +38,6 @@ constexpr int kTcThreads = 128;  // 4 warps: one TMEM lane (tile row) per thread
 constexpr int kTcRows = 128;     // M of one tile
 constexpr int kKB = 64;          // k-block: 64 16-bit elements = one 128-byte swizzle row
 constexpr int kStages = 3;       // shrink ring depth
-constexpr int kTcN = 128;        // columns of H2 per expand CTA
 
 struct TCShrinkParams {
     CUtensorMap tmap_a;  // A as [L][H1][r], box {64, 64, 1}
@@ -361,9 +360,18 @@ __global__ void __launch_bounds__(kTcThreads)
 }
 
 // ---------------------------------------------------------------- expand
+// Columns of H2 per expand CTA: 128 for 16-bit y, 64 for fp32 y (the y tile
+// staged in shared memory then stays at 32 KB and two or more CTAs fit per SM).
+template <typename Ty> constexpr int tc_cols() { return sizeof(Ty) == 4 ? 64 : 128; }
+// Bytes of one staged y row: the tile's columns plus 16 bytes, so that the
+// 16-byte accesses of 8 consecutive rows fall in different banks.
+template <typename Ty> constexpr int tc_ypitch() { return tc_cols<Ty>() * (int)sizeof(Ty) + 16; }
+
 template <typename Tin, typename Ty>
 __global__ void __launch_bounds__(kTcThreads)
     sgmv_tc_expand_kernel(const __grid_constant__ TCExpandParams P) {
+    constexpr int N = tc_cols<Ty>();
+    constexpr int YP = tc_ypitch<Ty>();
     const int32_t *const seg_ptr = P.seg_ptr;
     const int32_t *const idx = P.idx;
     const int32_t *const perm = P.perm;
@@ -371,13 +379,13 @@ __global__ void __launch_bounds__(kTcThreads)
     const int nseg = P.S, nrows_all = P.T, nadapters = P.L, min_len = P.min_len,
               max_len = P.max_len, rk = P.r, H2 = P.H2;
     const float scale = P.scale;
-    void *const yptr = P.y;
+    Ty *const gY = static_cast<Ty *>(P.y);
     const CUtensorMap *const tmap_b = &P.tmap_b;
     const CUtensorMap *const tmap_vhi = &P.tmap_vhi;
     const CUtensorMap *const tmap_vlo = &P.tmap_vlo;
 
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t bar_b, bar_v, bar_mma;
+    __shared__ __align__(8) uint64_t bar_b, bar_v, bar_y, bar_mma;
     __shared__ int s_info[4];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -389,6 +397,7 @@ __global__ void __launch_bounds__(kTcThreads)
         if (lane == 0) {
             mbar_init(&bar_b, 1);
             mbar_init(&bar_v, 1);
+            mbar_init(&bar_y, 1);
             mbar_init(&bar_mma, 1);
             mbar_init_fence();
         }
@@ -396,19 +405,23 @@ __global__ void __launch_bounds__(kTcThreads)
     __syncthreads();
     if (s_info[0] < 0) return;
     const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
-    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)kTcN);
+    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)N);
 
     uint8_t *base = align1024(dsm);
-    const uint32_t tile_bytes = (uint32_t)rk * 256u;  // [r][128] and [128][r] 16-bit tiles
-    uint8_t *b_tile = base;                  // two N-atoms of [r rows][64 columns]
-    uint8_t *vhi_tile = base + tile_bytes;   // r/64 K-blocks of [128 rows][64]
-    uint8_t *vlo_tile = base + 2 * tile_bytes;
-    const int j0 = (int)blockIdx.x * kTcN;
+    const uint32_t v_bytes = (uint32_t)rk * 256u;  // [128 rows][r] 16-bit, as r/64 K-blocks
+    const uint32_t b_bytes = (uint32_t)rk * N * 2u; // N/64 N-atoms of [r rows][64 columns]
+    uint8_t *b_tile = base;
+    uint8_t *vhi_tile = base + b_bytes;
+    uint8_t *vlo_tile = vhi_tile + v_bytes;
+    uint8_t *y_tile = vlo_tile + v_bytes;  // [128 rows][YP bytes]
+    const int j0 = (int)blockIdx.x * N;
+    const int ncols = min(N, H2 - j0);
+    const uint32_t yrow_bytes = (uint32_t)ncols * sizeof(Ty);
 
     if (tid == 0) {  // weights: independent of the previous kernel
-        mbar_arrive_expect_tx(&bar_b, tile_bytes);
-        tma_load_3d(b_tile, tmap_b, j0, 0, a, &bar_b);
-        tma_load_3d(b_tile + rk * 128, tmap_b, j0 + 64, 0, a, &bar_b);
+        mbar_arrive_expect_tx(&bar_b, b_bytes);
+        for (int c = 0; c < N; c += 64)
+            tma_load_3d(b_tile + c * rk * 2, tmap_b, j0 + c, 0, a, &bar_b);
     }
     int row = -1;
     if (tid < nrows) {
@@ -418,20 +431,24 @@ __global__ void __launch_bounds__(kTcThreads)
             row = -1;
         }
     }
+    const int nvalid = __syncthreads_count(row >= 0);
     pdl_wait();
     if (tid == 0) {  // v of the tile, written by the shrink kernel
-        mbar_arrive_expect_tx(&bar_v, 2 * tile_bytes);
+        mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);
         for (int kb = 0; kb < rk / kKB; ++kb) {
             tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, p0, &bar_v);
             tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, p0, &bar_v);
         }
+        mbar_arrive_expect_tx(&bar_y, yrow_bytes * (uint32_t)nvalid);
     }
+    // this thread's y row, one bulk copy, while the MMAs run
+    if (row >= 0)
+        bulk_g2s(y_tile + tid * YP, gY + (size_t)row * H2 + j0, yrow_bytes, &bar_y);
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    bool lost = false;
     if (tid == 0) {
         const bool ok = mbar_wait(&bar_b, 0) && mbar_wait(&bar_v, 0);
         if (!ok) {
@@ -440,8 +457,7 @@ __global__ void __launch_bounds__(kTcThreads)
             mbar_wait(&bar_v, 0);
         }
         tc_fence_after();
-        const uint32_t idesc =
-            idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, kTcN);
+        const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, N);
         const uint32_t ba = smem_addr(b_tile);
         uint32_t acc = 0;
         for (int h = 0; h < 2; ++h) {
@@ -457,38 +473,41 @@ __global__ void __launch_bounds__(kTcThreads)
         }
         mma_commit(&bar_mma);
     }
-    {
-        int bad = 0;
-        if (tid == 0 && !mbar_wait(&bar_mma, 0)) {
-            set_error(err, kErrTimeout);
-            mbar_wait(&bar_mma, 0);
-            bad = 1;
-        }
-        if (__syncthreads_or(bad)) lost = true;
+    bool lost = false;
+    if (!mbar_wait(&bar_mma, 0) || !mbar_wait(&bar_y, 0)) {
+        set_error(err, kErrTimeout);
+        mbar_wait(&bar_mma, 0);
+        mbar_wait(&bar_y, 0);
+        lost = true;
     }
     tc_fence_after();
 
-    Ty *yrow = static_cast<Ty *>(yptr) + (size_t)(row < 0 ? 0 : row) * H2;
-    for (int c0 = 0; c0 < kTcN; c0 += 32) {
+    // y row in shared memory += scale * accumulator row, 32 columns at a time
+    uint8_t *yr = y_tile + tid * YP;
+    for (int c0 = 0; c0 < N; c0 += 32) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-        if (row >= 0 && !lost) {
+        if (row >= 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int j = j0 + c0 + q * 8;
-                if (j < H2) {
-                    float y[8];
-                    load8<Ty>(yrow + j, y);
+                Ty *p = reinterpret_cast<Ty *>(yr) + c0 + q * 8;
+                float y[8];
+                lds8<Ty>(p, y);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = fmaf(scale, v[q * 8 + i], y[i]);
-                    store8<Ty>(yrow + j, y);
-                }
+                for (int i = 0; i < 8; ++i) y[i] = fmaf(scale, v[q * 8 + i], y[i]);
+                sts8<Ty>(p, y);
             }
         }
     }
+    fence_proxy_async();  // generic shared-memory writes -> bulk-copy (async proxy) reads
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, (uint32_t)kTcN);
+    if (row >= 0 && !lost) {
+        bulk_s2g(gY + (size_t)row * H2 + j0, yr, yrow_bytes);
+        bulk_commit();
+        bulk_wait_read();  // the copy has read shared memory: safe to exit
+    }
+    if (warp == 0) tmem_dealloc(tmem, (uint32_t)N);
 }
 
 // ---------------------------------------------------------------- host side
@@ -621,9 +640,11 @@ int tc_launch_t(const TCArgs &g) {
     ep.min_len = g.min_len;
     ep.max_len = g.max_len;
     ep.scale = g.scale;
-    const size_t expand_smem = 1024 + (size_t)3 * g.r * 256;
+    constexpr int N = tc_cols<Ty>();
+    const size_t expand_smem = 1024 + (size_t)g.r * N * 2 + (size_t)2 * g.r * 256 +
+                               (size_t)kTcRows * tc_ypitch<Ty>();
     return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep,
-                  dim3((unsigned)((g.H2 + kTcN - 1) / kTcN), (unsigned)g.slots, 1), 1, expand_smem,
+                  dim3((unsigned)((g.H2 + N - 1) / N), (unsigned)g.slots, 1), 1, expand_smem,
                   g.stream);
 }
 
