@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode-distinct",
                    choices=["tiny", "decode-distinct", "decode-shared", "decode-zipf", "prefill",
-                            "llama7b-stack"])
+                            "llama7b-q", "llama7b-stack"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="host-core budget of the oracle baseline sample")
@@ -72,6 +72,38 @@ def measured_peak():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    """Hash of the CUDA sources: a profile's counters stand only for this code."""
+    import hashlib
+
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "rank_gemv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per update call measured by ncu for this workload (from
+    profiles/traffic.md), or None when the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    want = source_hash()
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 3 and cells[0] == workload and cells[1] == want:
+            try:
+                return float(cells[2])
+            except ValueError:
+                return None
+    return None
 
 
 def config_of(name, w, n_copies=None, l2_note=None):
@@ -354,7 +386,8 @@ def run_ours(args, rank, world, local):
         "bytes_per_step": bytes_step,
         "roofline": {"bound": "hbm", "kernel": kname, "kernels_per_call": per_call,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic(args.workload), "source_hash": source_hash(),
                      "bytes_per_call": bytes_apply, "call_us": apply_s * 1e6},
         "gpu_launches": K * launches_step,
         "clocks": clocks,

@@ -14,8 +14,10 @@
 //   3. griddepcontrol.wait -- the outputs may still be read by the SGMV kernel
 //      launched before on the stream -- then write seg_ptr / idx and pad them
 //      with empty segments up to S_max;
-//   4. stable scatter of row numbers into perm by one warp, 32 rows per step,
-//      ranking equal ids inside a step with __match_any_sync.
+//   4. stable scatter of row numbers into perm, 32 rows per step per warp,
+//      ranking equal ids inside a step with __match_any_sync: for large
+//      batches every warp takes a contiguous chunk of rows, placed from
+//      per-(warp, id) start positions; otherwise one warp walks all rows.
 // The kernel never triggers its dependents early, so the next kernel on the
 // stream starts only after the metadata is complete.
 #include "sgmv_device.cuh"
@@ -29,8 +31,8 @@ __global__ void __launch_bounds__(kBuilderThreads)
     build_segments_kernel(const int32_t *__restrict__ ra, int32_t T, int32_t L,
                           int32_t *__restrict__ perm, int32_t *__restrict__ seg_ptr,
                           int32_t *__restrict__ idx, int32_t *__restrict__ S_out, int32_t S_max,
-                          int *err) {
-    extern __shared__ int cnt[];  // L + 1 bins
+                          int *err, bool multi_warp) {
+    extern __shared__ int cnt[];  // L + 1 bins (then the per-warp table when multi_warp)
     __shared__ int w_c[32], w_n[32];
     __shared__ int s_total;
     const int nb = L + 1;
@@ -116,19 +118,47 @@ __global__ void __launch_bounds__(kBuilderThreads)
     }
     __syncthreads();
 
-    if (warp == 0) {
-        for (int base = 0; base < T; base += 32) {
+    // Stable scatter.  With a per-warp table (multi_warp), the rows are cut
+    // into one contiguous chunk per warp: each warp counts its chunk's ids,
+    // the counts are turned into per-(warp, id) start positions, and every
+    // warp places its chunk in order.  Otherwise one warp walks all rows.
+    const int nw = multi_warp ? nwarps : 1;
+    const int chunk = (T + nw - 1) / nw;
+    int *wpos = cnt + nb;  // [nwarps][nb], multi_warp only
+    if (multi_warp) {
+        for (int e = tid; e < nwarps * nb; e += blockDim.x) wpos[e] = 0;
+        __syncthreads();
+        for (int t = warp * chunk + lane; t < min(T, (warp + 1) * chunk); t += 32) {
+            int key = ra[t] + 1;
+            if (key < 0 || key > L) key = 0;
+            atomicAdd(&wpos[warp * nb + key], 1);
+        }
+        __syncthreads();
+        for (int b = tid; b < nb; b += blockDim.x) {
+            int off = cnt[b];
+            for (int w = 0; w < nwarps; ++w) {
+                const int c = wpos[w * nb + b];
+                wpos[w * nb + b] = off;
+                off += c;
+            }
+        }
+        __syncthreads();
+    }
+    if (warp < nw) {
+        int *run = multi_warp ? wpos + warp * nb : cnt;
+        const int t_end = min(T, (warp + 1) * chunk);
+        for (int base = warp * chunk; base < t_end; base += 32) {
             const int t = base + lane;
-            int key = -1;  // lanes past T get a key no real row has
-            if (t < T) {
+            int key = -1;  // lanes past the chunk get a key no real row has
+            if (t < t_end) {
                 key = ra[t] + 1;
                 if (key < 0 || key > L) key = 0;
             }
             const unsigned grp = __match_any_sync(0xffffffffu, key);
             const int rank = __popc(grp & ((1u << lane) - 1u));
-            if (t < T) perm[cnt[key] + rank] = t;
+            if (t < t_end) perm[run[key] + rank] = t;
             __syncwarp();
-            if (t < T && rank == 0) cnt[key] += __popc(grp);
+            if (t < t_end && rank == 0) run[key] += __popc(grp);
             __syncwarp();
         }
     }
@@ -137,7 +167,10 @@ __global__ void __launch_bounds__(kBuilderThreads)
 int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
                           int32_t *seg_ptr, int32_t *idx, int32_t *S, int32_t S_max, int *err,
                           cudaStream_t stream) {
-    const size_t smem = (size_t)(L + 1) * sizeof(int);
+    // per-warp table when it fits in 96 KB next to the bins and there are
+    // enough rows to share out
+    const bool multi_warp = T > 256 && (size_t)(L + 1) * (kBuilderThreads / 32 + 1) * 4 <= 98304;
+    const size_t smem = (size_t)(L + 1) * sizeof(int) * (multi_warp ? kBuilderThreads / 32 + 1 : 1);
     cudaError_t e = cudaFuncSetAttribute(build_segments_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
@@ -152,7 +185,7 @@ int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int3
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return (int)cudaLaunchKernelEx(&cfg, build_segments_kernel, row_adapter, T, L, perm, seg_ptr,
-                                   idx, S, S_max, err);
+                                   idx, S, S_max, err, multi_warp);
 }
 
 }  // namespace sgmv

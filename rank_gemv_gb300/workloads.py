@@ -22,6 +22,8 @@ Named workloads:
                      by id, H1=4096, H2=11008, r=16, fp16
     prefill          8 segments, lengths uniform on the integers 64..512, adapters
                      0..7, H1=4096, H2=11008, r=64, bf16 (Y fp32 by default)
+    llama7b-q        one projection of llama7b-stack: T=128 rows on 128 adapters,
+                     4096->4096, r=16, fp16 (a small case of the same launch)
     llama7b-stack    32 layers x 7 projections of Llama-2-7B (q,k,v,o 4096->4096,
                      gate,up 4096->11008, down 11008->4096), r=16, T=128 rows,
                      row t on adapter t out of 128, fp16; drawn per projection
@@ -128,6 +130,11 @@ def make(name: str, seed: int = 0, *, y_dtype=None, y0="zeros", shuffle_rows=Fal
     elif name == "decode-zipf":
         T, L, H1, H2, r, dt = 64, 128, 4096, 11008, 16, F16
         ra = torch.sort(zipf_ids(g, T, L)).values
+    elif name == "llama7b-q":
+        # one projection of llama7b-stack (q of layer 0): a small case of the
+        # same kernel launch, for profiling
+        T, L, H1, H2, r, dt = 128, 128, 4096, 4096, 16, F16
+        ra = torch.arange(T, dtype=torch.int32)
     elif name == "prefill":
         L, H1, H2, r, dt = 8, 4096, 11008, 64, BF16
         lens = torch.randint(64, 513, (8,), generator=g, dtype=torch.int64)
