@@ -120,6 +120,93 @@ int choose_cluster(int32_t H1, int32_t H2) {
     return cl;
 }
 
+// Streaming multiprocessors of the current device (looked up once per device).
+int num_sms() {
+    static std::mutex mu;
+    static int cache[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Encodes the B tensor map, then launches.
+int stream_launch(int in_dtype, StreamLaunch &l) {
+    StreamParams &p = l.p;
+    const cuuint64_t es = 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.H2, (cuuint64_t)p.r, (cuuint64_t)p.L};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.H2 * es, (cuuint64_t)p.r * p.H2 * es};
+    const cuuint32_t box[3] = {256, (cuuint32_t)p.r, 1};
+    if (!tmap_encode(&p.tmap_b, in_dtype == SGMV_BF16, 3, p.B, dims, strides, box, false))
+        return (int)cudaErrorInvalidValue;
+    return in_dtype == SGMV_F16 ? stream_launch_f16(l) : stream_launch_bf16(l);
+}
+
+// Shared memory the streaming kernel may use for its ring and buffers.
+// Two CTAs fit on one SM (228 KB), so the next call's CTAs can start, group
+// and request their weights while this call's CTAs still run.
+constexpr uint32_t kStreamSmemBudget = 110u * 1024u;
+constexpr uint32_t kStreamSmemMax = 200u * 1024u;
+
+// Launch shape of the streaming kernel for a batch of T rows whose short
+// segments make at most `slots` 8-row tiles, or false when the kernel does
+// not apply (r not a multiple of 4 or above 32, or more tiles per cluster
+// than its table holds).  The cluster size -- and with it the summation order
+// -- depends on T and the dimensions only, never on the segmentation: as
+// many CTAs per tile (8, 4, 2, 1) as keep CTAs x T within the SM count, each
+// with at least 64 columns of H1 and of H2.
+bool stream_shape(int32_t T, int32_t H1, int32_t H2, int32_t r, int in_dtype, int y_dtype,
+                  int64_t slots, StreamLaunch &l) {
+    if (r % 4 != 0 || r > 32 || slots <= 0) return false;
+    const int nsm = num_sms();
+    if (nsm <= 0) return false;
+    int cl = 8;
+    while (cl > 1 && ((int64_t)cl * T > nsm || H1 < cl * 64 || H2 < cl * 64)) cl >>= 1;
+    const int64_t gmax = std::max(1, nsm / cl);
+    if (ceil_div(T, gmax) > kStreamMaxTiles) return false;
+    StreamParams &p = l.p;
+    const int rk = r <= 16 ? 16 : 32;
+    p.cl = cl;
+    p.G = (int32_t)std::min<int64_t>(slots, gmax);
+    p.hc = round8(ceil_div(H1, cl));
+    p.jc = round8(ceil_div(H2, cl));
+    p.hn = kStreamAElems / rk;
+    const uint32_t es = (uint32_t)elem_size(in_dtype), ys = (uint32_t)elem_size(y_dtype);
+    const uint32_t w = align_up((uint32_t)std::max(p.hn * r, r * kStreamJn) * es, 128);
+    const uint32_t act = align_up(8u * std::max<uint32_t>((uint32_t)p.hn * es, kStreamJn * ys), 128);
+    p.stage_bytes = w + act;
+    p.act_off = w;
+    const uint32_t red = (uint32_t)(kStreamConsumers / 32) * 8u * (uint32_t)rk * 4u;
+    const uint32_t recv = cl > 1 ? 2u * (uint32_t)cl * 8u * (uint32_t)rk * 4u : 0u;
+    const uint32_t vbytes = 2u * 8u * (uint32_t)rk * 4u;
+    const uint32_t tab = (uint32_t)kStreamMaxTiles * 12u * 4u;
+    const int64_t chunks = ceil_div(slots, p.G) * (ceil_div(p.hc, p.hn) + ceil_div(p.jc, kStreamJn));
+    const uint32_t fixed = red + recv + vbytes + tab;
+    // A CTA with few chunks to stream (small batches) keeps to half an SM, so
+    // the next call's CTAs can start beside it and request their weights
+    // early.  A CTA with many chunks, or with large stages, takes a whole SM
+    // for a deeper ring: more bytes in flight per SM.
+    int64_t nst = (int64_t)(kStreamSmemBudget - fixed) / p.stage_bytes;
+    if (nst < 3 || chunks > 2 * nst) nst = (int64_t)(kStreamSmemMax - fixed) / p.stage_bytes;
+    nst = std::min<int64_t>(std::min<int64_t>(nst, kStreamMaxStages), chunks);
+    if (nst < 1) return false;
+    p.nst = (int32_t)nst;
+    p.red_off = (uint32_t)nst * p.stage_bytes;
+    p.recv_off = p.red_off + red;
+    p.v_off = p.recv_off + recv;
+    p.tab_off = p.v_off + vbytes;
+    p.smem_bytes = p.tab_off + tab;
+    l.rk = rk;
+    l.in_dtype = in_dtype;
+    l.y_dtype = y_dtype;
+    return true;
+}
+
 void stage_sizes(CCParams &p, int mode, int elem);
 
 // Fill the derived launch parameters once rows, r, cl, hc and jc are set.
@@ -394,7 +481,34 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     const int64_t slots = tile_slots(T, S, seg_ptr_host, p.rows, 1, cc_max_len);
     if (slots > 65535) return SGMV_ERR_UNSUPPORTED;
     p.err = err;
-    if (slots > 0) {
+    StreamLaunch sl = {};
+    if (slots > 0 &&
+        stream_shape(T, H1, H2, r, in_dtype, y_dtype,
+                     tile_slots(T, S, seg_ptr_host, kRowsMax, 1, cc_max_len), sl)) {
+        StreamParams &q = sl.p;
+        q.y = y;
+        q.x = x;
+        q.A = A;
+        q.B = B;
+        q.perm = perm;
+        q.seg_ptr = seg_ptr;
+        q.idx = idx;
+        q.err = err;
+        q.S = S;
+        q.T = T;
+        q.L = L;
+        q.H1 = H1;
+        q.H2 = H2;
+        q.r = r;
+        q.min_len = 1;
+        q.max_len = cc_max_len;
+        q.scale = scale;
+        sl.grouped = false;
+        sl.stream = static_cast<cudaStream_t>(stream);
+        st = cuda_status("streaming kernel", stream_launch(in_dtype, sl));
+        if (st != SGMV_OK) return st;
+        g_launches = 1;
+    } else if (slots > 0) {
         l.mode = kFused;
         l.y_dtype = y_dtype;
         l.rmax = rmax_of(r);
@@ -467,6 +581,35 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
         // One launch: every CTA groups the rows itself.
         int *err = error_word();
         if (!err) return SGMV_ERR_CUDA;
+        StreamLaunch sl = {};
+        if (stream_shape(T, H1, H2, r, in_dtype, y_dtype,
+                         ((int64_t)T + (int64_t)smax * (kRowsMax - 1)) / kRowsMax, sl)) {
+            StreamParams &q = sl.p;
+            q.y = y;
+            q.x = x;
+            q.A = A;
+            q.B = B;
+            q.err = err;
+            q.row_adapter = row_adapter;
+            q.perm_out = perm;
+            q.seg_out = seg_ptr;
+            q.idx_out = idx;
+            q.S_out = S;
+            q.S_max = smax;
+            q.T = T;
+            q.L = L;
+            q.H1 = H1;
+            q.H2 = H2;
+            q.r = r;
+            q.min_len = 1;
+            q.max_len = INT_MAX;
+            q.scale = scale;
+            sl.grouped = true;
+            sl.stream = static_cast<cudaStream_t>(stream);
+            st = cuda_status("grouped streaming kernel", stream_launch(in_dtype, sl));
+            if (st == SGMV_OK) g_launches = 1;
+            return st;
+        }
         CCLaunch l = {};
         CCParams &p = l.p;
         p.y = y;

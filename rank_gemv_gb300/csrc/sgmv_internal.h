@@ -1,6 +1,7 @@
 // sgmv_internal.h -- parameters shared by the C-ABI host code and the kernels.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (no libcuda link)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -122,6 +123,10 @@ constexpr int kTcMinLen = 64;
 
 int tc_launch(const TCArgs &g);
 
+// Encode a tiled tensor map (f16 / bf16 elements, 128-byte swizzle or none).
+bool tmap_encode(CUtensorMap *m, bool bf16, int rank, const void *ptr, const cuuint64_t *dims,
+                 const cuuint64_t *strides, const cuuint32_t *box, bool swizzle128);
+
 // Launch one CUDA-core kernel; returns a cudaError_t value.
 int cc_launch_f16(const CCLaunch &l);
 int cc_launch_bf16(const CCLaunch &l);
@@ -130,5 +135,57 @@ int cc_launch_bf16(const CCLaunch &l);
 int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int32_t *perm,
                           int32_t *seg_ptr, int32_t *idx, int32_t *S, int32_t S_max, int *err,
                           cudaStream_t stream);
+
+
+// ---- persistent streaming CUDA-core kernel (short segments, r <= 32) -------
+constexpr int kStreamConsumers = 256;                   // 8 compute warps
+constexpr int kStreamThreads = kStreamConsumers + 32;   // + 1 copy-issuing warp
+constexpr int kStreamMaxStages = 8;
+constexpr int kStreamMaxTiles = 64;   // tiles one cluster walks in one launch
+constexpr int kStreamJn = 2 * kStreamConsumers;  // columns of one B chunk (two per compute thread)
+constexpr int kStreamAElems = 8192;   // elements of one A chunk at the rank bound
+
+// One launch of the streaming kernel.  Grid: x = CTA rank in the cluster
+// (slices [rank*hc, ...) of H1 and [rank*jc, ...) of H2), y = cluster; cluster
+// c walks the tiles c, c + G, c + 2G, ... of the batch.  Every CTA streams its
+// slices of the tiles' A and B through a ring of `nst` shared-memory stages.
+struct StreamParams {
+    CUtensorMap tmap_b;  // B as [L][r][H2], box {256, r, 1}, no swizzle
+    void *y;
+    const void *x;
+    const void *A;
+    const void *B;
+    const int32_t *perm;
+    const int32_t *seg_ptr;
+    const int32_t *idx;
+    int *err;
+    const int32_t *row_adapter;  // grouped form: adapter id of every row
+    int32_t *perm_out;           // grouped form, optional: grouping written out
+    int32_t *seg_out;
+    int32_t *idx_out;
+    int32_t *S_out;
+    int32_t S_max;
+    int32_t S, T, L, H1, H2, r;
+    int32_t cl, G;               // CTAs per cluster, clusters
+    int32_t hc, jc;              // columns of H1 / H2 per CTA (multiples of 8)
+    int32_t hn;                  // columns of one A chunk (kStreamAElems / rank bound)
+    int32_t nst;                 // ring stages
+    uint32_t stage_bytes, act_off;  // bytes per stage; offset of the x / y rows in it
+    uint32_t red_off, recv_off, v_off, tab_off, smem_bytes;
+    int32_t min_len, max_len;
+    float scale;
+};
+
+struct StreamLaunch {
+    StreamParams p;
+    int in_dtype, y_dtype;
+    int rk;          // 16 or 32: compile-time bound on r
+    bool grouped;
+    cudaStream_t stream;
+};
+
+// Launch the streaming kernel; returns a cudaError_t value.
+int stream_launch_f16(const StreamLaunch &l);
+int stream_launch_bf16(const StreamLaunch &l);
 
 }  // namespace sgmv

@@ -1,0 +1,663 @@
+// sgmv_stream.cuh -- persistent streaming CUDA-core SGMV kernel for
+// decode-sized segments (rank r <= 32, r a multiple of 4).
+//
+// Method ("Punica: when LoRA fine-tuned models need multi-tenant serving",
+// omica.com.cn article, §2.2): for every row of a segment, shrink
+// v = x . A[idx] with A gathered out of the stacked adapters, then expand
+// y += scale * v . B[idx].  Decode rows do about one flop per weight byte, so
+// the kernel is built to keep HBM busy rather than the arithmetic units.
+//
+// Work decomposition:
+//   * a tile is up to 8 consecutive rows of one segment (one adapter);
+//   * CL CTAs form a cluster (CL = 1, 2, 4 or 8, fewer for larger batches);
+//     CTA `rank` owns the slice [rank*hc, ...) of H1 and [rank*jc, ...) of H2;
+//   * cluster c walks the tiles c, c + G, c + 2G, ...: the kernel is
+//     persistent over tiles, and each CTA streams its slices of every tile's
+//     A and B through a ring of shared-memory stages: one 1-D bulk (TMA) copy
+//     per A chunk (contiguous in A[a]), tiled tensor (TMA) boxes of 256
+//     columns x r rows per B chunk, one bulk copy per x or y row.  One warp
+//     only issues copies; eight warps compute.  The ring order is A(0); A(1) B(0); A(2) B(1); ...: the shrink of tile m runs
+//     before the expand of tile m-1, so the cluster exchange of tile m-1's v
+//     is hidden behind it, and the copies never wait for an exchange;
+//   * partial v of a CTA's H1 slice goes to every CTA of the cluster through
+//     distributed shared memory (double-buffered by tile parity, one mbarrier
+//     per buffer with one release-arrive per CTA), and each CTA sums the
+//     partials in rank order: the same bits in every CTA.
+// Summation order of every output element: fixed by (H1, H2, r, CL) alone --
+// not by the number of rows in a tile, the chunking or the tile assignment --
+// so cutting a segment into tiles differently changes no bit.
+// Programmatic dependent launch: segment metadata and weights are read before
+// griddepcontrol.wait; x and y only after it.
+#pragma once
+
+#include <climits>
+
+#include "sgmv_device.cuh"
+#include "sgmv_internal.h"
+
+namespace sgmv {
+
+constexpr int kStreamWarps = kStreamConsumers / 32;
+constexpr int kTileRows = 8;
+
+__device__ __forceinline__ void consumers_sync() { named_sync<1, kStreamConsumers>(); }
+
+// Walks a CTA's ring in order: A(0); then for m = 1 .. nt-1: A(m), B(m-1);
+// then B(nt-1).  Chunk = A(blk, i) when !isB, else B(blk - 1, i).
+struct RingIter {
+    int blk, isB, i, nt, nA, nB;
+    __device__ __forceinline__ void start(int nt_, int nA_, int nB_) {
+        nt = nt_;
+        nA = nA_;
+        nB = nB_;
+        blk = 0;
+        isB = 0;
+        i = 0;
+        settle();
+    }
+    __device__ __forceinline__ void settle() {
+        for (;;) {
+            if (blk > nt) return;
+            if (!isB) {
+                if (blk < nt && i < nA) return;
+                isB = 1;
+                i = 0;
+            }
+            if (blk >= 1 && i < nB) return;
+            ++blk;
+            isB = 0;
+            i = 0;
+        }
+    }
+    __device__ __forceinline__ void next() {
+        ++i;
+        settle();
+    }
+    __device__ __forceinline__ int tile() const { return isB ? blk - 1 : blk; }
+};
+
+// Bounded wait of a compute thread; after a timeout the error word is set, the
+// wait is repeated once (copies still in flight land before the CTA moves on)
+// and the thread stops writing y.
+__device__ __forceinline__ void stream_wait(uint64_t *bar, uint32_t parity, bool &lost, int *err) {
+    if (!mbar_wait(bar, parity)) {
+        set_error(err, kErrTimeout);
+        mbar_wait(bar, parity);
+        lost = true;
+    }
+}
+
+// Shrink of one tile with R rows (R >= the tile's rows): the CTA's partial of
+// v over its H1 slice, one warp partial per warp written to red[warp][t][k].
+// Thread (warp, lane) owns k-quad kq = lane % (RK/4) and the columns
+// h = warp*HL + lane/(RK/4) + HSTR*j of the slice, summed in increasing h;
+// the HL lanes of a k-quad are then summed by a butterfly in a fixed order.
+template <typename Tin, int RK, int R>
+__device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes, uint32_t act_off,
+                                              int nst, int &q, int nA, int hlen, int hn, int rk,
+                                              uint64_t *full, uint64_t *empty, float *red,
+                                              bool &lost, int *err) {
+    constexpr int KQ = RK / 4, HL = 32 / KQ, HSTR = kStreamWarps * HL;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int kq = lane % KQ, hl = lane / KQ;
+    const int hoff = warp * HL + hl;
+    const bool kact = 4 * kq < rk;
+    float acc[R][4];
+#pragma unroll
+    for (int t = 0; t < R; ++t)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
+    for (int i = 0; i < nA; ++i, ++q) {
+        const int s = q % nst;
+        stream_wait(&full[s], (uint32_t)((q / nst) & 1), lost, err);
+        const int nh = min(hn, hlen - i * hn);
+        const uint8_t *base = sm + (size_t)s * stage_bytes;
+        const Tin *As = reinterpret_cast<const Tin *>(base);
+        const Tin *Xs = reinterpret_cast<const Tin *>(base + act_off);
+        if (kact) {
+#pragma unroll 2
+            for (int h = hoff; h < nh; h += HSTR) {
+                const uint2 av = lds64(As + h * rk + 4 * kq);
+                float a[4];
+                unpack2<Tin>(av.x, a[0], a[1]);
+                unpack2<Tin>(av.y, a[2], a[3]);
+#pragma unroll
+                for (int t = 0; t < R; ++t) {
+                    const unsigned short xb = lds16(Xs + t * hn + h);
+                    const float x = to_f<Tin>(*reinterpret_cast<const Tin *>(&xb));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc[t][u] = fmaf(x, a[u], acc[t][u]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+#pragma unroll
+    for (int off = 16; off >= KQ; off >>= 1)
+#pragma unroll
+        for (int t = 0; t < R; ++t)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[t][u] += __shfl_xor_sync(0xffffffffu, acc[t][u], off);
+    if (hl == 0 && kact)
+#pragma unroll
+        for (int t = 0; t < R; ++t)
+            sts128(red + (warp * kTileRows + t) * RK + 4 * kq,
+                   make_uint4(__float_as_uint(acc[t][0]), __float_as_uint(acc[t][1]),
+                              __float_as_uint(acc[t][2]), __float_as_uint(acc[t][3])));
+}
+
+// Expand of one tile with R rows: y[row, j] += scale * v . B[a][:, j] for the
+// CTA's H2 slice, two adjacent columns per thread, r-sum in increasing k.
+template <typename Tin, typename Ty, int RK, int R>
+__device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes, uint32_t act_off,
+                                              int nst, int &q, int nB, int jlen, int j0, int rk,
+                                              const float *sv, const int (&row)[kTileRows],
+                                              Ty *gY, int H2, float scale, uint64_t *full,
+                                              uint64_t *empty, bool &lost, int *err) {
+    const int tid = threadIdx.x;
+    const int c = 2 * tid;
+    // B chunk in shared memory: boxes of 256 columns, [box][k][256]
+    const int boff = (c >> 8) * rk * 256 + (c & 255);
+    for (int i = 0; i < nB; ++i, ++q) {
+        const int s = q % nst;
+        stream_wait(&full[s], (uint32_t)((q / nst) & 1), lost, err);
+        const int nj = min(kStreamJn, jlen - i * kStreamJn);
+        const uint8_t *base = sm + (size_t)s * stage_bytes;
+        const Tin *Bs = reinterpret_cast<const Tin *>(base);
+        const Ty *Ys = reinterpret_cast<const Ty *>(base + act_off);
+        if (c < nj) {
+            float acc[R][2];
+#pragma unroll
+            for (int t = 0; t < R; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < RK; kk += 4) {
+                if (kk < rk) {
+                    float v[R][4];
+#pragma unroll
+                    for (int t = 0; t < R; ++t) {
+                        const uint4 u = lds128(sv + t * RK + kk);
+                        v[t][0] = __uint_as_float(u.x);
+                        v[t][1] = __uint_as_float(u.y);
+                        v[t][2] = __uint_as_float(u.z);
+                        v[t][3] = __uint_as_float(u.w);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float b0, b1;
+                        unpack2<Tin>(lds32(Bs + boff + (kk + e) * 256), b0, b1);
+#pragma unroll
+                        for (int t = 0; t < R; ++t) {
+                            acc[t][0] = fmaf(v[t][e], b0, acc[t][0]);
+                            acc[t][1] = fmaf(v[t][e], b1, acc[t][1]);
+                        }
+                    }
+                }
+            }
+            if (!lost) {
+                const int jg = j0 + i * kStreamJn + c;
+#pragma unroll
+                for (int t = 0; t < R; ++t) {
+                    if (row[t] < 0) continue;
+                    float y0, y1;
+                    lds2<Ty>(Ys + t * kStreamJn + c, y0, y1);
+                    st2<Ty>(gY + (size_t)row[t] * H2 + jg, fmaf(scale, acc[t][0], y0),
+                            fmaf(scale, acc[t][1], y1));
+                }
+            }
+        }
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+template <typename Tin, typename Ty, int RK, bool GROUPED>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+    sgmv_stream_kernel(const __grid_constant__ StreamParams P) {
+    // Parameters read once into registers (see sgmv_cc.cuh).
+    const int T = P.T, L = P.L, H1 = P.H1, H2 = P.H2, rk = P.r;
+    const int ncl = P.cl, G = P.G, hn = P.hn, nst = P.nst;
+    const int min_len = P.min_len, max_len = P.max_len;
+    const uint32_t stage_bytes = P.stage_bytes, act_off = P.act_off;
+    const float scale = P.scale;
+    int *const err = P.err;
+
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ __align__(8) uint64_t full[kStreamMaxStages], empty[kStreamMaxStages], vfull[2];
+    __shared__ int s_wsum[kStreamThreads / 32];
+    __shared__ int s_total;
+    constexpr int kG = GROUPED ? kGroupMaxT : 4;
+    __shared__ __align__(16) int g_key[kG];
+    __shared__ __align__(16) int g_cnt[kG];
+    __shared__ __align__(16) int g_rank[kG];
+    __shared__ int g_sperm[kG];
+
+    float *const red = reinterpret_cast<float *>(sm + P.red_off);    // [8 warps][8][RK]
+    float *const recv = reinterpret_cast<float *>(sm + P.recv_off);  // [2][cl][8][RK]
+    float *const s_v = reinterpret_cast<float *>(sm + P.v_off);      // [2][8][RK]
+    int *const tab = reinterpret_cast<int *>(sm + P.tab_off);        // [tiles][4]: p0, n, a
+    int *const trow = tab + 4 * kStreamMaxTiles;                     // [tiles][8] rows
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = (int)blockIdx.x, cid = (int)blockIdx.y;
+    const bool report = rank == 0 && cid == 0;
+
+    // The next kernel on the stream may start as soon as every CTA of this
+    // one has: it reads nothing this kernel writes before its own
+    // griddepcontrol.wait, which still waits for this grid to finish.
+    pdl_trigger();
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 2);  // weights, then the x / y rows
+            mbar_init(&empty[s], kStreamWarps);
+        }
+        mbar_init(&vfull[0], (uint32_t)ncl);
+        mbar_init(&vfull[1], (uint32_t)ncl);
+        mbar_init_fence();
+        s_total = 0;
+    }
+
+    // ---- this cluster's tiles: tab[m] = global tile cid + m*G ---------------
+    int g_less = 0, g_dless = 0, g_nseg = 0, gkey = -1, grank = 0;
+    if (!GROUPED) {
+        // Tiles per segment, block-scanned over the segments in order.
+        const int S = P.S;
+        const int32_t *seg_ptr = P.seg_ptr;
+        const int32_t *idx = P.idx;
+        auto seg = [&](int s, int &b, int &len, int &a, bool rep) {
+            b = seg_ptr[s];
+            const int e = seg_ptr[s + 1];
+            a = idx[s];
+            if (b < 0 || e < b || e > T) {
+                if (rep) set_error(err, kErrBadSegments);
+                return 0;
+            }
+            len = e - b;
+            if (len == 0 || a == -1 || len < min_len || len > max_len) return 0;
+            if (a < -1 || a >= L) {
+                if (rep) set_error(err, kErrBadIndex);
+                return 0;
+            }
+            return (len + kTileRows - 1) / kTileRows;
+        };
+        const int per = (S + kStreamThreads - 1) / kStreamThreads;
+        const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+        int own = 0;
+        for (int s = s0; s < s1; ++s) {
+            int b, len, a;
+            own += seg(s, b, len, a, report);
+        }
+        int incl = own;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            constexpr int NW = kStreamThreads / 32;
+            const int w = lane < NW ? s_wsum[lane] : 0;
+            int wi = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += o;
+            }
+            if (lane < NW) s_wsum[lane] = wi - w;
+            if (lane == NW - 1) s_total = wi;
+        }
+        __syncthreads();
+        int gbase = s_wsum[warp] + incl - own;  // first global tile of this thread's segments
+        for (int s = s0; s < s1; ++s) {
+            int b = 0, len = 0, a = 0;
+            const int n = seg(s, b, len, a, false);
+            // tiles j of this segment with (gbase + j) % G == cid
+            for (int j = ((cid - gbase % G) % G + G) % G; j < n; j += G) {
+                const int m = (gbase + j) / G;
+                if (m < kStreamMaxTiles) {
+                    tab[4 * m] = b + kTileRows * j;
+                    tab[4 * m + 1] = min(kTileRows, len - kTileRows * j);
+                    tab[4 * m + 2] = a;
+                }
+            }
+            gbase += n;
+        }
+    } else {
+        // Every CTA groups the batch itself (T <= kGroupMaxT): sorted position
+        // of row t = (#rows with a smaller id) + (#earlier rows with its id);
+        // tiles are numbered over ids in ascending order, 8 rows at a time.
+        // Keys past T are INT_MAX and ranks past T are 1, so that padded
+        // entries count for nothing below.
+        const int32_t *ra = P.row_adapter;
+        const int T4 = (T + 3) & ~3;
+        if (tid < T4) {
+            if (tid < T) {
+                gkey = ra[tid];
+                if (gkey < -1 || gkey >= L) {
+                    if (report) set_error(err, kErrBadIndex);
+                    gkey = -1;
+                }
+            }
+            g_key[tid] = tid < T ? gkey : INT_MAX;
+            if (tid >= T) g_rank[tid] = 1;
+        }
+        __syncthreads();
+        int cnt = 0;
+        if (tid < T) {
+            for (int u = 0; u < T4; u += 4) {
+                const uint4 k4 = lds128(g_key + u);
+                const int ku[4] = {(int)k4.x, (int)k4.y, (int)k4.z, (int)k4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    g_less += ku[e] < gkey;
+                    cnt += ku[e] == gkey;
+                    grank += (ku[e] == gkey) & (u + e < tid);
+                }
+            }
+            g_cnt[tid] = cnt;
+            g_rank[tid] = grank;
+            g_sperm[g_less + grank] = tid;
+        }
+        __syncthreads();
+        if (tid < T) {
+            int tb = 0;  // tiles of the adapters with a smaller id
+            for (int u = 0; u < T4; u += 4) {
+                const uint4 k4 = lds128(g_key + u), r4 = lds128(g_rank + u), c4 = lds128(g_cnt + u);
+                const int ku[4] = {(int)k4.x, (int)k4.y, (int)k4.z, (int)k4.w};
+                const int rr[4] = {(int)r4.x, (int)r4.y, (int)r4.z, (int)r4.w};
+                const int cc[4] = {(int)c4.x, (int)c4.y, (int)c4.z, (int)c4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (rr[e] == 0 && ku[e] < gkey) {
+                        ++g_dless;
+                        if (ku[e] >= 0) tb += (cc[e] + kTileRows - 1) / kTileRows;
+                    }
+                }
+            }
+            if (gkey >= 0 && grank % kTileRows == 0) {
+                const int gt = tb + grank / kTileRows;
+                if (gt % G == cid && gt / G < kStreamMaxTiles) {
+                    const int m = gt / G;
+                    tab[4 * m] = g_less + grank;
+                    tab[4 * m + 1] = min(kTileRows, cnt - grank);
+                    tab[4 * m + 2] = gkey;
+                }
+                if (grank == 0) atomicAdd(&s_total, (cnt + kTileRows - 1) / kTileRows);
+            }
+        }
+        g_nseg = __syncthreads_count(tid < T && grank == 0);
+    }
+    __syncthreads();
+    const int ntot = s_total;
+    int nt = ntot > cid ? (ntot - 1 - cid) / G + 1 : 0;
+    if (nt > kStreamMaxTiles) {
+        if (rank == 0) set_error(err, kErrBadSegments);
+        nt = kStreamMaxTiles;
+    }
+    // Grouped form, CTA (0,0): the grouping is written out for later calls,
+    // after the previous kernel on the stream (which may still read it).
+    auto write_meta = [&]() {
+        if (tid < T) {
+            P.perm_out[g_less + grank] = tid;
+            if (grank == 0) {
+                P.seg_out[g_dless] = g_less;
+                P.idx_out[g_dless] = gkey;
+            }
+        }
+        if (tid == 0) {
+            P.seg_out[g_nseg] = T;
+            *P.S_out = g_nseg;
+        }
+        for (int sidx = g_nseg + tid; sidx < P.S_max; sidx += kStreamThreads) {
+            P.idx_out[sidx] = -1;
+            P.seg_out[sidx + 1] = T;
+        }
+    };
+    const bool meta_out = GROUPED && report && P.perm_out != nullptr;
+    if (nt == 0) {  // the same for every CTA of the cluster
+        if (meta_out) {
+            pdl_wait();
+            write_meta();
+        }
+        return;
+    }
+    if (ncl > 1) cluster_arrive_relaxed();  // waited on before the first peer access
+
+    const int h0 = min(H1, rank * P.hc), h1 = min(H1, h0 + P.hc);
+    const int j0 = min(H2, rank * P.jc), j1 = min(H2, j0 + P.jc);
+    const int nA = (h1 - h0 + hn - 1) / hn;
+    const int nB = (j1 - j0 + kStreamJn - 1) / kStreamJn;
+    const int total = nt * (nA + nB);
+
+    if (warp == kStreamWarps) {
+        // ---- copy warp: fills the ring in the order the compute warps use it.
+        // Weights need only the adapter ids, so they are requested while the
+        // compute warps look up the tiles' rows.
+        const Tin *gA = static_cast<const Tin *>(P.A);
+        const Tin *gX = static_cast<const Tin *>(P.x);
+        const Ty *gY = static_cast<const Ty *>(P.y);
+        const uint32_t bbox = (uint32_t)rk * 256u * (uint32_t)sizeof(Tin);
+        RingIter it;
+        int cur_a = -1, cur_r = -1, a = 0, row = -1;
+        uint32_t nvalid = 0;
+        auto issue_w = [&](int s) {  // weights of chunk `it` into stage s
+            if (it.tile() != cur_a) {
+                cur_a = it.tile();
+                a = (int)lds32(tab + 4 * cur_a + 2);
+            }
+            uint8_t *dst = sm + (size_t)s * stage_bytes;
+            if (lane == 0) {
+                if (!it.isB) {
+                    const int hlo = h0 + it.i * hn, n = min(hn, h1 - hlo);
+                    const uint32_t bytes = (uint32_t)(n * rk) * (uint32_t)sizeof(Tin);
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    bulk_g2s(dst, gA + ((size_t)a * H1 + hlo) * rk, bytes, &full[s]);
+                } else {
+                    const int jlo = j0 + it.i * kStreamJn, n = min(kStreamJn, j1 - jlo);
+                    const int nbox = (n + 255) >> 8;
+                    mbar_arrive_expect_tx(&full[s], bbox * (uint32_t)nbox);
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_load_3d(dst + bx * bbox, &P.tmap_b, jlo + 256 * bx, 0, a, &full[s]);
+                }
+            }
+        };
+        auto issue_act = [&](int s) {  // x or y rows of chunk `it` into stage s
+            if (it.tile() != cur_r) {
+                cur_r = it.tile();
+                row = lane < kTileRows ? (int)lds32(trow + kTileRows * cur_r + lane) : -1;
+                nvalid = (uint32_t)__popc(__ballot_sync(0xffffffffu, row >= 0));
+            }
+            uint8_t *dst = sm + (size_t)s * stage_bytes + act_off;
+            if (!it.isB) {
+                const int hlo = h0 + it.i * hn, n = min(hn, h1 - hlo);
+                const uint32_t rowb = (uint32_t)n * (uint32_t)sizeof(Tin);
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], rowb * nvalid);
+                __syncwarp();
+                if (row >= 0)
+                    bulk_g2s(dst + (size_t)lane * hn * sizeof(Tin), gX + (size_t)row * H1 + hlo,
+                             rowb, &full[s]);
+            } else {
+                const int jlo = j0 + it.i * kStreamJn, n = min(kStreamJn, j1 - jlo);
+                const uint32_t rowb = (uint32_t)n * (uint32_t)sizeof(Ty);
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], rowb * nvalid);
+                __syncwarp();
+                if (row >= 0)
+                    bulk_g2s(dst + (size_t)lane * kStreamJn * sizeof(Ty),
+                             gY + (size_t)row * H2 + jlo, rowb, &full[s]);
+            }
+        };
+        const int pre = min(nst, total);
+        it.start(nt, nA, nB);
+        for (int q = 0; q < pre; ++q, it.next()) issue_w(q);  // before the previous kernel ends
+        named_sync<2, kStreamThreads>();  // the rows table is complete
+        pdl_wait();
+        it.start(nt, nA, nB);
+        for (int q = 0; q < pre; ++q, it.next()) issue_act(q);
+        for (int q = pre, s = pre % nst; q < total; ++q, it.next()) {
+            if (!mbar_wait(&empty[s], (uint32_t)((q / nst - 1) & 1))) set_error(err, kErrTimeout);
+            __syncwarp();
+            issue_w(s);
+            issue_act(s);
+            if (++s == nst) s = 0;
+        }
+        if (ncl > 1) cluster_wait();
+    } else {
+        // ---- compute warps -------------------------------------------------
+        // Physical rows of the tiles; invalid perm entries are skipped and reported.
+        for (int e = tid; e < nt * kTileRows; e += kStreamConsumers) {
+            const int m = e / kTileRows, t = e % kTileRows;
+            int row = -1;
+            if (t < tab[4 * m + 1]) {
+                const int p = tab[4 * m] + t;
+                row = GROUPED ? g_sperm[p] : (P.perm ? P.perm[p] : p);
+                if (row < 0 || row >= T) {
+                    if (rank == 0) set_error(err, kErrBadIndex);
+                    row = -1;
+                }
+            }
+            trow[e] = row;
+        }
+        named_sync<2, kStreamThreads>();
+        pdl_wait();  // y is written below: only after the previous kernel
+        if (meta_out) write_meta();
+        if (ncl > 1) cluster_wait();  // every CTA of the cluster has started
+        Ty *gY = static_cast<Ty *>(P.y);
+        bool lost = false;
+        int q = 0;
+        float part = 0.f;  // element (t, k) = (tid / rk, tid % rk) of this CTA's partial v
+        for (int m = 0; m <= nt; ++m) {
+            if (m < nt) {
+                const int n = (int)lds32(tab + 4 * m + 1);
+                if (n <= 1)
+                    stream_shrink<Tin, RK, 1>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                                              full, empty, red, lost, err);
+                else if (n <= 2)
+                    stream_shrink<Tin, RK, 2>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                                              full, empty, red, lost, err);
+                else if (n <= 4)
+                    stream_shrink<Tin, RK, 4>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                                              full, empty, red, lost, err);
+                else
+                    stream_shrink<Tin, RK, 8>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                                              full, empty, red, lost, err);
+                consumers_sync();
+                part = 0.f;
+                if (tid < n * rk) {
+                    const int t = tid / rk, k = tid - (tid / rk) * rk;
+#pragma unroll
+                    for (int w = 0; w < kStreamWarps; ++w)
+                        part += ldsf(red + (w * kTileRows + t) * RK + k);
+                    if (ncl == 1) stsf(s_v + ((m & 1) * kTileRows + t) * RK + k, part);
+                }
+            }
+            if (ncl > 1) {
+                if (m >= 1) {
+                    // v of tile m-1: every CTA's partial has arrived
+                    const int b = (m - 1) & 1;
+                    if (!mbar_wait_cluster(&vfull[b], (uint32_t)(((m - 1) >> 1) & 1))) {
+                        set_error(err, kErrTimeout);
+                        mbar_wait_cluster(&vfull[b], (uint32_t)(((m - 1) >> 1) & 1));
+                        lost = true;
+                    }
+                    const int n1 = (int)lds32(tab + 4 * (m - 1) + 1);
+                    if (tid < n1 * rk) {
+                        const int t = tid / rk, k = tid - (tid / rk) * rk;
+                        float sum = 0.f;
+                        for (int c = 0; c < ncl; ++c)
+                            sum += ldsf(recv + ((b * ncl + c) * kTileRows + t) * RK + k);
+                        stsf(s_v + (b * kTileRows + t) * RK + k, sum);
+                    }
+                }
+                if (m < nt) {
+                    // Push this CTA's partial of tile m into slot (m & 1, rank)
+                    // of every CTA.  The slot was last read for tile m-2, before
+                    // its owner arrived for tile m-1, which the wait above saw.
+                    const int b = m & 1;
+                    const int n = (int)lds32(tab + 4 * m + 1);
+                    if (tid < n * rk) {
+                        const int t = tid / rk, k = tid - (tid / rk) * rk;
+                        float *slot = recv + ((b * ncl + rank) * kTileRows + t) * RK + k;
+                        for (int c = 0; c < ncl; ++c) st_peer(peer_addr(slot, (uint32_t)c), part);
+                    }
+                    consumers_sync();
+                    if (tid < ncl) {
+                        fence_acq_rel_cluster();
+                        mbar_arrive_remote(peer_addr(&vfull[b], (uint32_t)tid));
+                    }
+                }
+            }
+            consumers_sync();  // s_v of tile m-1 is complete
+            if (m >= 1) {
+                const int mm = m - 1;
+                const int n = (int)lds32(tab + 4 * mm + 1);
+                int row[kTileRows];
+#pragma unroll
+                for (int t = 0; t < kTileRows; ++t) row[t] = (int)lds32(trow + kTileRows * mm + t);
+                const float *sv = s_v + (mm & 1) * kTileRows * RK;
+                if (n <= 1)
+                    stream_expand<Tin, Ty, RK, 1>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                                                  rk, sv, row, gY, H2, scale, full, empty, lost, err);
+                else if (n <= 2)
+                    stream_expand<Tin, Ty, RK, 2>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                                                  rk, sv, row, gY, H2, scale, full, empty, lost, err);
+                else if (n <= 4)
+                    stream_expand<Tin, Ty, RK, 4>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                                                  rk, sv, row, gY, H2, scale, full, empty, lost, err);
+                else
+                    stream_expand<Tin, Ty, RK, 8>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                                                  rk, sv, row, gY, H2, scale, full, empty, lost, err);
+            }
+        }
+    }
+    // No CTA leaves while a peer may still write into its shared memory.
+    if (ncl > 1) cluster_sync();
+}
+
+// ---- host-side launcher for one input type ----------------------------------
+template <typename Tin, typename Ty, int RK>
+static void *stream_pick(bool grouped) {
+    return grouped ? (void *)sgmv_stream_kernel<Tin, Ty, RK, true>
+                   : (void *)sgmv_stream_kernel<Tin, Ty, RK, false>;
+}
+
+template <typename Tin, typename Ty>
+static void *stream_pick_rk(int rk, bool grouped) {
+    return rk == 16 ? stream_pick<Tin, Ty, 16>(grouped) : stream_pick<Tin, Ty, 32>(grouped);
+}
+
+template <typename Tin>
+static int stream_launch_impl(const StreamLaunch &l) {
+    void *fn;
+    switch (l.y_dtype) {
+        case 0: fn = stream_pick_rk<Tin, __half>(l.rk, l.grouped); break;
+        case 1: fn = stream_pick_rk<Tin, __nv_bfloat16>(l.rk, l.grouped); break;
+        default: fn = stream_pick_rk<Tin, float>(l.rk, l.grouped); break;
+    }
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)l.p.smem_bytes);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)l.p.cl, (unsigned)l.p.G, 1);
+    cfg.blockDim = dim3(kStreamThreads, 1, 1);
+    cfg.dynamicSmemBytes = l.p.smem_bytes;
+    cfg.stream = l.stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (l.p.cl > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)l.p.cl;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    void *args[] = {(void *)&l.p};
+    return (int)cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace sgmv

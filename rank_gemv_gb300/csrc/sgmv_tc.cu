@@ -23,6 +23,8 @@
 //   then owns one row: tcgen05.ld 32 columns at a time, y += scale * acc in
 //   fp32, rounded once to y's type.
 // Every mbarrier wait is bounded; TMEM is freed on every path.
+#include <mutex>
+
 #include <cuda.h>  // CUtensorMap and the encoder's signature (no libcuda link)
 
 #include <cstring>
@@ -120,14 +122,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 // 16-byte asynchronous copy; src_bytes 0 writes zeros.
@@ -513,35 +507,46 @@ __global__ void __launch_bounds__(kTcThreads)
 // ---------------------------------------------------------------- host side
 namespace {
 
-typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiled encoder() {
-    static EncodeTiled fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link libcuda), looked up once.
+EncodeTiledFn tiled_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    }
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
     return fn;
 }
 
-bool encode(CUtensorMap *m, bool bf16, int rank, const void *ptr, const cuuint64_t *dims,
-            const cuuint64_t *strides, const cuuint32_t *box) {
-    EncodeTiled fn = encoder();
+}  // namespace
+
+bool tmap_encode(CUtensorMap *m, bool bf16, int rank, const void *ptr, const cuuint64_t *dims,
+                 const cuuint64_t *strides, const cuuint32_t *box, bool swizzle128) {
+    EncodeTiledFn fn = tiled_encoder();
     if (!fn) return false;
     const cuuint32_t es[3] = {1, 1, 1};
     return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
               (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool encode(CUtensorMap *m, bool bf16, int rank, const void *ptr, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box) {
+    return sgmv::tmap_encode(m, bf16, rank, ptr, dims, strides, box, true);
 }
 
 template <typename K, typename P>
