@@ -135,15 +135,28 @@ int num_sms() {
     return cache[dev];
 }
 
-// Encodes the B tensor map, then launches.
+// Encodes the B tensor map, then launches.  With H2 and every CTA's first
+// column multiples of 256, B is viewed as [L][H2/256][r][256] so that one
+// copy brings a whole chunk; otherwise as [L][r][H2], one copy per 256 columns.
 int stream_launch(int in_dtype, StreamLaunch &l) {
     StreamParams &p = l.p;
+    const bool bf16 = in_dtype == SGMV_BF16;
     const cuuint64_t es = 2;
-    const cuuint64_t dims[3] = {(cuuint64_t)p.H2, (cuuint64_t)p.r, (cuuint64_t)p.L};
-    const cuuint64_t strides[2] = {(cuuint64_t)p.H2 * es, (cuuint64_t)p.r * p.H2 * es};
-    const cuuint32_t box[3] = {256, (cuuint32_t)p.r, 1};
-    if (!tmap_encode(&p.tmap_b, in_dtype == SGMV_BF16, 3, p.B, dims, strides, box, false))
-        return (int)cudaErrorInvalidValue;
+    p.b4d = 0;
+    if (p.H2 % 256 == 0 && p.jc % 256 == 0) {
+        const cuuint64_t dims[4] = {256, (cuuint64_t)p.r, (cuuint64_t)p.H2 / 256, (cuuint64_t)p.L};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.H2 * es, 256 * es,
+                                       (cuuint64_t)p.r * p.H2 * es};
+        const cuuint32_t box[4] = {256, (cuuint32_t)p.r, (cuuint32_t)(p.hn / 256), 1};
+        p.b4d = tmap_encode(&p.tmap_b, bf16, 4, p.B, dims, strides, box, false) ? 1 : 0;
+    }
+    if (!p.b4d) {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.H2, (cuuint64_t)p.r, (cuuint64_t)p.L};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.H2 * es, (cuuint64_t)p.r * p.H2 * es};
+        const cuuint32_t box[3] = {256, (cuuint32_t)p.r, 1};
+        if (!tmap_encode(&p.tmap_b, bf16, 3, p.B, dims, strides, box, false))
+            return (int)cudaErrorInvalidValue;
+    }
     return in_dtype == SGMV_F16 ? stream_launch_f16(l) : stream_launch_bf16(l);
 }
 
@@ -153,16 +166,23 @@ int stream_launch(int in_dtype, StreamLaunch &l) {
 constexpr uint32_t kStreamSmemBudget = 110u * 1024u;
 constexpr uint32_t kStreamSmemMax = 200u * 1024u;
 
-// Launch shape of the streaming kernel for a batch of T rows whose short
-// segments make at most `slots` 8-row tiles, or false when the kernel does
-// not apply (r not a multiple of 4 or above 32, or more tiles per cluster
-// than its table holds).  The cluster size -- and with it the summation order
+// Launch shape of the streaming kernel for a batch of T rows in S segments
+// (the last max_len rows long at most), or false when the kernel does not
+// apply (r not a multiple of 4 or above 32, or more tiles per cluster than its
+// table holds).  Rows per tile: 1 when segments average up to 2 rows (every
+// row streams its adapter on its own; rows that share an adapter read it
+// again from L2), up to 8 for longer segments, whose rows then share each
+// staged weight chunk.  The cluster size -- and with it the summation order
 // -- depends on T and the dimensions only, never on the segmentation: as
 // many CTAs per tile (8, 4, 2, 1) as keep CTAs x T within the SM count, each
 // with at least 64 columns of H1 and of H2.
-bool stream_shape(int32_t T, int32_t H1, int32_t H2, int32_t r, int in_dtype, int y_dtype,
-                  int64_t slots, StreamLaunch &l) {
-    if (r % 4 != 0 || r > 32 || slots <= 0) return false;
+bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len, int32_t H1,
+                  int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l) {
+    if (r % 4 != 0 || r > 32 || T <= 0 || S <= 0) return false;
+    const int64_t avg = ceil_div(T, S);
+    const int trows = avg <= 2 ? 1 : avg <= 4 ? 2 : avg <= 8 ? 4 : 8;
+    const int64_t slots = tile_slots(T, S, seg_ptr_host, trows, 1, max_len);
+    if (slots <= 0) return false;
     const int nsm = num_sms();
     if (nsm <= 0) return false;
     int cl = 8;
@@ -175,17 +195,21 @@ bool stream_shape(int32_t T, int32_t H1, int32_t H2, int32_t r, int in_dtype, in
     p.G = (int32_t)std::min<int64_t>(slots, gmax);
     p.hc = round8(ceil_div(H1, cl));
     p.jc = round8(ceil_div(H2, cl));
-    p.hn = kStreamAElems / rk;
+    if (H2 % 256 == 0) {  // lets B chunks start on 256-column blocks (one copy each)
+        const int32_t jc256 = (int32_t)(ceil_div(H2, 256LL * cl) * 256);
+        if ((int64_t)(cl - 1) * jc256 < H2) p.jc = jc256;
+    }
+    p.hn = kStreamChunkElems / rk;
     const uint32_t es = (uint32_t)elem_size(in_dtype), ys = (uint32_t)elem_size(y_dtype);
-    const uint32_t w = align_up((uint32_t)std::max(p.hn * r, r * kStreamJn) * es, 128);
-    const uint32_t act = align_up(8u * std::max<uint32_t>((uint32_t)p.hn * es, kStreamJn * ys), 128);
+    const uint32_t w = align_up((uint32_t)(p.hn * r) * es, 128);
+    const uint32_t act = align_up((uint32_t)trows * (uint32_t)p.hn * std::max(es, ys), 128);
     p.stage_bytes = w + act;
     p.act_off = w;
     const uint32_t red = (uint32_t)(kStreamConsumers / 32) * 8u * (uint32_t)rk * 4u;
     const uint32_t recv = cl > 1 ? 2u * (uint32_t)cl * 8u * (uint32_t)rk * 4u : 0u;
     const uint32_t vbytes = 2u * 8u * (uint32_t)rk * 4u;
     const uint32_t tab = (uint32_t)kStreamMaxTiles * 12u * 4u;
-    const int64_t chunks = ceil_div(slots, p.G) * (ceil_div(p.hc, p.hn) + ceil_div(p.jc, kStreamJn));
+    const int64_t chunks = ceil_div(slots, p.G) * (ceil_div(p.hc, p.hn) + ceil_div(p.jc, p.hn));
     const uint32_t fixed = red + recv + vbytes + tab;
     // A CTA with few chunks to stream (small batches) keeps to half an SM, so
     // the next call's CTAs can start beside it and request their weights
@@ -196,6 +220,7 @@ bool stream_shape(int32_t T, int32_t H1, int32_t H2, int32_t r, int in_dtype, in
     nst = std::min<int64_t>(std::min<int64_t>(nst, kStreamMaxStages), chunks);
     if (nst < 1) return false;
     p.nst = (int32_t)nst;
+    p.trows = trows;
     p.red_off = (uint32_t)nst * p.stage_bytes;
     p.recv_off = p.red_off + red;
     p.v_off = p.recv_off + recv;
@@ -483,8 +508,7 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     p.err = err;
     StreamLaunch sl = {};
     if (slots > 0 &&
-        stream_shape(T, H1, H2, r, in_dtype, y_dtype,
-                     tile_slots(T, S, seg_ptr_host, kRowsMax, 1, cc_max_len), sl)) {
+        stream_shape(T, S, seg_ptr_host, cc_max_len, H1, H2, r, in_dtype, y_dtype, sl)) {
         StreamParams &q = sl.p;
         q.y = y;
         q.x = x;
@@ -582,8 +606,7 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
         int *err = error_word();
         if (!err) return SGMV_ERR_CUDA;
         StreamLaunch sl = {};
-        if (stream_shape(T, H1, H2, r, in_dtype, y_dtype,
-                         ((int64_t)T + (int64_t)smax * (kRowsMax - 1)) / kRowsMax, sl)) {
+        if (stream_shape(T, smax, nullptr, INT_MAX, H1, H2, r, in_dtype, y_dtype, sl)) {
             StreamParams &q = sl.p;
             q.y = y;
             q.x = x;

@@ -144,6 +144,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int c0, 
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *map, int c0, int c1, int c2,
+                                            int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+
 // ---- 1-D bulk copy shared -> global (bulk-group completion) ---------------
 __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
@@ -241,6 +251,32 @@ __device__ __forceinline__ uint2 lds64(const void *p) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_addr(p))
                  : "memory");
     return v;
+}
+
+// ---- fused multiply-adds --------------------------------------------------
+// c + a * b with 16-bit a, b and an fp32 accumulator, rounded once: the
+// product of two 16-bit floats is exact in fp32, so this equals
+// fmaf(float(a), float(b), c) bit for bit, without the two conversions.
+template <typename T> __device__ __forceinline__ float fma16(unsigned short a, unsigned short b, float c);
+template <> __device__ __forceinline__ float fma16<__half>(unsigned short a, unsigned short b, float c) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+template <> __device__ __forceinline__ float fma16<__nv_bfloat16>(unsigned short a, unsigned short b,
+                                                                 float c) {
+    float d;
+    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+// (c0, c1) += a * (b0, b1) as one packed fp32 instruction (each lane one fmaf).
+__device__ __forceinline__ void fma2(float a, float b0, float b1, float &c0, float &c1) {
+    uint64_t av, bv, cv;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(av) : "f"(a));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(bv) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(cv) : "f"(c0), "f"(c1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(cv) : "l"(av), "l"(bv));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(cv));
 }
 
 // ---- element conversions ---------------------------------------------------

@@ -142,15 +142,19 @@ constexpr int kStreamConsumers = 256;                   // 8 compute warps
 constexpr int kStreamThreads = kStreamConsumers + 32;   // + 1 copy-issuing warp
 constexpr int kStreamMaxStages = 8;
 constexpr int kStreamMaxTiles = 64;   // tiles one cluster walks in one launch
-constexpr int kStreamJn = 2 * kStreamConsumers;  // columns of one B chunk (two per compute thread)
-constexpr int kStreamAElems = 8192;   // elements of one A chunk at the rank bound
+// Columns of one A chunk and of one B chunk at rank bound RK (32 KB of
+// weights per chunk at r = RK): 1024 for RK = 16, 512 for RK = 32.
+constexpr int kStreamChunkElems = 16384;
 
 // One launch of the streaming kernel.  Grid: x = CTA rank in the cluster
 // (slices [rank*hc, ...) of H1 and [rank*jc, ...) of H2), y = cluster; cluster
 // c walks the tiles c, c + G, c + 2G, ... of the batch.  Every CTA streams its
 // slices of the tiles' A and B through a ring of `nst` shared-memory stages.
 struct StreamParams {
-    CUtensorMap tmap_b;  // B as [L][r][H2], box {256, r, 1}, no swizzle
+    // B, no swizzle: as [L][H2/256][r][256] with box {256, r, chunk/256, 1}
+    // (b4d, whole chunk in one copy), else as [L][r][H2] with box {256, r, 1}
+    CUtensorMap tmap_b;
+    int32_t b4d;
     void *y;
     const void *x;
     const void *A;
@@ -168,8 +172,9 @@ struct StreamParams {
     int32_t S, T, L, H1, H2, r;
     int32_t cl, G;               // CTAs per cluster, clusters
     int32_t hc, jc;              // columns of H1 / H2 per CTA (multiples of 8)
-    int32_t hn;                  // columns of one A chunk (kStreamAElems / rank bound)
+    int32_t hn;                  // columns of one A or B chunk (kStreamChunkElems / rank bound)
     int32_t nst;                 // ring stages
+    int32_t trows;               // rows per tile, 1..8 (the x / y part of a stage holds trows rows)
     uint32_t stage_bytes, act_off;  // bytes per stage; offset of the x / y rows in it
     uint32_t red_off, recv_off, v_off, tab_off, smem_bytes;
     int32_t min_len, max_len;

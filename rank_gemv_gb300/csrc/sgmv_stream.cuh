@@ -8,14 +8,15 @@
 // the kernel is built to keep HBM busy rather than the arithmetic units.
 //
 // Work decomposition:
-//   * a tile is up to 8 consecutive rows of one segment (one adapter);
+//   * a tile is up to `trows` (1..8) consecutive rows of one segment;
 //   * CL CTAs form a cluster (CL = 1, 2, 4 or 8, fewer for larger batches);
 //     CTA `rank` owns the slice [rank*hc, ...) of H1 and [rank*jc, ...) of H2;
 //   * cluster c walks the tiles c, c + G, c + 2G, ...: the kernel is
 //     persistent over tiles, and each CTA streams its slices of every tile's
-//     A and B through a ring of shared-memory stages: one 1-D bulk (TMA) copy
-//     per A chunk (contiguous in A[a]), tiled tensor (TMA) boxes of 256
-//     columns x r rows per B chunk, one bulk copy per x or y row.  One warp
+//     A and B through a ring of shared-memory stages, 32 KB of weights per
+//     chunk at the rank bound: one 1-D bulk (TMA) copy per A chunk
+//     (contiguous in A[a]), tiled tensor (TMA) boxes of 256 columns x r rows
+//     per B chunk, one bulk copy per x or y row.  One warp
 //     only issues copies; eight warps compute.  The ring order is A(0); A(1) B(0); A(2) B(1); ...: the shrink of tile m runs
 //     before the expand of tile m-1, so the cluster exchange of tile m-1's v
 //     is hidden behind it, and the copies never wait for an exchange;
@@ -118,15 +119,15 @@ __device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes,
 #pragma unroll 2
             for (int h = hoff; h < nh; h += HSTR) {
                 const uint2 av = lds64(As + h * rk + 4 * kq);
-                float a[4];
-                unpack2<Tin>(av.x, a[0], a[1]);
-                unpack2<Tin>(av.y, a[2], a[3]);
+                const unsigned short a[4] = {(unsigned short)(av.x & 0xffffu),
+                                             (unsigned short)(av.x >> 16),
+                                             (unsigned short)(av.y & 0xffffu),
+                                             (unsigned short)(av.y >> 16)};
 #pragma unroll
                 for (int t = 0; t < R; ++t) {
                     const unsigned short xb = lds16(Xs + t * hn + h);
-                    const float x = to_f<Tin>(*reinterpret_cast<const Tin *>(&xb));
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) acc[t][u] = fmaf(x, a[u], acc[t][u]);
+                    for (int u = 0; u < 4; ++u) acc[t][u] = fma16<Tin>(xb, a[u], acc[t][u]);
                 }
             }
         }
@@ -148,25 +149,30 @@ __device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes,
 }
 
 // Expand of one tile with R rows: y[row, j] += scale * v . B[a][:, j] for the
-// CTA's H2 slice, two adjacent columns per thread, r-sum in increasing k.
+// CTA's H2 slice; each thread owns JN / 512 pairs of adjacent columns of a
+// chunk and runs the r-sum in increasing k.
 template <typename Tin, typename Ty, int RK, int R>
 __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes, uint32_t act_off,
                                               int nst, int &q, int nB, int jlen, int j0, int rk,
                                               const float *sv, const int (&row)[kTileRows],
                                               Ty *gY, int H2, float scale, uint64_t *full,
                                               uint64_t *empty, bool &lost, int *err) {
+    constexpr int JN = kStreamChunkElems / RK;
+    constexpr int PP = JN / (2 * kStreamConsumers);
     const int tid = threadIdx.x;
-    const int c = 2 * tid;
-    // B chunk in shared memory: boxes of 256 columns, [box][k][256]
-    const int boff = (c >> 8) * rk * 256 + (c & 255);
     for (int i = 0; i < nB; ++i, ++q) {
         const int s = q % nst;
         stream_wait(&full[s], (uint32_t)((q / nst) & 1), lost, err);
-        const int nj = min(kStreamJn, jlen - i * kStreamJn);
+        const int nj = min(JN, jlen - i * JN);
         const uint8_t *base = sm + (size_t)s * stage_bytes;
         const Tin *Bs = reinterpret_cast<const Tin *>(base);
         const Ty *Ys = reinterpret_cast<const Ty *>(base + act_off);
-        if (c < nj) {
+#pragma unroll
+        for (int pp = 0; pp < PP; ++pp) {
+            const int c = 2 * (tid + pp * kStreamConsumers);
+            if (c >= nj) break;
+            // B chunk in shared memory: boxes of 256 columns, [box][k][256]
+            const Tin *bcol = Bs + (c >> 8) * rk * 256 + (c & 255);
             float acc[R][2];
 #pragma unroll
             for (int t = 0; t < R; ++t) acc[t][0] = acc[t][1] = 0.f;
@@ -185,22 +191,19 @@ __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes,
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float b0, b1;
-                        unpack2<Tin>(lds32(Bs + boff + (kk + e) * 256), b0, b1);
+                        unpack2<Tin>(lds32(bcol + (kk + e) * 256), b0, b1);
 #pragma unroll
-                        for (int t = 0; t < R; ++t) {
-                            acc[t][0] = fmaf(v[t][e], b0, acc[t][0]);
-                            acc[t][1] = fmaf(v[t][e], b1, acc[t][1]);
-                        }
+                        for (int t = 0; t < R; ++t) fma2(v[t][e], b0, b1, acc[t][0], acc[t][1]);
                     }
                 }
             }
             if (!lost) {
-                const int jg = j0 + i * kStreamJn + c;
+                const int jg = j0 + i * JN + c;
 #pragma unroll
                 for (int t = 0; t < R; ++t) {
                     if (row[t] < 0) continue;
                     float y0, y1;
-                    lds2<Ty>(Ys + t * kStreamJn + c, y0, y1);
+                    lds2<Ty>(Ys + t * JN + c, y0, y1);
                     st2<Ty>(gY + (size_t)row[t] * H2 + jg, fmaf(scale, acc[t][0], y0),
                             fmaf(scale, acc[t][1], y1));
                 }
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     const int T = P.T, L = P.L, H1 = P.H1, H2 = P.H2, rk = P.r;
     const int ncl = P.cl, G = P.G, hn = P.hn, nst = P.nst;
     const int min_len = P.min_len, max_len = P.max_len;
+    const int trows = P.trows;  // rows per tile, 1..8
     const uint32_t stage_bytes = P.stage_bytes, act_off = P.act_off;
     const float scale = P.scale;
     int *const err = P.err;
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 if (rep) set_error(err, kErrBadIndex);
                 return 0;
             }
-            return (len + kTileRows - 1) / kTileRows;
+            return (len + trows - 1) / trows;
         };
         const int per = (S + kStreamThreads - 1) / kStreamThreads;
         const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             for (int j = ((cid - gbase % G) % G + G) % G; j < n; j += G) {
                 const int m = (gbase + j) / G;
                 if (m < kStreamMaxTiles) {
-                    tab[4 * m] = b + kTileRows * j;
-                    tab[4 * m + 1] = min(kTileRows, len - kTileRows * j);
+                    tab[4 * m] = b + trows * j;
+                    tab[4 * m + 1] = min(trows, len - trows * j);
                     tab[4 * m + 2] = a;
                 }
             }
@@ -371,19 +375,19 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 for (int e = 0; e < 4; ++e) {
                     if (rr[e] == 0 && ku[e] < gkey) {
                         ++g_dless;
-                        if (ku[e] >= 0) tb += (cc[e] + kTileRows - 1) / kTileRows;
+                        if (ku[e] >= 0) tb += (cc[e] + trows - 1) / trows;
                     }
                 }
             }
-            if (gkey >= 0 && grank % kTileRows == 0) {
-                const int gt = tb + grank / kTileRows;
+            if (gkey >= 0 && grank % trows == 0) {
+                const int gt = tb + grank / trows;
                 if (gt % G == cid && gt / G < kStreamMaxTiles) {
                     const int m = gt / G;
                     tab[4 * m] = g_less + grank;
-                    tab[4 * m + 1] = min(kTileRows, cnt - grank);
+                    tab[4 * m + 1] = min(trows, cnt - grank);
                     tab[4 * m + 2] = gkey;
                 }
-                if (grank == 0) atomicAdd(&s_total, (cnt + kTileRows - 1) / kTileRows);
+                if (grank == 0) atomicAdd(&s_total, (cnt + trows - 1) / trows);
             }
         }
         g_nseg = __syncthreads_count(tid < T && grank == 0);
@@ -427,7 +431,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     const int h0 = min(H1, rank * P.hc), h1 = min(H1, h0 + P.hc);
     const int j0 = min(H2, rank * P.jc), j1 = min(H2, j0 + P.jc);
     const int nA = (h1 - h0 + hn - 1) / hn;
-    const int nB = (j1 - j0 + kStreamJn - 1) / kStreamJn;
+    constexpr int JN = kStreamChunkElems / RK;
+    const int nB = (j1 - j0 + JN - 1) / JN;
     const int total = nt * (nA + nB);
 
     if (warp == kStreamWarps) {
@@ -438,6 +443,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         const Tin *gX = static_cast<const Tin *>(P.x);
         const Ty *gY = static_cast<const Ty *>(P.y);
         const uint32_t bbox = (uint32_t)rk * 256u * (uint32_t)sizeof(Tin);
+        const bool b4d = P.b4d != 0;
         RingIter it;
         int cur_a = -1, cur_r = -1, a = 0, row = -1;
         uint32_t nvalid = 0;
@@ -454,12 +460,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                     mbar_arrive_expect_tx(&full[s], bytes);
                     bulk_g2s(dst, gA + ((size_t)a * H1 + hlo) * rk, bytes, &full[s]);
                 } else {
-                    const int jlo = j0 + it.i * kStreamJn, n = min(kStreamJn, j1 - jlo);
-                    const int nbox = (n + 255) >> 8;
-                    mbar_arrive_expect_tx(&full[s], bbox * (uint32_t)nbox);
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_3d(dst + bx * bbox, &P.tmap_b, jlo + 256 * bx, 0, a, &full[s]);
+                    const int jlo = j0 + it.i * JN;
+                    if (b4d && j1 - jlo >= JN) {  // a whole chunk in one copy
+                        mbar_arrive_expect_tx(&full[s], bbox * (uint32_t)(JN / 256));
+                        tma_load_4d(dst, &P.tmap_b, 0, 0, jlo >> 8, a, &full[s]);
+                    }
                 }
+            }
+            if (it.isB && !(b4d && j1 - (j0 + it.i * JN) >= JN)) {  // one box of 256 columns per lane
+                const int jlo = j0 + it.i * JN, n = min(JN, j1 - jlo);
+                const int nbox = (n + 255) >> 8;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], bbox * (uint32_t)nbox);
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_3d(dst + lane * bbox, &P.tmap_b, jlo + 256 * lane, 0, a, &full[s]);
             }
         };
         auto issue_act = [&](int s) {  // x or y rows of chunk `it` into stage s
@@ -478,12 +492,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                     bulk_g2s(dst + (size_t)lane * hn * sizeof(Tin), gX + (size_t)row * H1 + hlo,
                              rowb, &full[s]);
             } else {
-                const int jlo = j0 + it.i * kStreamJn, n = min(kStreamJn, j1 - jlo);
+                const int jlo = j0 + it.i * JN, n = min(JN, j1 - jlo);
                 const uint32_t rowb = (uint32_t)n * (uint32_t)sizeof(Ty);
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], rowb * nvalid);
                 __syncwarp();
                 if (row >= 0)
-                    bulk_g2s(dst + (size_t)lane * kStreamJn * sizeof(Ty),
+                    bulk_g2s(dst + (size_t)lane * JN * sizeof(Ty),
                              gY + (size_t)row * H2 + jlo, rowb, &full[s]);
             }
         };
