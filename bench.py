@@ -209,6 +209,17 @@ class Batch:
     def step(self, sgmv):
         self.apply(sgmv)
 
+    def update(self, sgmv):
+        """The update kernels alone (roofline): sgmv_apply on the grouping the
+        last step wrote, or the single grouped launch for batches of up to 64
+        rows (their grouping happens inside the kernel)."""
+        if self.w.T <= 64:
+            self.apply(sgmv)
+            return
+        perm, seg_ptr, idx, _ = self.meta
+        sgmv.sgmv_apply(self.Y, self.X, self.A, self.B, seg_ptr, idx, self.w.scale, perm=perm,
+                        S=self.smax, workspace=self.ws)
+
 
 class StackBatch:
     """All 224 projections of the llama7b-stack workload, resident on the device."""
@@ -251,6 +262,12 @@ class StackBatch:
 
     def step(self, sgmv):
         self.apply(sgmv)
+
+    def update(self, sgmv):
+        """All 224 update calls on the grouping of the last step (roofline)."""
+        perm, seg_ptr, idx, _ = self.meta
+        for X, A, B, Y in self.projs:
+            sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
 
     def bytes_moved(self):
         from rank_gemv_gb300 import workloads as wl
@@ -337,9 +354,11 @@ def run_ours(args, rank, world, local):
     n = len(batches)
     g_full = capture([(lambda b=b: b.step(sgmv)) for b in batches])
     g_rem = capture([(lambda b=b: b.step(sgmv)) for b in batches[: K % n]]) if K % n else None
-    # the update calls alone (here the same calls as a step)
-    k_full = capture([(lambda b=b: b.apply(sgmv)) for b in batches])
-    k_rem = capture([(lambda b=b: b.apply(sgmv)) for b in batches[: K % n]]) if K % n else None
+    # the update kernels alone, for the roofline
+    k_full = capture([(lambda b=b: b.update(sgmv)) for b in batches])
+    k_rem = capture([(lambda b=b: b.update(sgmv)) for b in batches[: K % n]]) if K % n else None
+    batches[0].update(sgmv)
+    per_call = sgmv.sgmv_last_launch_count()
 
     # soak under the clock sampler, then the timed steps
     sampler = ClockSampler(gpu_id_for(dev))
@@ -363,17 +382,18 @@ def run_ours(args, rank, world, local):
 
     value = world * K * T / elapsed
     peak, peak_kind = measured_peak()
-    # roofline of one sgmv_apply call (one fused kernel for decode batches;
-    # CUDA-core + tensor-core shrink + expand for prefill), timed alone in a
+    # roofline of one update call (the streaming kernel for decode batches;
+    # streaming + tensor-core shrink + expand for prefill), timed alone in a
     # graph of K steps' worth of calls
     apply_s = kernel_s / (K * n_apply)
     bytes_apply = bytes_step / n_apply
     achieved = bytes_apply / apply_s / 1e9
-    per_call = launches_apply // n_apply
-    kname = ("sgmv_cc_kernel (grouping + shrink + expand in one launch, CUDA cores)"
-             if per_call == 1 else
-             "sgmv_apply_rows: build_segments_kernel + sgmv_cc_kernel + sgmv_tc_shrink_kernel"
-             " + sgmv_tc_expand_kernel")
+    if args.workload == "prefill":
+        kname = "sgmv_tc_shrink_kernel + sgmv_tc_expand_kernel (tensor cores; the streaming kernel gets no short segment)"
+    elif w0 is not None and w0.T <= 64:
+        kname = "sgmv_stream_kernel (grouping + shrink + expand in one launch, CUDA cores)"
+    else:
+        kname = "sgmv_stream_kernel (shrink + expand, CUDA cores; grouping excluded)"
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak",

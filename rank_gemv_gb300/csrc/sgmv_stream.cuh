@@ -232,9 +232,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     __shared__ int s_total;
     constexpr int kG = GROUPED ? kGroupMaxT : 4;
     __shared__ __align__(16) int g_key[kG];
-    __shared__ __align__(16) int g_cnt[kG];
-    __shared__ __align__(16) int g_rank[kG];
-    __shared__ int g_sperm[kG];
+    __shared__ int g_pn[kG], g_pkey[kG], g_flag[kG], g_sperm[kG];
+    __shared__ int g_nseg_s;
 
     float *const red = reinterpret_cast<float *>(sm + P.red_off);    // [8 warps][8][RK]
     float *const recv = reinterpret_cast<float *>(sm + P.recv_off);  // [2][cl][8][RK]
@@ -262,7 +261,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
 
     // ---- this cluster's tiles: tab[m] = global tile cid + m*G ---------------
-    int g_less = 0, g_dless = 0, g_nseg = 0, gkey = -1, grank = 0;
+    int g_less = 0, g_nseg = 0, gkey = -1, grank = 0;
     if (!GROUPED) {
         // Tiles per segment, block-scanned over the segments in order.
         const int S = P.S;
@@ -328,11 +327,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             gbase += n;
         }
     } else {
-        // Every CTA groups the batch itself (T <= kGroupMaxT): sorted position
-        // of row t = (#rows with a smaller id) + (#earlier rows with its id);
-        // tiles are numbered over ids in ascending order, 8 rows at a time.
-        // Keys past T are INT_MAX and ranks past T are 1, so that padded
-        // entries count for nothing below.
+        // Every CTA groups the batch itself (T <= kGroupMaxT).  Row t's sorted
+        // position is p = (#rows with a smaller id) + (#earlier rows with its
+        // id).  Each row then marks, at its position, whether it starts a
+        // segment and whether it starts a tile (every trows-th row of an id,
+        // ids >= 0 only); one scan over the positions numbers both.
+        // Keys past T are INT_MAX, so that padded entries count for nothing.
         const int32_t *ra = P.row_adapter;
         const int T4 = (T + 3) & ~3;
         if (tid < T4) {
@@ -344,11 +344,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 }
             }
             g_key[tid] = tid < T ? gkey : INT_MAX;
-            if (tid >= T) g_rank[tid] = 1;
         }
         __syncthreads();
-        int cnt = 0;
         if (tid < T) {
+            int cnt = 0;
             for (int u = 0; u < T4; u += 4) {
                 const uint4 k4 = lds128(g_key + u);
                 const int ku[4] = {(int)k4.x, (int)k4.y, (int)k4.z, (int)k4.w};
@@ -359,38 +358,44 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                     grank += (ku[e] == gkey) & (u + e < tid);
                 }
             }
-            g_cnt[tid] = cnt;
-            g_rank[tid] = grank;
-            g_sperm[g_less + grank] = tid;
+            const int p = g_less + grank;
+            g_sperm[p] = tid;
+            g_pn[p] = min(trows, cnt - grank);  // rows of the tile starting here
+            g_pkey[p] = gkey;                   // id at sorted position p
+            // bit 0..15: starts a tile; bit 16..: starts a segment
+            g_flag[p] = ((gkey >= 0 && (grank & (trows - 1)) == 0) ? 1 : 0) | (grank == 0 ? 0x10000 : 0);
         }
         __syncthreads();
-        if (tid < T) {
-            int tb = 0;  // tiles of the adapters with a smaller id
-            for (int u = 0; u < T4; u += 4) {
-                const uint4 k4 = lds128(g_key + u), r4 = lds128(g_rank + u), c4 = lds128(g_cnt + u);
-                const int ku[4] = {(int)k4.x, (int)k4.y, (int)k4.z, (int)k4.w};
-                const int rr[4] = {(int)r4.x, (int)r4.y, (int)r4.z, (int)r4.w};
-                const int cc[4] = {(int)c4.x, (int)c4.y, (int)c4.z, (int)c4.w};
+        // Exclusive scan of the flags over positions 0 .. T-1 (two warps).
+        const int f = tid < T ? g_flag[tid] : 0;
+        int inc = f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (rr[e] == 0 && ku[e] < gkey) {
-                        ++g_dless;
-                        if (ku[e] >= 0) tb += (cc[e] + trows - 1) / trows;
-                    }
-                }
-            }
-            if (gkey >= 0 && grank % trows == 0) {
-                const int gt = tb + grank / trows;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += o;
+        }
+        if (lane == 31 && warp < 2) s_wsum[warp] = inc;
+        __syncthreads();
+        const int before = (warp == 1 ? s_wsum[0] : 0) + inc - f;  // warps 0, 1 hold positions
+        if (tid < T) {
+            if (f & 1) {
+                const int gt = before & 0xffff;
                 if (gt % G == cid && gt / G < kStreamMaxTiles) {
                     const int m = gt / G;
-                    tab[4 * m] = g_less + grank;
-                    tab[4 * m + 1] = min(trows, cnt - grank);
-                    tab[4 * m + 2] = gkey;
+                    tab[4 * m] = tid;
+                    tab[4 * m + 1] = g_pn[tid];
+                    tab[4 * m + 2] = g_pkey[tid];
                 }
-                if (grank == 0) atomicAdd(&s_total, (cnt + trows - 1) / trows);
             }
+            g_flag[tid] = before;  // segment number (high half) of position tid
         }
-        g_nseg = __syncthreads_count(tid < T && grank == 0);
+        if (tid == 0) {
+            const int tot = s_wsum[0] + (T > 32 ? s_wsum[1] : 0);
+            s_total = tot & 0xffff;
+            g_nseg_s = tot >> 16;
+        }
+        __syncthreads();
+        g_nseg = g_nseg_s;
     }
     __syncthreads();
     const int ntot = s_total;
@@ -401,12 +406,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
     // Grouped form, CTA (0,0): the grouping is written out for later calls,
     // after the previous kernel on the stream (which may still read it).
-    auto write_meta = [&]() {
+    auto write_meta = [&]() {  // thread p < T: sorted position p
         if (tid < T) {
-            P.perm_out[g_less + grank] = tid;
-            if (grank == 0) {
-                P.seg_out[g_dless] = g_less;
-                P.idx_out[g_dless] = gkey;
+            P.perm_out[tid] = g_sperm[tid];
+            const int sg = g_flag[tid] >> 16;  // segments before position p
+            if (tid == 0 || g_pkey[tid] != g_pkey[tid - 1]) {
+                P.seg_out[sg] = tid;
+                P.idx_out[sg] = g_pkey[tid];
             }
         }
         if (tid == 0) {
@@ -501,13 +507,72 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                              gY + (size_t)row * H2 + jlo, rowb, &full[s]);
             }
         };
+        // The first `pre` chunks fill stages 0 .. pre-1 with one chunk per lane:
+        // lane q requests chunk q's weights now and, after griddepcontrol.wait,
+        // its x / y rows, so each phase leaves in one instruction.
         const int pre = min(nst, total);
+        {
+            RingIter mine;
+            mine.start(nt, nA, nB);
+            for (int k = 0; k < lane && k < pre; ++k) mine.next();
+            const bool own = lane < pre;
+            const int tile = own ? mine.tile() : 0;
+            uint8_t *dst = sm + (size_t)lane * stage_bytes;
+            uint64_t *bar = &full[own ? lane : 0];
+            if (own) {
+                const int ma = (int)lds32(tab + 4 * tile + 2);
+                if (!mine.isB) {
+                    const int hlo = h0 + mine.i * hn, n = min(hn, h1 - hlo);
+                    const uint32_t bytes = (uint32_t)(n * rk) * (uint32_t)sizeof(Tin);
+                    mbar_arrive_expect_tx(bar, bytes);
+                    bulk_g2s(dst, gA + ((size_t)ma * H1 + hlo) * rk, bytes, bar);
+                } else {
+                    const int jlo = j0 + mine.i * JN, n = min(JN, j1 - jlo);
+                    if (b4d && n >= JN) {
+                        mbar_arrive_expect_tx(bar, bbox * (uint32_t)(JN / 256));
+                        tma_load_4d(dst, &P.tmap_b, 0, 0, jlo >> 8, ma, bar);
+                    } else {
+                        const int nbox = (n + 255) >> 8;
+                        mbar_arrive_expect_tx(bar, bbox * (uint32_t)nbox);
+                        for (int bx = 0; bx < nbox; ++bx)
+                            tma_load_3d(dst + bx * bbox, &P.tmap_b, jlo + 256 * bx, 0, ma, bar);
+                    }
+                }
+            }
+            named_sync<2, kStreamThreads>();  // the rows table is complete
+            pdl_wait();
+            if (own) {
+                int rows_[kTileRows];
+                uint32_t nv = 0;
+#pragma unroll
+                for (int t = 0; t < kTileRows; ++t) {
+                    rows_[t] = t < trows ? (int)lds32(trow + kTileRows * tile + t) : -1;
+                    nv += rows_[t] >= 0;
+                }
+                uint8_t *adst = dst + act_off;
+                if (!mine.isB) {
+                    const int hlo = h0 + mine.i * hn, n = min(hn, h1 - hlo);
+                    const uint32_t rowb = (uint32_t)n * (uint32_t)sizeof(Tin);
+                    mbar_arrive_expect_tx(bar, rowb * nv);
+#pragma unroll
+                    for (int t = 0; t < kTileRows; ++t)
+                        if (rows_[t] >= 0)
+                            bulk_g2s(adst + (size_t)t * hn * sizeof(Tin),
+                                     gX + (size_t)rows_[t] * H1 + hlo, rowb, bar);
+                } else {
+                    const int jlo = j0 + mine.i * JN, n = min(JN, j1 - jlo);
+                    const uint32_t rowb = (uint32_t)n * (uint32_t)sizeof(Ty);
+                    mbar_arrive_expect_tx(bar, rowb * nv);
+#pragma unroll
+                    for (int t = 0; t < kTileRows; ++t)
+                        if (rows_[t] >= 0)
+                            bulk_g2s(adst + (size_t)t * JN * sizeof(Ty),
+                                     gY + (size_t)rows_[t] * H2 + jlo, rowb, bar);
+                }
+            }
+        }
         it.start(nt, nA, nB);
-        for (int q = 0; q < pre; ++q, it.next()) issue_w(q);  // before the previous kernel ends
-        named_sync<2, kStreamThreads>();  // the rows table is complete
-        pdl_wait();
-        it.start(nt, nA, nB);
-        for (int q = 0; q < pre; ++q, it.next()) issue_act(q);
+        for (int q = 0; q < pre; ++q) it.next();
         for (int q = pre, s = pre % nst; q < total; ++q, it.next()) {
             if (!mbar_wait(&empty[s], (uint32_t)((q / nst - 1) & 1))) set_error(err, kErrTimeout);
             __syncwarp();
