@@ -467,16 +467,23 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
 
     int *err = error_word();
     if (!err) return SGMV_ERR_CUDA;
-    // Dispatch: segments of at least kTcMinLen rows to the tensor cores when a
-    // workspace holds their v and r suits the tensor-core tiles.
+    // Dispatch, when a workspace holds v and r suits the tensor-core tiles:
+    // in prefill-like batches (segments average 8 rows or more) every segment
+    // goes to the tensor cores, which read each segment's weights once as the
+    // CUDA-core kernel would, and no CUDA-core launch is made; otherwise
+    // segments of at least kTcMinLen rows go to the tensor cores and the rest
+    // to the CUDA-core kernel.  The choice depends on T and S only, so host
+    // and device metadata give the same bits.
     bool use_tc = workspace != nullptr && (r == 64 || r == 128) && T >= kTcMinLen;
     int64_t tc_slots = 0;
+    int32_t tc_min = kTcMinLen;
     if (use_tc) {
-        tc_slots = tile_slots(T, S, seg_ptr_host, 128, kTcMinLen, INT_MAX);
+        if ((int64_t)T >= 8LL * S) tc_min = 1;
+        tc_slots = tile_slots(T, S, seg_ptr_host, 128, tc_min, INT_MAX);
         if (tc_slots > 65535) return SGMV_ERR_UNSUPPORTED;
         use_tc = tc_slots > 0;
     }
-    const int32_t cc_max_len = use_tc ? kTcMinLen - 1 : INT_MAX;
+    const int32_t cc_max_len = use_tc ? tc_min - 1 : INT_MAX;
 
     CCLaunch l = {};
     CCParams &p = l.p;
@@ -564,7 +571,7 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     g.H1 = H1;
     g.H2 = H2;
     g.r = r;
-    g.min_len = kTcMinLen;
+    g.min_len = tc_min;
     g.max_len = INT_MAX;
     g.scale = scale;
     g.in_dtype = in_dtype;

@@ -1,8 +1,9 @@
 """Tensor-core (tcgen05) path for long segments against the fp64 oracle.
 
-sgmv_apply sends segments of at least 64 rows to the tensor cores when it is
-given a workspace and r is 64 or 128; shorter segments stay on the CUDA-core
-kernel in the same call.
+sgmv_apply sends segments to the tensor cores when it is given a workspace and
+r is 64 or 128: all of them when segments average 8 rows or more, else those
+of at least 64 rows, the shorter ones going to the CUDA-core kernel in the
+same call.
 """
 import numpy as np
 import pytest
@@ -93,6 +94,26 @@ def test_short_and_long_segments_in_one_call():
     assert torch.equal(y_dev, y_host)
     untouched = (ra == -1).nonzero().flatten()
     assert torch.equal(y_dev[untouched].cpu(), w.Y0[untouched])
+
+
+def test_split_between_cuda_and_tensor_cores():
+    # decode rows (40 one-row segments) next to two long segments: segments
+    # average under 8 rows, so the long ones go to the tensor cores and the
+    # short ones to the CUDA-core kernel in the same call
+    lens = [1] * 40 + [100, 80]
+    ids = list(range(40)) + [40, 41]
+    ra = torch.tensor(ids, dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    g = torch.Generator().manual_seed(11)
+    ra = ra[torch.randperm(ra.numel(), generator=g)]
+    w = wl.draw(ra.numel(), 42, 1024, 776, 64, ra, dtype=torch.bfloat16, y_dtype=torch.float32,
+                y0="randn", seed=12, scale=0.75)
+    y_dev = run(w)
+    y_host = run(w, host_meta=True)
+    assert sg().sgmv_last_launch_count() == 3  # CUDA-core + tensor-core shrink + expand
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y_dev, ref, "split batch")
+    assert torch.equal(y_dev, y_host)
 
 
 @pytest.mark.parametrize("H1,H2", [(4104, 11016), (64, 136), (11008, 4096), (192, 8)])
