@@ -577,6 +577,7 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     g.in_dtype = in_dtype;
     g.y_dtype = y_dtype;
     g.slots = tc_slots;
+    g.nsm = num_sms();
     g.stream = static_cast<cudaStream_t>(stream);
     st = cuda_status("tensor-core kernels", tc_launch(g));
     if (st == SGMV_OK) g_launches += 2;

@@ -114,6 +114,7 @@ struct TCArgs {
     float scale;
     int in_dtype, y_dtype;
     int64_t slots;   // 128-row tile slots
+    int32_t nsm;     // streaming multiprocessors of the device
     cudaStream_t stream;
 };
 

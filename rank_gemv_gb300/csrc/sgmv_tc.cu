@@ -17,16 +17,22 @@
 //   written as two 16-bit halves, hi = round(v) and lo = round(v - hi), so
 //   the expand can run on 16-bit tensor cores and still see v to about
 //   16 significant bits.
-// Expand (sgmv_tc_expand_kernel): one CTA per (128-row tile, 128 columns of
-//   H2).  TMA brings B[a][:, j0:j0+128] (N-major) and the tile's v hi/lo
-//   (K-major); 2 x r/16 MMAs accumulate v_hi.B + v_lo.B in TMEM; each thread
-//   then owns one row: tcgen05.ld 32 columns at a time, y += scale * acc in
-//   fp32, rounded once to y's type.
+// Expand (sgmv_tc_expand_kernel): one CTA per (128-row tile, run of column
+//   blocks of N = 64 (fp32 y) or 128 columns), about one wave in all.  The
+//   tile's v hi/lo is loaded once (TMA, K-major); per block, TMA brings
+//   B[a][:, j:j+N] (N-major) and 2 x r/16 MMAs accumulate v_hi.B + v_lo.B into
+//   one of two TMEM buffers, so block k+1's products are made while block k's
+//   epilogue runs.  y comes in by 16-byte cp.async copies (coalesced: a warp
+//   reads two 256-byte row pieces per instruction) through a 2-3 stage ring
+//   filled ahead; each thread owns one row: tcgen05.ld 32 columns at a time,
+//   y += scale * acc in fp32, rounded once; coalesced 16-byte stores write
+//   the block back.
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <mutex>
 
 #include <cuda.h>  // CUtensorMap and the encoder's signature (no libcuda link)
 
+#include <algorithm>
 #include <cstring>
 #include <type_traits>
 
@@ -40,6 +46,10 @@ constexpr int kTcThreads = 128;  // 4 warps: one TMEM lane (tile row) per thread
 constexpr int kTcRows = 128;     // M of one tile
 constexpr int kKB = 64;          // k-block: 64 16-bit elements = one 128-byte swizzle row
 constexpr int kStages = 3;       // shrink ring depth
+constexpr int kExpandThreads = 2 * kTcRows + 32;  // two epilogue groups + a copy / MMA warp
+constexpr int kExpandYStages = 2;  // most y stages per epilogue group
+constexpr int kExpandBStages = 3;  // most B stages
+constexpr size_t kExpandSmemMax = 220u * 1024u;
 
 struct TCShrinkParams {
     CUtensorMap tmap_a;  // A as [L][H1][r], box {64, 64, 1}
@@ -58,6 +68,9 @@ struct TCExpandParams {
     const int32_t *perm, *seg_ptr, *idx;
     int *err;
     int32_t S, T, L, H2, r, min_len, max_len;
+    int32_t nb;   // column blocks per CTA
+    int32_t ny;   // y stages per epilogue group (1 or 2)
+    int32_t nbs;  // B stages (2 or 3)
     float scale;
 };
 
@@ -356,22 +369,29 @@ __global__ void __launch_bounds__(kTcThreads)
 // ---------------------------------------------------------------- expand
 // Columns of H2 per expand CTA: 128 for 16-bit y, 64 for fp32 y (the y tile
 // staged in shared memory then stays at 32 KB and two or more CTAs fit per SM).
+// Barrier of one 128-thread epilogue group (named barriers 1 and 2).
+__device__ __forceinline__ void group_sync(int g) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kTcRows) : "memory");
+}
 template <typename Ty> constexpr int tc_cols() { return sizeof(Ty) == 4 ? 64 : 128; }
 // Bytes of one staged y row: the tile's columns plus 16 bytes, so that the
 // 16-byte accesses of 8 consecutive rows fall in different banks.
 template <typename Ty> constexpr int tc_ypitch() { return tc_cols<Ty>() * (int)sizeof(Ty) + 16; }
 
 template <typename Tin, typename Ty>
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(kExpandThreads, 1)
     sgmv_tc_expand_kernel(const __grid_constant__ TCExpandParams P) {
-    constexpr int N = tc_cols<Ty>();
+    constexpr int N = tc_cols<Ty>();   // columns of one block
     constexpr int YP = tc_ypitch<Ty>();
+    constexpr int CH = N * (int)sizeof(Ty) / 16;  // 16-byte chunks of a row's block (16)
+    constexpr int RPI = kTcRows / CH;              // rows covered by one pass of a group (8)
+    constexpr int E16 = 16 / (int)sizeof(Ty);      // elements per chunk
     const int32_t *const seg_ptr = P.seg_ptr;
     const int32_t *const idx = P.idx;
     const int32_t *const perm = P.perm;
     int *const err = P.err;
     const int nseg = P.S, nrows_all = P.T, nadapters = P.L, min_len = P.min_len,
-              max_len = P.max_len, rk = P.r, H2 = P.H2;
+              max_len = P.max_len, rk = P.r, H2 = P.H2, ny = P.ny, nbs = P.nbs;
     const float scale = P.scale;
     Ty *const gY = static_cast<Ty *>(P.y);
     const CUtensorMap *const tmap_b = &P.tmap_b;
@@ -379,129 +399,204 @@ __global__ void __launch_bounds__(kTcThreads)
     const CUtensorMap *const tmap_vlo = &P.tmap_vlo;
 
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t bar_b, bar_v, bar_y, bar_mma;
+    __shared__ __align__(8) uint64_t bar_v, b_full[kExpandBStages], b_empty[kExpandBStages];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], y_full[2][kExpandYStages];
     __shared__ int s_info[4];
+    __shared__ int s_row[kTcRows];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
+
+    const int nblk = (H2 + N - 1) / N;
+    const int b0 = (int)blockIdx.x * P.nb;
+    const int nb = min(nblk, b0 + P.nb) - b0;  // column blocks of this CTA (>= 1)
 
     if (warp == 0) {
         find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, min_len, max_len, err,
                   blockIdx.y, false, report, s_info);
         if (lane == 0) {
-            mbar_init(&bar_b, 1);
             mbar_init(&bar_v, 1);
-            mbar_init(&bar_y, 1);
-            mbar_init(&bar_mma, 1);
+            for (int i = 0; i < nbs; ++i) {
+                mbar_init(&b_full[i], 1);
+                mbar_init(&b_empty[i], 1);
+            }
+            for (int g = 0; g < 2; ++g) {
+                mbar_init(&acc_full[g], 1);
+                mbar_init(&acc_empty[g], kTcRows / 32);  // one arrival per warp of the group
+                for (int i = 0; i < ny; ++i) mbar_init(&y_full[g][i], kTcRows);  // cp.async, per thread
+            }
             mbar_init_fence();
         }
     }
     __syncthreads();
-    if (s_info[0] < 0) return;
+    if (s_info[0] < 0 || nb <= 0) return;
     const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
-    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)N);
+    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)(2 * N));
 
     uint8_t *base = align1024(dsm);
-    const uint32_t v_bytes = (uint32_t)rk * 256u;  // [128 rows][r] 16-bit, as r/64 K-blocks
-    const uint32_t b_bytes = (uint32_t)rk * N * 2u; // N/64 N-atoms of [r rows][64 columns]
-    uint8_t *b_tile = base;
-    uint8_t *vhi_tile = base + b_bytes;
-    uint8_t *vlo_tile = vhi_tile + v_bytes;
-    uint8_t *y_tile = vlo_tile + v_bytes;  // [128 rows][YP bytes]
-    const int j0 = (int)blockIdx.x * N;
-    const int ncols = min(N, H2 - j0);
-    const uint32_t yrow_bytes = (uint32_t)ncols * sizeof(Ty);
+    const uint32_t v_bytes = (uint32_t)rk * 256u;   // [128 rows][r] 16-bit, as r/64 K-blocks
+    const uint32_t b_bytes = (uint32_t)rk * N * 2u;  // N/64 N-atoms of [r rows][64 columns]
+    uint8_t *vhi_tile = base;
+    uint8_t *vlo_tile = base + v_bytes;
+    uint8_t *b_stage0 = base + 2 * v_bytes;
+    uint8_t *y_stage0 = b_stage0 + (size_t)nbs * b_bytes;  // [2 groups][ny][128 rows][YP]
+    const uint32_t ystage_bytes = (uint32_t)kTcRows * YP;
 
-    if (tid == 0) {  // weights: independent of the previous kernel
-        mbar_arrive_expect_tx(&bar_b, b_bytes);
-        for (int c = 0; c < N; c += 64)
-            tma_load_3d(b_tile + c * rk * 2, tmap_b, j0 + c, 0, a, &bar_b);
-    }
-    int row = -1;
-    if (tid < nrows) {
-        row = perm ? perm[p0 + tid] : p0 + tid;
-        if (row < 0 || row >= nrows_all) {
-            set_error(err, kErrBadIndex);
-            row = -1;
+    if (tid < kTcRows) {
+        int row = -1;
+        if (tid < nrows) {
+            row = perm ? perm[p0 + tid] : p0 + tid;
+            if (row < 0 || row >= nrows_all) {
+                set_error(err, kErrBadIndex);
+                row = -1;
+            }
         }
+        s_row[tid] = row;
     }
-    const int nvalid = __syncthreads_count(row >= 0);
-    pdl_wait();
-    if (tid == 0) {  // v of the tile, written by the shrink kernel
-        mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);
-        for (int kb = 0; kb < rk / kKB; ++kb) {
-            tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, p0, &bar_v);
-            tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, p0, &bar_v);
-        }
-        mbar_arrive_expect_tx(&bar_y, yrow_bytes * (uint32_t)nvalid);
-    }
-    // this thread's y row, one bulk copy, while the MMAs run
-    if (row >= 0)
-        bulk_g2s(y_tile + tid * YP, gY + (size_t)row * H2 + j0, yrow_bytes, &bar_y);
-    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    if (tid == 0) {
-        const bool ok = mbar_wait(&bar_b, 0) && mbar_wait(&bar_v, 0);
-        if (!ok) {
-            set_error(err, kErrTimeout);
-            mbar_wait(&bar_b, 0);
-            mbar_wait(&bar_v, 0);
-        }
-        tc_fence_after();
-        const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, N);
-        const uint32_t ba = smem_addr(b_tile);
-        uint32_t acc = 0;
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t va = smem_addr(h ? vlo_tile : vhi_tile);
-            for (int kb = 0; kb < rk / kKB; ++kb)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_f16(tmem, sw128_desc(va + kb * 16384 + kk * 32, 16, 1024),
-                            sw128_desc(ba + (kb * 4 + kk) * 2048, (uint32_t)rk * 128, 1024),
-                            idesc, acc);
-                    acc = 1;
-                }
-        }
-        mma_commit(&bar_mma);
-    }
-    bool lost = false;
-    if (!mbar_wait(&bar_mma, 0) || !mbar_wait(&bar_y, 0)) {
-        set_error(err, kErrTimeout);
-        mbar_wait(&bar_mma, 0);
-        mbar_wait(&bar_y, 0);
-        lost = true;
-    }
-    tc_fence_after();
+    pdl_trigger();
 
-    // y row in shared memory += scale * accumulator row, 32 columns at a time
-    uint8_t *yr = y_tile + tid * YP;
-    for (int c0 = 0; c0 < N; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-        if (row >= 0) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                Ty *p = reinterpret_cast<Ty *>(yr) + c0 + q * 8;
-                float y[8];
-                lds8<Ty>(p, y);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = fmaf(scale, v[q * 8 + i], y[i]);
-                sts8<Ty>(p, y);
+    if (warp == kExpandThreads / 32 - 1) {
+        // ---- copy / MMA warp: B through a ring, the tile's v once, products
+        // of block k into accumulator buffer k & 1 (the buffer of group k & 1)
+        if (lane == 0) {
+            auto load_b = [&](int k) {
+                const int st = k % nbs;
+                mbar_arrive_expect_tx(&b_full[st], b_bytes);
+                for (int c = 0; c < N; c += 64)
+                    tma_load_3d(b_stage0 + (size_t)st * b_bytes + c * rk * 2, tmap_b,
+                                (b0 + k) * N + c, 0, a, &b_full[st]);
+            };
+            for (int k = 0; k < min(nbs, nb); ++k) load_b(k);  // weights: before the wait
+            pdl_wait();
+            mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);  // v: written by the shrink kernel
+            for (int kb = 0; kb < rk / kKB; ++kb) {
+                tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, p0, &bar_v);
+                tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, p0, &bar_v);
             }
+            bool ok = mbar_wait(&bar_v, 0);
+            // after a wait runs out, later ones are skipped: the error is set
+            // and every wait of the compute warps is bounded as well
+            auto pwait = [&](uint64_t *bar, uint32_t par) {
+                if (ok) ok = mbar_wait(bar, par);
+            };
+            const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, N);
+            for (int k = 0; k < nb; ++k) {
+                const int st = k % nbs, g = k & 1;
+                pwait(&b_full[st], (uint32_t)((k / nbs) & 1));
+                if (k >= 2) pwait(&acc_empty[g], (uint32_t)(((k >> 1) - 1) & 1));
+                tc_fence_after();
+                const uint32_t ba = smem_addr(b_stage0 + (size_t)st * b_bytes);
+                const uint32_t d = tmem + (uint32_t)(g * N);
+                uint32_t acc = 0;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t va = smem_addr(h ? vlo_tile : vhi_tile);
+                    for (int kb = 0; kb < rk / kKB; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            mma_f16(d, sw128_desc(va + kb * 16384 + kk * 32, 16, 1024),
+                                    sw128_desc(ba + (kb * 4 + kk) * 2048, (uint32_t)rk * 128, 1024),
+                                    idesc, acc);
+                            acc = 1;
+                        }
+                }
+                mma_commit(&acc_full[g]);
+                mma_commit(&b_empty[st]);
+                if (k + nbs < nb) {  // refill the stage once block k's products are made
+                    pwait(&b_empty[st], (uint32_t)((k / nbs) & 1));
+                    load_b(k + nbs);
+                }
+            }
+            if (!ok) set_error(err, kErrTimeout);
+        }
+    } else {
+        // ---- epilogue groups: group g (warps 4g .. 4g+3, one tile row per
+        // thread, TMEM lanes of warp % 4) takes blocks g, g + 2, ...
+        const int g = warp >> 2, lt = tid & (kTcRows - 1);
+        const int nmine = (nb - g + 1) >> 1;  // blocks of this group
+        uint8_t *my_y = y_stage0 + (size_t)g * ny * ystage_bytes;
+        // y of the group's i-th block into stage i % ny: thread lt copies chunk
+        // lt % CH of rows lt / CH + RPI * j (two 256-byte row pieces per warp
+        // instruction)
+        auto load_y = [&](int i) {
+            uint8_t *st = my_y + (size_t)(i % ny) * ystage_bytes;
+            const int j = (b0 + g + 2 * i) * N;
+            const int c = lt % CH;
+            const bool col_ok = j + c * E16 < H2;
+#pragma unroll 4
+            for (int r = lt / CH; r < kTcRows; r += RPI) {
+                const int row = s_row[r];
+                if (row >= 0 && col_ok)
+                    cp_async16(st + r * YP + c * 16, gY + (size_t)row * H2 + j + c * E16, 16);
+            }
+            cp_async_arrive(&y_full[g][i % ny]);
+        };
+        pdl_wait();  // y may be written by the previous kernel
+        for (int i = 0; i < min(ny, nmine); ++i) load_y(i);
+        bool lost = false;
+        auto wait = [&](uint64_t *bar, uint32_t par) {
+            if (!mbar_wait(bar, par)) {
+                set_error(err, kErrTimeout);
+                mbar_wait(bar, par);
+                lost = true;
+            }
+        };
+        const int my_row = s_row[lt];
+        for (int i = 0; i < nmine; ++i) {
+            const int k = g + 2 * i;
+            wait(&acc_full[g], (uint32_t)(i & 1));
+            tc_fence_after();
+            wait(&y_full[g][i % ny], (uint32_t)((i / ny) & 1));
+            // y row in shared memory += scale * accumulator row, 32 columns at a time
+            uint8_t *st = my_y + (size_t)(i % ny) * ystage_bytes;
+            uint8_t *yr = st + (size_t)lt * YP;
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(g * N + c0), v);
+                if (my_row >= 0) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        Ty *p = reinterpret_cast<Ty *>(yr) + c0 + q * 8;
+                        float y[8];
+                        lds8<Ty>(p, y);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[e] = fmaf(scale, v[q * 8 + e], y[e]);
+                        sts8<Ty>(p, y);
+                    }
+                }
+            }
+            // the accumulator buffer is free for block k + 2
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[g]);
+            group_sync(g);
+            // write the block back: 16-byte stores, two row pieces per warp instruction
+            {
+                const int j = k * N + b0 * N;
+                const int c = lt % CH;
+                if (!lost && j + c * E16 < H2) {
+#pragma unroll 4
+                    for (int r = lt / CH; r < kTcRows; r += RPI) {
+                        const int row = s_row[r];
+                        if (row >= 0)
+                            *reinterpret_cast<uint4 *>(gY + (size_t)row * H2 + j + c * E16) =
+                                lds128(st + r * YP + c * 16);
+                    }
+                }
+            }
+            group_sync(g);  // stage i % ny has been read: refill it
+            if (i + ny < nmine) load_y(i + ny);
         }
     }
-    fence_proxy_async();  // generic shared-memory writes -> bulk-copy (async proxy) reads
     tc_fence_before();
     __syncthreads();
-    if (row >= 0 && !lost) {
-        bulk_s2g(gY + (size_t)row * H2 + j0, yr, yrow_bytes);
-        bulk_commit();
-        bulk_wait_read();  // the copy has read shared memory: safe to exit
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)(2 * N));
     }
-    if (warp == 0) tmem_dealloc(tmem, (uint32_t)N);
 }
 
 // ---------------------------------------------------------------- host side
@@ -550,13 +645,14 @@ bool encode(CUtensorMap *m, bool bf16, int rank, const void *ptr, const cuuint64
 }
 
 template <typename K, typename P>
-int launch(K kernel, const P &params, dim3 grid, int cluster, size_t smem, cudaStream_t stream) {
+int launch(K kernel, const P &params, dim3 grid, int cluster, size_t smem, cudaStream_t stream,
+           int threads = kTcThreads) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -646,11 +742,22 @@ int tc_launch_t(const TCArgs &g) {
     ep.max_len = g.max_len;
     ep.scale = g.scale;
     constexpr int N = tc_cols<Ty>();
-    const size_t expand_smem = 1024 + (size_t)g.r * N * 2 + (size_t)2 * g.r * 256 +
-                               (size_t)kTcRows * tc_ypitch<Ty>();
+    const int nblk = (g.H2 + N - 1) / N;
+    // about one CTA per SM over all tiles: each CTA a run of column blocks
+    const int64_t want = std::max<int64_t>(1, g.nsm);
+    ep.nb = (int32_t)std::max<int64_t>(1, ((int64_t)nblk * g.slots + want - 1) / want);
+    // v once, B ring, two y stages per epilogue group: as deep as fits
+    const size_t vb = (size_t)2 * g.r * 256, bstage = (size_t)g.r * N * 2;
+    const size_t ystage = (size_t)kTcRows * tc_ypitch<Ty>();
+    ep.nbs = kExpandBStages;
+    ep.ny = kExpandYStages;
+    auto total = [&]() { return 1024 + vb + ep.nbs * bstage + (size_t)2 * ep.ny * ystage; };
+    if (total() > kExpandSmemMax) ep.nbs = 2;
+    if (total() > kExpandSmemMax) ep.ny = 1;
+    const size_t expand_smem = total();
     return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep,
-                  dim3((unsigned)((g.H2 + N - 1) / N), (unsigned)g.slots, 1), 1, expand_smem,
-                  g.stream);
+                  dim3((unsigned)((nblk + ep.nb - 1) / ep.nb), (unsigned)g.slots, 1), 1,
+                  expand_smem, g.stream, kExpandThreads);
 }
 
 template <typename Tin>
