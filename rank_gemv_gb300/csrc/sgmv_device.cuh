@@ -209,6 +209,17 @@ __device__ __forceinline__ void st_peer(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Store 16 bytes into another CTA's shared memory (addresses from peer_addr)
+// and count them on that CTA's mbarrier `remote_bar` as transaction bytes.
+__device__ __forceinline__ void st_async4(uint32_t remote, float a, float b, float c, float d,
+                                          uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            remote),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+        : "memory");
+}
+
 // ---- explicit shared-memory access ----------------------------------------
 // Pointers into dynamic shared memory that pass through lambdas or offset
 // arithmetic can lose their address space, and the generic loads the compiler

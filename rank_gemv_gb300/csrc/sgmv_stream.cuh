@@ -254,8 +254,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             mbar_init(&full[s], 2);  // weights, then the x / y rows
             mbar_init(&empty[s], kStreamWarps);
         }
-        mbar_init(&vfull[0], (uint32_t)ncl);
-        mbar_init(&vfull[1], (uint32_t)ncl);
+        mbar_init(&vfull[0], 1);  // armed once per tile with the bytes the peers push
+        mbar_init(&vfull[1], 1);
         mbar_init_fence();
         s_total = 0;
     }
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         Ty *gY = static_cast<Ty *>(P.y);
         bool lost = false;
         int q = 0;
-        float part = 0.f;  // element (t, k) = (tid / rk, tid % rk) of this CTA's partial v
+        float4 part;  // elements (t, 4q .. 4q+3) of this CTA's partial v, tid = t * (rk/4) + q
         for (int m = 0; m <= nt; ++m) {
             if (m < nt) {
                 const int n = (int)lds32(tab + 4 * m + 1);
@@ -621,13 +621,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                     stream_shrink<Tin, RK, 8>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
                                               full, empty, red, lost, err);
                 consumers_sync();
-                part = 0.f;
-                if (tid < n * rk) {
-                    const int t = tid / rk, k = tid - (tid / rk) * rk;
+                // this CTA's partial of v, four consecutive k per thread
+                part = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tid < n * (rk / 4)) {
+                    const int t = tid / (rk / 4), k = 4 * (tid - t * (rk / 4));
 #pragma unroll
-                    for (int w = 0; w < kStreamWarps; ++w)
-                        part += ldsf(red + (w * kTileRows + t) * RK + k);
-                    if (ncl == 1) stsf(s_v + ((m & 1) * kTileRows + t) * RK + k, part);
+                    for (int w = 0; w < kStreamWarps; ++w) {
+                        const uint4 u = lds128(red + (w * kTileRows + t) * RK + k);
+                        part.x += __uint_as_float(u.x);
+                        part.y += __uint_as_float(u.y);
+                        part.z += __uint_as_float(u.z);
+                        part.w += __uint_as_float(u.w);
+                    }
+                    if (ncl == 1)
+                        sts128(s_v + ((m & 1) * kTileRows + t) * RK + k,
+                               make_uint4(__float_as_uint(part.x), __float_as_uint(part.y),
+                                          __float_as_uint(part.z), __float_as_uint(part.w)));
                 }
             }
             if (ncl > 1) {
@@ -650,19 +659,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 }
                 if (m < nt) {
                     // Push this CTA's partial of tile m into slot (m & 1, rank)
-                    // of every CTA.  The slot was last read for tile m-2, before
-                    // its owner arrived for tile m-1, which the wait above saw.
+                    // of every CTA with st.async, which counts the bytes on
+                    // the owner's vfull[m & 1]; each CTA expects ncl partials.
+                    // The slot was last read for tile m-2: its owner had read
+                    // it (and passed the barrier below) before pushing tile
+                    // m-1, which the wait above saw.
                     const int b = m & 1;
                     const int n = (int)lds32(tab + 4 * m + 1);
-                    if (tid < n * rk) {
-                        const int t = tid / rk, k = tid - (tid / rk) * rk;
+                    consumers_sync();  // this CTA's reads of its own slots are done
+                    if (tid == 0)
+                        mbar_arrive_expect_tx(&vfull[b], (uint32_t)(ncl * n * rk) * 4u);
+                    if (tid < n * (rk / 4)) {
+                        const int t = tid / (rk / 4), k = 4 * (tid - t * (rk / 4));
                         float *slot = recv + ((b * ncl + rank) * kTileRows + t) * RK + k;
-                        for (int c = 0; c < ncl; ++c) st_peer(peer_addr(slot, (uint32_t)c), part);
-                    }
-                    consumers_sync();
-                    if (tid < ncl) {
-                        fence_acq_rel_cluster();
-                        mbar_arrive_remote(peer_addr(&vfull[b], (uint32_t)tid));
+                        for (int c = 0; c < ncl; ++c)
+                            st_async4(peer_addr(slot, (uint32_t)c), part.x, part.y, part.z, part.w,
+                                      peer_addr(&vfull[b], (uint32_t)c));
                     }
                 }
             }
