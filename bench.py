@@ -53,6 +53,9 @@ def parse_args():
     p.add_argument("--latency-iters", type=int, default=50)
     p.add_argument("--no-extras", action="store_true",
                    help="skip e2e, cpu baseline and latency (for profiling runs)")
+    p.add_argument("--figure", action="store_true",
+                   help="the pages' micro-benchmark instead: latency of the base layer alone, "
+                        "with a per-adapter loop and with SGMV, over batch sizes and adapter counts")
     return p.parse_args()
 
 
@@ -589,9 +592,106 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def figure_point(sgmv, dev, W, A, B, T, n_adapters, seed):
+    """One point of the latency-vs-batch figure: T rows over n_adapters adapters
+    (round robin, shuffled).  Returns the three methods as callables on shared
+    buffers, the largest difference between the per-adapter loop and SGMV
+    relative to RMS(y), and the inputs (x, row -> adapter ids, y)."""
+    import torch
+
+    H1, H2 = W.shape
+    g = torch.Generator().manual_seed(seed)
+    ids = (torch.arange(T) % n_adapters)[torch.randperm(T, generator=g)].to(torch.int32)
+    x = torch.randn(T, H1, generator=g).to(W.dtype).to(dev)
+    y = torch.empty(T, H2, dtype=W.dtype, device=dev)
+    ra = ids.to(dev)
+    groups = [(int(a), (ids == a).nonzero().flatten().to(dev)) for a in torch.unique(ids)]
+    smax = sgmv.sgmv_max_segments(T, A.shape[0])
+    meta = (torch.empty(T, dtype=torch.int32, device=dev),
+            torch.empty(smax + 1, dtype=torch.int32, device=dev),
+            torch.empty(smax, dtype=torch.int32, device=dev),
+            torch.empty(1, dtype=torch.int32, device=dev))
+
+    def base():
+        torch.matmul(x, W, out=y)
+
+    def naive():  # the loop the pages compare against: one pair of matmuls per adapter
+        base()
+        for a, rows in groups:
+            y.index_add_(0, rows, (x.index_select(0, rows) @ A[a]) @ B[a])
+
+    def with_sgmv():
+        base()
+        sgmv.sgmv_apply_rows(y, x, A, B, ra, 1.0, out=meta)
+
+    naive()
+    y_naive = y.float().clone()
+    with_sgmv()
+    y_sgmv = y.float()
+    rms = y_naive.pow(2).mean().sqrt().item()
+    err = (y_naive - y_sgmv).abs().max().item() / max(rms, 1e-30)
+    return {"base": base, "naive": naive, "sgmv": with_sgmv}, err, (x, ids, y)
+
+
+def run_figure(args):
+    """The pages' micro-benchmark (the "Punica: when LoRA fine-tuned models need
+    multi-tenant serving" article, §2.2 figure): one Llama-2-7B q projection,
+    4096 -> 4096, r = 16, fp16, base weight W and 128 stacked adapters.  For
+    each point, the latency of y = x W alone, of that plus a per-adapter loop
+    of matmuls, and of that plus SGMV; one step after a 256 MB L2 flush, each
+    method captured as a CUDA graph, median of --latency-iters.  Batches of
+    1..128 rows on distinct adapters, then 2..100 adapters over 128 rows.
+    Prints one JSON line per point."""
+    import torch
+
+    from rank_gemv_gb300 import build as _build
+    from rank_gemv_gb300 import sgmv
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sgmv.load_library()
+    H, r, L = 4096, 16, 128
+    g = torch.Generator().manual_seed(args.seed)
+    W = (torch.randn(H, H, generator=g) * H ** -0.5).half().to(dev)
+    A = (torch.randn(L, H, r, generator=g) * H ** -0.5).half().to(dev)
+    B = (torch.randn(L, r, H, generator=g) * r ** -0.5).half().to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    points = [(T, T) for T in (1, 2, 4, 8, 16, 32, 64, 128)]
+    points += [(128, n) for n in (2, 4, 8, 16, 32, 64, 100)]
+    for i, (T, n) in enumerate(points):
+        fns, err, _ = figure_point(sgmv, dev, W, A, B, T, n, args.seed + i)
+        assert err < 2e-2, f"per-adapter loop and SGMV disagree at T={T}, adapters={n}: {err}"
+        out = {"figure": "latency_vs_batch", "layer": "llama2-7b q 4096x4096, r=16, fp16",
+               "T": T, "adapters": n, "unit": "us", "max_diff_over_rms": err}
+        for name, fn in fns.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                fn()
+            ts = []
+            for it in range(args.latency_iters):
+                flush.fill_(it & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                graph.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            out[name] = statistics.median(ts)
+        assert sgmv.sgmv_get_device_error(dev) == 0
+        print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.figure:
+        if rank == 0:
+            run_figure(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
