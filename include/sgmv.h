@@ -230,6 +230,27 @@ int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const
                        int32_t L, int32_t H1, int32_t H2, int32_t r, void *stream);
 
 /*
+ * Loads one adapter into slot `slot` of the stacked pools: A_src [H1][r] into
+ * A_pool[slot] and B_src [r][H2] into B_pool[slot], as two asynchronous copies
+ * on `stream`.  Page: [Review] "Punica: Multi-Tenant LoRA Serving" (nubint.ai
+ * review), "Proposed method" and findings: LoRA weights are loaded on demand,
+ * in milliseconds, instead of keeping every adapter resident.
+ *   A_pool  [L][H1][r]  device, in_dtype        stacked "A" matrices
+ *   B_pool  [L][r][H2]  device, in_dtype        stacked "B" matrices
+ *   A_src, B_src        host or device memory, in_dtype, contiguous; from
+ *                       page-locked host memory the copies overlap with
+ *                       kernels on other streams and return at once
+ * Nothing is allocated.  The caller orders the copies before the SGMV calls
+ * that read the slot (an event on `stream`) and must not overwrite a slot that
+ * an SGMV call in flight still reads.  Errors: SGMV_ERR_INVALID_ARG for null
+ * pointers, slot outside [0, L), non-positive sizes or an input type other
+ * than f16 / bf16; SGMV_ERR_CUDA if a copy cannot be enqueued.
+ */
+int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, const void *A_src,
+                      const void *B_src, int32_t L, int32_t H1, int32_t H2, int32_t r,
+                      void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's sticky
  * error word.  Returns SGMV_OK if no kernel reported an error since the last
  * read, else the first status code reported (SGMV_ERR_BAD_INDEX,

@@ -692,6 +692,24 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
     return st;
 }
 
+int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, const void *A_src,
+                      const void *B_src, int32_t L, int32_t H1, int32_t H2, int32_t r,
+                      void *stream) {
+    g_launches = 0;
+    if (!A_pool || !B_pool || !A_src || !B_src) return SGMV_ERR_INVALID_ARG;
+    if (L < 1 || H1 < 1 || H2 < 1 || r < 1 || slot < 0 || slot >= L) return SGMV_ERR_INVALID_ARG;
+    if (in_dtype != SGMV_F16 && in_dtype != SGMV_BF16) return SGMV_ERR_INVALID_ARG;
+    const size_t a_bytes = (size_t)H1 * (size_t)r * 2u, b_bytes = (size_t)r * (size_t)H2 * 2u;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = cuda_status("adapter A copy",
+                         cudaMemcpyAsync(static_cast<uint8_t *>(A_pool) + (size_t)slot * a_bytes,
+                                         A_src, a_bytes, cudaMemcpyDefault, s));
+    if (st != SGMV_OK) return st;
+    return cuda_status("adapter B copy",
+                       cudaMemcpyAsync(static_cast<uint8_t *>(B_pool) + (size_t)slot * b_bytes,
+                                       B_src, b_bytes, cudaMemcpyDefault, s));
+}
+
 int sgmv_get_device_error(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

@@ -45,6 +45,7 @@ SIGNATURES = {
                                _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sgmv_apply_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp,
                                   _i32, _i32, _i32, _i32, _i32, _vp]),
+    "sgmv_load_adapter": (_int, [_vp, _vp, _int, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
     "sgmv_get_device_error": (_int, [_vp]),
 }
 
@@ -237,6 +238,26 @@ def sgmv_apply_noalloc(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_h
         _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")),
         _nseg(idx, S), _ptr(sph), T, L, H1, H2, r, _stream(x.device)), "sgmv_apply_noalloc")
     return y
+
+
+def sgmv_load_adapter(A_pool, B_pool, slot, A_src, B_src, stream=None):
+    """Copy one adapter (A_src [H1, r], B_src [r, H2]; host -- ideally pinned --
+    or device tensors) into slot `slot` of the pools A_pool [L, H1, r] and
+    B_pool [L, r, H2], asynchronously on `stream` (default: the current
+    stream of the pools' device)."""
+    L, H1, r = A_pool.shape
+    H2 = B_pool.shape[2]
+    if tuple(A_src.shape) != (H1, r) or tuple(B_src.shape) != (r, H2):
+        raise ValueError("adapter shapes do not match the pools")
+    if A_src.dtype != A_pool.dtype or B_src.dtype != B_pool.dtype or A_pool.dtype != B_pool.dtype:
+        raise TypeError("adapter and pool types differ")
+    for t in (A_pool, B_pool, A_src, B_src):
+        if not t.is_contiguous():
+            raise TypeError("tensors must be contiguous")
+    st = (stream if stream is not None else torch.cuda.current_stream(A_pool.device)).cuda_stream
+    _check(load_library().sgmv_load_adapter(
+        _ptr(A_pool), _ptr(B_pool), _DTYPES[A_pool.dtype], int(slot), _ptr(A_src), _ptr(B_src),
+        L, H1, H2, r, st), "sgmv_load_adapter")
 
 
 def sgmv_get_device_error(device=None) -> int:

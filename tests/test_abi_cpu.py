@@ -157,3 +157,15 @@ def test_apply_rows_rejects_bad_arguments(lib):
     assert call(perm=A16) == 1          # metadata outputs: all or none
     assert call(ws=A16, wsb=8) == 6
     assert call(y_dt=5) == 1
+
+
+@pytest.mark.parametrize("kw", [
+    dict(slot=-1), dict(slot=2), dict(L=0), dict(H1=0), dict(r=0), dict(in_dt=2),
+    dict(A=None), dict(B=None), dict(a=None), dict(b=None),
+])
+def test_load_adapter_rejects_bad_arguments(lib, kw):
+    args = dict(A=A16, B=A16, in_dt=0, slot=0, a=A16, b=A16, L=2, H1=64, H2=64, r=16)
+    args.update(kw)
+    assert lib.sgmv_load_adapter(args["A"], args["B"], args["in_dt"], args["slot"], args["a"],
+                                 args["b"], args["L"], args["H1"], args["H2"], args["r"],
+                                 None) == 1
