@@ -46,6 +46,7 @@ constexpr int kTcThreads = 128;  // 4 warps: one TMEM lane (tile row) per thread
 constexpr int kTcRows = 128;     // M of one tile
 constexpr int kKB = 64;          // k-block: 64 16-bit elements = one 128-byte swizzle row
 constexpr int kStages = 3;       // shrink ring depth
+constexpr int kShrinkProducers = 96;  // warps 1-3 of the shrink load its ring
 constexpr int kExpandThreads = 2 * kTcRows + 32;  // two epilogue groups + a copy / MMA warp
 constexpr int kExpandYStages = 2;  // most y stages per epilogue group
 constexpr int kExpandBStages = 3;  // most B stages
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kTcThreads)
                   blockIdx.y, false, report, s_info);
         if (lane == 0) {
             for (int s = 0; s < kStages; ++s) {
-                mbar_init(&full[s], kTcThreads + 1);  // 128 cp.async arrivals + the TMA one
+                mbar_init(&full[s], kShrinkProducers + 1);  // cp.async arrivals + the TMA one
                 mbar_init(&empty[s], 1);
             }
             mbar_init(&done, 1);
@@ -232,40 +233,58 @@ __global__ void __launch_bounds__(kTcThreads)
     const int k1 = min(H1, k0 + hk);
     const int nkb = k1 > k0 ? (k1 - k0 + kKB - 1) / kKB : 0;
 
-    auto issue_a = [&](int kb) {  // thread 0
+    auto issue_a = [&](int kb) {  // thread kTcThreads - kShrinkProducers (first producer)
         const int st = kb % kStages;
         mbar_arrive_expect_tx(&full[st], a_bytes);
         for (int c = 0; c < rk; c += 64)
             tma_load_3d(stage_a(st) + c * kKB * sizeof(Tin), tmap_a, c, k0 + kb * kKB, a,
                         &full[st]);
     };
-    if (tid == 0)
+    // Warp 0 issues the MMAs (lane 0); warps 1-3 are the producers: the
+    // first of them loads A by TMA, all of them gather the tile's X rows.
+    const int prod = tid - (kTcThreads - kShrinkProducers);  // producer index, < 0 in warp 0
+    if (prod == 0)
         for (int kb = 0; kb < min(nkb, kStages); ++kb) issue_a(kb);
 
-    // Physical row of this thread's tile row (metadata is complete before launch).
-    int row = -1;
-    if (tid < nrows) {
-        row = perm ? perm[p0 + tid] : p0 + tid;
+    // Physical rows of this producer's tile rows prod and prod + kShrinkProducers
+    // (metadata is complete before launch).
+    auto phys = [&](int m) {
+        if (m >= nrows) return -1;
+        int row = perm ? perm[p0 + m] : p0 + m;
         if (row < 0 || row >= nrows_all) {
             set_error(err, kErrBadIndex);
             row = -1;
         }
-    }
-    auto issue_x = [&](int kb) {  // every thread: the 8 chunks of its own row
+        return row;
+    };
+    const int row0 = prod >= 0 ? phys(prod) : -1;
+    const int m1 = prod + kShrinkProducers;
+    const int row1 = prod >= 0 && m1 < kTcRows ? phys(m1) : -1;
+    auto issue_x = [&](int kb) {  // every producer: the 8 chunks of its tile rows
         const int st = kb % kStages;
         uint8_t *xs = stage_x(st);
         const int kk0 = k0 + kb * kKB;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const int k = kk0 + c * 8;
-            const bool ok = row >= 0 && k < k1;
-            cp_async16(xs + sw128_offset(tid, c), ok ? gX + (size_t)row * H1 + k : gX,
+            const bool ok = row0 >= 0 && k < k1;
+            cp_async16(xs + sw128_offset(prod, c), ok ? gX + (size_t)row0 * H1 + k : gX,
                        ok ? 16u : 0u);
+        }
+        if (m1 < kTcRows) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int k = kk0 + c * 8;
+                const bool ok = row1 >= 0 && k < k1;
+                cp_async16(xs + sw128_offset(m1, c), ok ? gX + (size_t)row1 * H1 + k : gX,
+                           ok ? 16u : 0u);
+            }
         }
         cp_async_arrive(&full[st]);
     };
     pdl_wait();
-    for (int kb = 0; kb < min(nkb, kStages); ++kb) issue_x(kb);
+    if (prod >= 0)
+        for (int kb = 0; kb < min(nkb, kStages); ++kb) issue_x(kb);
     pdl_trigger();
 
     tc_fence_before();
@@ -274,10 +293,11 @@ __global__ void __launch_bounds__(kTcThreads)
     const uint32_t tmem = s_tmem;
     const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, rk);
     bool lost = false;
-    for (int kb = 0; kb < nkb; ++kb) {
-        const int st = kb % kStages;
-        const uint32_t ph = (uint32_t)((kb / kStages) & 1);
-        if (tid == 0) {
+    if (tid == 0) {
+        // MMA issuer: each k-block once its stage is full, then the stage back
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int st = kb % kStages;
+            const uint32_t ph = (uint32_t)((kb / kStages) & 1);
             if (!mbar_wait(&full[st], ph)) {
                 lost = true;
                 set_error(err, kErrTimeout);
@@ -292,17 +312,20 @@ __global__ void __launch_bounds__(kTcThreads)
                         sw128_desc(aa + kk * 2048, kKB * 128, 1024), idesc, (kb | kk) != 0);
             mma_commit(&empty[st]);
         }
-        if (kb + kStages < nkb) {
-            // one waiter, then the CTA barrier (sleeping waiters wake late)
-            int bad = 0;
-            if (tid == 0 && !mbar_wait(&empty[st], ph)) {
+    } else if (prod >= 0) {
+        // producers: refill a stage once the MMAs that read it are done; one
+        // producer waits, a producer-only barrier releases the others
+        for (int kb = kStages; kb < nkb; ++kb) {
+            const int st = kb % kStages;
+            const uint32_t ph = (uint32_t)(((kb / kStages) - 1) & 1);
+            if (prod == 0 && !mbar_wait(&empty[st], ph)) {
                 set_error(err, kErrTimeout);
                 mbar_wait(&empty[st], ph);
-                bad = 1;
+                lost = true;
             }
-            if (__syncthreads_or(bad)) lost = true;
-            if (tid == 0) issue_a(kb + kStages);
-            issue_x(kb + kStages);
+            named_sync<1, kShrinkProducers>();
+            if (prod == 0) issue_a(kb);
+            issue_x(kb);
         }
     }
     {
