@@ -386,12 +386,8 @@ def run_ours(args, rank, world, local):
     kernel_s = timed_replays(k_full, n, k_rem, K)
     assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during timing"
 
-    if world > 1:
-        t = torch.tensor([elapsed, kernel_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed, kernel_s = float(t[0]), float(t[1])
-
-    value = world * K * T / elapsed
+    elapsed, kernel_s = max_over_ranks([elapsed, kernel_s], world, dev)
+    value = replica_throughput(world, K, T, elapsed)
     peak, peak_kind = measured_peak()
     # roofline of one update call (the streaming kernel for decode batches;
     # streaming + tensor-core shrink + expand for prefill), timed alone in a
@@ -593,6 +589,25 @@ def run_reference(args, rank, world):
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def max_over_ranks(values, world, device=None):
+    """The largest of each value over all ranks (the job's time is its slowest
+    replica's); the values themselves when there is one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def replica_throughput(world, K, T, elapsed):
+    """Rows/s of the whole job: every replica ran K steps of T rows within
+    `elapsed` seconds (the slowest rank's time)."""
+    return world * K * T / elapsed
 
 
 def figure_point(sgmv, dev, W, A, B, T, n_adapters, seed):
