@@ -205,7 +205,11 @@ bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max
     const uint32_t act = align_up((uint32_t)trows * (uint32_t)p.hn * std::max(es, ys), 128);
     p.stage_bytes = w + act;
     p.act_off = w;
-    const uint32_t red = (uint32_t)(kStreamConsumers / 32) * 8u * (uint32_t)rk * 4u;
+    // 16 compute warps when a CTA owns whole tiles (more warps to hide the
+    // compute warps' latencies; one CTA per SM anyway); a function of T and
+    // the dimensions only, like the cluster size: it fixes the summation order
+    l.cw = cl == 1 ? 16 : 8;
+    const uint32_t red = (uint32_t)l.cw * 8u * (uint32_t)rk * 4u;
     const uint32_t recv = cl > 1 ? 2u * (uint32_t)cl * 8u * (uint32_t)rk * 4u : 0u;
     const uint32_t vbytes = 2u * 8u * (uint32_t)rk * 4u;
     const uint32_t tab = (uint32_t)kStreamMaxTiles * 12u * 4u;

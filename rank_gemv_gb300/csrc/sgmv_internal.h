@@ -139,8 +139,8 @@ int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int3
 
 
 // ---- persistent streaming CUDA-core kernel (short segments, r <= 32) -------
-constexpr int kStreamConsumers = 256;                   // 8 compute warps
-constexpr int kStreamThreads = kStreamConsumers + 32;   // + 1 copy-issuing warp
+// Compute warps per CTA: 8 (two CTAs fit on an SM), or 16 when one CTA owns
+// whole tiles and a whole SM; plus one copy-issuing warp.
 constexpr int kStreamMaxStages = 8;
 constexpr int kStreamMaxTiles = 64;   // tiles one cluster walks in one launch
 // Columns of one A chunk and of one B chunk at rank bound RK (32 KB of
@@ -186,6 +186,7 @@ struct StreamLaunch {
     StreamParams p;
     int in_dtype, y_dtype;
     int rk;          // 16 or 32: compile-time bound on r
+    int cw;          // compute warps: 8 or 16
     bool grouped;
     cudaStream_t stream;
 };

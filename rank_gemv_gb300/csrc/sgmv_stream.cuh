@@ -38,10 +38,10 @@
 
 namespace sgmv {
 
-constexpr int kStreamWarps = kStreamConsumers / 32;
 constexpr int kTileRows = 8;
 
-__device__ __forceinline__ void consumers_sync() { named_sync<1, kStreamConsumers>(); }
+// Barrier of the CW compute warps (the copy warp does not take part).
+template <int CW> __device__ __forceinline__ void consumers_sync() { named_sync<1, CW * 32>(); }
 
 // Walks a CTA's ring in order: A(0); then for m = 1 .. nt-1: A(m), B(m-1);
 // then B(nt-1).  Chunk = A(blk, i) when !isB, else B(blk - 1, i).
@@ -93,12 +93,12 @@ __device__ __forceinline__ void stream_wait(uint64_t *bar, uint32_t parity, bool
 // Thread (warp, lane) owns k-quad kq = lane % (RK/4) and the columns
 // h = warp*HL + lane/(RK/4) + HSTR*j of the slice, summed in increasing h;
 // the HL lanes of a k-quad are then summed by a butterfly in a fixed order.
-template <typename Tin, int RK, int R>
+template <typename Tin, int RK, int R, int CW>
 __device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes, uint32_t act_off,
                                               int nst, int &q, int nA, int hlen, int hn, int rk,
                                               uint64_t *full, uint64_t *empty, float *red,
                                               bool &lost, int *err) {
-    constexpr int KQ = RK / 4, HL = 32 / KQ, HSTR = kStreamWarps * HL;
+    constexpr int KQ = RK / 4, HL = 32 / KQ, HSTR = CW * HL;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int kq = lane % KQ, hl = lane / KQ;
     const int hoff = warp * HL + hl;
@@ -149,16 +149,16 @@ __device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes,
 }
 
 // Expand of one tile with R rows: y[row, j] += scale * v . B[a][:, j] for the
-// CTA's H2 slice; each thread owns JN / 512 pairs of adjacent columns of a
-// chunk and runs the r-sum in increasing k.
-template <typename Tin, typename Ty, int RK, int R>
+// CTA's H2 slice; each thread owns JN / (64 CW) pairs (at least one) of adjacent
+// columns of a chunk and runs the r-sum in increasing k.
+template <typename Tin, typename Ty, int RK, int R, int CW>
 __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes, uint32_t act_off,
                                               int nst, int &q, int nB, int jlen, int j0, int rk,
                                               const float *sv, const int (&row)[kTileRows],
                                               Ty *gY, int H2, float scale, uint64_t *full,
                                               uint64_t *empty, bool &lost, int *err) {
     constexpr int JN = kStreamChunkElems / RK;
-    constexpr int PP = JN / (2 * kStreamConsumers);
+    constexpr int PP = JN / (2 * CW * 32) > 0 ? JN / (2 * CW * 32) : 1;
     const int tid = threadIdx.x;
     for (int i = 0; i < nB; ++i, ++q) {
         const int s = q % nst;
@@ -169,7 +169,7 @@ __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes,
         const Ty *Ys = reinterpret_cast<const Ty *>(base + act_off);
 #pragma unroll
         for (int pp = 0; pp < PP; ++pp) {
-            const int c = 2 * (tid + pp * kStreamConsumers);
+            const int c = 2 * (tid + pp * CW * 32);
             if (c >= nj) break;
             // B chunk in shared memory: boxes of 256 columns, [box][k][256]
             const Tin *bcol = Bs + (c >> 8) * rk * 256 + (c & 255);
@@ -214,9 +214,10 @@ __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes,
     }
 }
 
-template <typename Tin, typename Ty, int RK, bool GROUPED>
-__global__ void __launch_bounds__(kStreamThreads, 2)
+template <typename Tin, typename Ty, int RK, bool GROUPED, int CW>
+__global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
     sgmv_stream_kernel(const __grid_constant__ StreamParams P) {
+    constexpr int kStreamConsumers = CW * 32, kStreamWarps = CW, kStreamThreads = CW * 32 + 32;
     // Parameters read once into registers (see sgmv_cc.cuh).
     const int T = P.T, L = P.L, H1 = P.H1, H2 = P.H2, rk = P.r;
     const int ncl = P.cl, G = P.G, hn = P.hn, nst = P.nst;
@@ -609,18 +610,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             if (m < nt) {
                 const int n = (int)lds32(tab + 4 * m + 1);
                 if (n <= 1)
-                    stream_shrink<Tin, RK, 1>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                    stream_shrink<Tin, RK, 1, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
                                               full, empty, red, lost, err);
                 else if (n <= 2)
-                    stream_shrink<Tin, RK, 2>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                    stream_shrink<Tin, RK, 2, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
                                               full, empty, red, lost, err);
                 else if (n <= 4)
-                    stream_shrink<Tin, RK, 4>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                    stream_shrink<Tin, RK, 4, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
                                               full, empty, red, lost, err);
                 else
-                    stream_shrink<Tin, RK, 8>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
+                    stream_shrink<Tin, RK, 8, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
                                               full, empty, red, lost, err);
-                consumers_sync();
+                consumers_sync<CW>();
                 // this CTA's partial of v, four consecutive k per thread
                 part = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (tid < n * (rk / 4)) {
@@ -666,7 +667,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                     // m-1, which the wait above saw.
                     const int b = m & 1;
                     const int n = (int)lds32(tab + 4 * m + 1);
-                    consumers_sync();  // this CTA's reads of its own slots are done
+                    consumers_sync<CW>();  // this CTA's reads of its own slots are done
                     if (tid == 0)
                         mbar_arrive_expect_tx(&vfull[b], (uint32_t)(ncl * n * rk) * 4u);
                     if (tid < n * (rk / 4)) {
@@ -678,7 +679,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                     }
                 }
             }
-            consumers_sync();  // s_v of tile m-1 is complete
+            consumers_sync<CW>();  // s_v of tile m-1 is complete
             if (m >= 1) {
                 const int mm = m - 1;
                 const int n = (int)lds32(tab + 4 * mm + 1);
@@ -687,16 +688,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 for (int t = 0; t < kTileRows; ++t) row[t] = (int)lds32(trow + kTileRows * mm + t);
                 const float *sv = s_v + (mm & 1) * kTileRows * RK;
                 if (n <= 1)
-                    stream_expand<Tin, Ty, RK, 1>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                    stream_expand<Tin, Ty, RK, 1, CW>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
                                                   rk, sv, row, gY, H2, scale, full, empty, lost, err);
                 else if (n <= 2)
-                    stream_expand<Tin, Ty, RK, 2>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                    stream_expand<Tin, Ty, RK, 2, CW>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
                                                   rk, sv, row, gY, H2, scale, full, empty, lost, err);
                 else if (n <= 4)
-                    stream_expand<Tin, Ty, RK, 4>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                    stream_expand<Tin, Ty, RK, 4, CW>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
                                                   rk, sv, row, gY, H2, scale, full, empty, lost, err);
                 else
-                    stream_expand<Tin, Ty, RK, 8>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
+                    stream_expand<Tin, Ty, RK, 8, CW>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
                                                   rk, sv, row, gY, H2, scale, full, empty, lost, err);
             }
         }
@@ -707,30 +708,31 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 
 // ---- host-side launcher for one input type ----------------------------------
 template <typename Tin, typename Ty, int RK>
-static void *stream_pick(bool grouped) {
-    return grouped ? (void *)sgmv_stream_kernel<Tin, Ty, RK, true>
-                   : (void *)sgmv_stream_kernel<Tin, Ty, RK, false>;
+static void *stream_pick(bool grouped, int cw) {
+    if (grouped) return (void *)sgmv_stream_kernel<Tin, Ty, RK, true, 8>;
+    return cw == 16 ? (void *)sgmv_stream_kernel<Tin, Ty, RK, false, 16>
+                    : (void *)sgmv_stream_kernel<Tin, Ty, RK, false, 8>;
 }
 
 template <typename Tin, typename Ty>
-static void *stream_pick_rk(int rk, bool grouped) {
-    return rk == 16 ? stream_pick<Tin, Ty, 16>(grouped) : stream_pick<Tin, Ty, 32>(grouped);
+static void *stream_pick_rk(int rk, bool grouped, int cw) {
+    return rk == 16 ? stream_pick<Tin, Ty, 16>(grouped, cw) : stream_pick<Tin, Ty, 32>(grouped, cw);
 }
 
 template <typename Tin>
 static int stream_launch_impl(const StreamLaunch &l) {
     void *fn;
     switch (l.y_dtype) {
-        case 0: fn = stream_pick_rk<Tin, __half>(l.rk, l.grouped); break;
-        case 1: fn = stream_pick_rk<Tin, __nv_bfloat16>(l.rk, l.grouped); break;
-        default: fn = stream_pick_rk<Tin, float>(l.rk, l.grouped); break;
+        case 0: fn = stream_pick_rk<Tin, __half>(l.rk, l.grouped, l.cw); break;
+        case 1: fn = stream_pick_rk<Tin, __nv_bfloat16>(l.rk, l.grouped, l.cw); break;
+        default: fn = stream_pick_rk<Tin, float>(l.rk, l.grouped, l.cw); break;
     }
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)l.p.smem_bytes);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)l.p.cl, (unsigned)l.p.G, 1);
-    cfg.blockDim = dim3(kStreamThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)(l.cw * 32 + 32), 1, 1);
     cfg.dynamicSmemBytes = l.p.smem_bytes;
     cfg.stream = l.stream;
     cudaLaunchAttribute attrs[2];
