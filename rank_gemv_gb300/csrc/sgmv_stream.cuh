@@ -702,8 +702,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
             }
         }
     }
-    // No CTA leaves while a peer may still write into its shared memory.
-    if (ncl > 1) cluster_sync();
+    // No closing cluster barrier: the only accesses to another CTA's shared
+    // memory are the st.async pushes of partial v, and every CTA waits for all
+    // pushes addressed to it (its vfull barriers) before it gets here.
 }
 
 // ---- host-side launcher for one input type ----------------------------------
