@@ -456,60 +456,101 @@ def distinct_vs_shared(args, dev, sgmv, wl):
 
 
 def e2e(args, dev, sgmv, wl, world, seed, K, W):
-    """The metric through the public API with host buffers: per step, copy the
-    batch's rows, row->adapter ids and Y from pinned memory, group + apply,
-    copy Y back and wait for it on the host."""
+    """The metric through the public API with host buffers, as a serving loop
+    runs it: every step copies that step's inputs (rows, row -> adapter ids,
+    y) from page-locked host memory, groups and applies, and copies y back;
+    the host waits for, and reads, each step's result.  Steps are pipelined
+    two deep: two sets of buffers, each step one CUDA-graph replay of those
+    copies and API calls, and the host waits for step s-2's result just
+    before step s reuses its buffers."""
     import torch
 
     if args.workload == "llama7b-stack":
         # inputs per step: the 224 projections' X and Y rows and the ids
-        stack = StackBatch(seed, dev, sgmv)
-        hx = [X.cpu().pin_memory() for X, _, _, _ in stack.projs]
-        hy = [Y.cpu().pin_memory() for _, _, _, Y in stack.projs]
-        hout = [torch.empty_like(h).pin_memory() for h in hy]
-        hra = stack.ra.cpu().pin_memory()
+        sets = []
+        for _ in range(2):
+            stack = StackBatch(seed, dev, sgmv)
+            hx = [X.cpu().pin_memory() for X, _, _, _ in stack.projs]
+            hy = [Y.cpu().pin_memory() for _, _, _, Y in stack.projs]
+            hout = [torch.empty_like(h).pin_memory() for h in hy]
+            hra = stack.ra.cpu().pin_memory()
+            sets.append((stack, hx, hy, hout, hra))
 
-        def one():
-            stack.ra.copy_(hra, non_blocking=True)
-            for (X, _, _, Y), a, b in zip(stack.projs, hx, hy):
-                X.copy_(a, non_blocking=True)
-                Y.copy_(b, non_blocking=True)
-            stack.step(sgmv)
-            for (_, _, _, Y), o in zip(stack.projs, hout):
-                o.copy_(Y, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+        def make_step(st):
+            stack, hx, hy, hout, hra = st
 
-        h2d = sum(h.nbytes for h in hx) + sum(h.nbytes for h in hy) + hra.nbytes
-        d2h = sum(h.nbytes for h in hout)
-        T = stack.T
+            def one():
+                stack.ra.copy_(hra, non_blocking=True)
+                for (X, _, _, Y), a, b in zip(stack.projs, hx, hy):
+                    X.copy_(a, non_blocking=True)
+                    Y.copy_(b, non_blocking=True)
+                stack.step(sgmv)
+                for (_, _, _, Y), o in zip(stack.projs, hout):
+                    o.copy_(Y, non_blocking=True)
+            return one, hout[0]
+
+        stack0, hx0, hy0, hout0, hra0 = sets[0]
+        h2d = sum(h.nbytes for h in hx0) + sum(h.nbytes for h in hy0) + hra0.nbytes
+        d2h = sum(h.nbytes for h in hout0)
+        T = stack0.T
         K = min(K, 20)
     else:
         w = wl.make(args.workload, seed)
-        b = Batch(w, dev, sgmv)
-        hx, hy, hra = w.X.pin_memory(), w.Y0.pin_memory(), w.row_adapter.pin_memory()
-        hout = torch.empty_like(hy).pin_memory()
+        sets = []
+        for _ in range(2):
+            b = Batch(w, dev, sgmv)
+            sets.append((b, w.X.clone().pin_memory(), w.Y0.clone().pin_memory(),
+                         w.row_adapter.clone().pin_memory(), torch.empty_like(w.Y0).pin_memory()))
 
-        def one():
-            b.X.copy_(hx, non_blocking=True)
-            b.Y.copy_(hy, non_blocking=True)
-            b.ra.copy_(hra, non_blocking=True)
-            b.step(sgmv)
-            hout.copy_(b.Y, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+        def make_step(st):
+            b, hx, hy, hra, hout = st
 
-        h2d, d2h, T = hx.nbytes + hy.nbytes + hra.nbytes, hout.nbytes, w.T
-    for _ in range(W):
-        one()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            def one():
+                b.X.copy_(hx, non_blocking=True)
+                b.Y.copy_(hy, non_blocking=True)
+                b.ra.copy_(hra, non_blocking=True)
+                b.step(sgmv)
+                hout.copy_(b.Y, non_blocking=True)
+            return one, hout
+
+        b0, hx0, hy0, hra0, hout0 = sets[0]
+        h2d, d2h, T = hx0.nbytes + hy0.nbytes + hra0.nbytes, hout0.nbytes, w.T
+    steps = [make_step(st) for st in sets]
+    for one, _ in steps:  # eager warm-up, then one graph per buffer set
+        for _ in range(W):
+            one()
     torch.cuda.synchronize()
+    graphs = [capture([one]) for one, _ in steps]
+    outs = [out for _, out in steps]
+    done = [torch.cuda.Event() for _ in steps]
+    checksum = 0.0
+
+    def run(n):
+        nonlocal checksum
+        for s_ in range(n):
+            i = s_ % 2
+            if s_ >= 2:
+                done[i].synchronize()                  # step s-2's result is on the host
+                checksum += float(outs[i].view(-1)[0])  # ... and read there
+            graphs[i].replay()
+            done[i].record()
+        for i in range(min(n, 2)):
+            done[i].synchronize()
+            checksum += float(outs[i].view(-1)[0])
+
+    run(W)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
     e0.record()
-    for _ in range(K):
-        one()
+    run(K)
     e1.record()
     torch.cuda.synchronize()
-    el = e0.elapsed_time(e1) / 1e3
+    wall = time.perf_counter() - t0
+    el = max(e0.elapsed_time(e1) / 1e3, wall)
     return {"value": world * K * T / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3}
+            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3,
+            "pipelining": "2 steps in flight; host waits for and reads every step's result"}
 
 
 # -------------------------------------------------- oracle (host cores)
