@@ -168,7 +168,7 @@ constexpr uint32_t kStreamSmemMax = 200u * 1024u;
 
 // Launch shape of the streaming kernel for a batch of T rows in S segments
 // (the last max_len rows long at most), or false when the kernel does not
-// apply (r not a multiple of 4 or above 32, or more tiles per cluster than its
+// apply (r not a multiple of 4 or above 64, or more tiles per cluster than its
 // table holds).  Rows per tile: 1 when segments average up to 2 rows (every
 // row streams its adapter on its own; rows that share an adapter read it
 // again from L2), up to 8 for longer segments, whose rows then share each
@@ -178,7 +178,7 @@ constexpr uint32_t kStreamSmemMax = 200u * 1024u;
 // with at least 64 columns of H1 and of H2.
 bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len, int32_t H1,
                   int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l) {
-    if (r % 4 != 0 || r > 32 || T <= 0 || S <= 0) return false;
+    if (r % 4 != 0 || r > 64 || T <= 0 || S <= 0) return false;
     const int64_t avg = ceil_div(T, S);
     const int trows = avg <= 2 ? 1 : avg <= 4 ? 2 : avg <= 8 ? 4 : 8;
     const int64_t slots = tile_slots(T, S, seg_ptr_host, trows, 1, max_len);
@@ -190,7 +190,7 @@ bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max
     const int64_t gmax = std::max(1, nsm / cl);
     if (ceil_div(T, gmax) > kStreamMaxTiles) return false;
     StreamParams &p = l.p;
-    const int rk = r <= 16 ? 16 : 32;
+    const int rk = r <= 16 ? 16 : r <= 32 ? 32 : 64;
     p.cl = cl;
     p.G = (int32_t)std::min<int64_t>(slots, gmax);
     p.hc = round8(ceil_div(H1, cl));

@@ -138,7 +138,7 @@ int build_segments_launch(const int32_t *row_adapter, int32_t T, int32_t L, int3
                           cudaStream_t stream);
 
 
-// ---- persistent streaming CUDA-core kernel (short segments, r <= 32) -------
+// ---- persistent streaming CUDA-core kernel (short segments, r <= 64) -------
 // Compute warps per CTA: 8 (two CTAs fit on an SM), or 16 when one CTA owns
 // whole tiles and a whole SM; plus one copy-issuing warp.
 constexpr int kStreamMaxStages = 8;
@@ -185,7 +185,7 @@ struct StreamParams {
 struct StreamLaunch {
     StreamParams p;
     int in_dtype, y_dtype;
-    int rk;          // 16 or 32: compile-time bound on r
+    int rk;          // 16, 32 or 64: compile-time bound on r
     int cw;          // compute warps: 8 or 16
     bool grouped;
     cudaStream_t stream;

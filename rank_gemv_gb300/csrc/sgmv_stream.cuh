@@ -1,5 +1,5 @@
 // sgmv_stream.cuh -- persistent streaming CUDA-core SGMV kernel for
-// decode-sized segments (rank r <= 32, r a multiple of 4).
+// decode-sized segments (rank r <= 64, r a multiple of 4).
 //
 // Method ("Punica: when LoRA fine-tuned models need multi-tenant serving",
 // omica.com.cn article, §2.2): for every row of a segment, shrink
@@ -650,8 +650,8 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                         lost = true;
                     }
                     const int n1 = (int)lds32(tab + 4 * (m - 1) + 1);
-                    if (tid < n1 * rk) {
-                        const int t = tid / rk, k = tid - (tid / rk) * rk;
+                    for (int e = tid; e < n1 * rk; e += kStreamConsumers) {
+                        const int t = e / rk, k = e - (e / rk) * rk;
                         float sum = 0.f;
                         for (int c = 0; c < ncl; ++c)
                             sum += ldsf(recv + ((b * ncl + c) * kTileRows + t) * RK + k);
@@ -717,7 +717,11 @@ static void *stream_pick(bool grouped, int cw) {
 
 template <typename Tin, typename Ty>
 static void *stream_pick_rk(int rk, bool grouped, int cw) {
-    return rk == 16 ? stream_pick<Tin, Ty, 16>(grouped, cw) : stream_pick<Tin, Ty, 32>(grouped, cw);
+    switch (rk) {
+        case 16: return stream_pick<Tin, Ty, 16>(grouped, cw);
+        case 32: return stream_pick<Tin, Ty, 32>(grouped, cw);
+        default: return stream_pick<Tin, Ty, 64>(grouped, cw);
+    }
 }
 
 template <typename Tin>

@@ -1,4 +1,4 @@
-// Streaming CUDA-core SGMV kernel, f16 inputs (all output types, r <= 16 / 32).
+// Streaming CUDA-core SGMV kernel, f16 inputs (all output types, rank bounds 16 / 32 / 64).
 #include "sgmv_stream.cuh"
 
 namespace sgmv {
