@@ -168,6 +168,22 @@ __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Bulk reduction shared -> global, in L2: dst[i] += src[i] for `bytes` / 4
+// floats (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_s2g_add_f32(float *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+// ... until at most one committed group is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// ... until every committed bulk operation of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---- clusters / distributed shared memory ---------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;

@@ -18,15 +18,19 @@
 //   the expand can run on 16-bit tensor cores and still see v to about
 //   16 significant bits.
 // Expand (sgmv_tc_expand_kernel): one CTA per (128-row tile, run of column
-//   blocks of N = 64 (fp32 y) or 128 columns), about one wave in all.  The
-//   tile's v hi/lo is loaded once (TMA, K-major); per block, TMA brings
-//   B[a][:, j:j+N] (N-major) and 2 x r/16 MMAs accumulate v_hi.B + v_lo.B into
-//   one of two TMEM buffers, so block k+1's products are made while block k's
-//   epilogue runs.  y comes in by 16-byte cp.async copies (coalesced: a warp
-//   reads two 256-byte row pieces per instruction) through a 2-3 stage ring
-//   filled ahead; each thread owns one row: tcgen05.ld 32 columns at a time,
-//   y += scale * acc in fp32, rounded once; coalesced 16-byte stores write
-//   the block back.
+//   blocks of N = 64 (fp32 y) or 128 columns), one CTA per SM in all; the
+//   CTAs are dealt to the tiles in proportion to each tile's cost (its rows
+//   plus a fixed cost per block).  The tile's v hi/lo is loaded once (TMA,
+//   K-major).  A B warp streams B[a][:, j:j+N] (N-major) through a ring; the
+//   MMA warp makes 2 x r/16 MMAs per block, v_hi.B + v_lo.B, into one of
+//   four (fp32 y) or two TMEM buffers, so it runs up to that many blocks
+//   ahead of the epilogue.  Two epilogue groups take alternate blocks; each
+//   thread owns one row and reads 32 accumulator columns per tcgen05.ld.
+//   fp32 y: the row's scale * acc goes to shared memory and one bulk
+//   reduction per row adds it to y in L2 (y never passes through the SM).
+//   16-bit y: y comes in by coalesced 16-byte cp.async copies through a
+//   2-stage ring, y += scale * acc in fp32 is rounded once, and coalesced
+//   16-byte stores write the block back.
 // Every mbarrier wait is bounded; TMEM is freed on every path.
 #include <mutex>
 
@@ -47,9 +51,13 @@ constexpr int kTcRows = 128;     // M of one tile
 constexpr int kKB = 64;          // k-block: 64 16-bit elements = one 128-byte swizzle row
 constexpr int kStages = 3;       // shrink ring depth
 constexpr int kShrinkProducers = 96;  // warps 1-3 of the shrink load its ring
-constexpr int kExpandThreads = 2 * kTcRows + 32;  // two epilogue groups + a copy / MMA warp
+constexpr int kExpandThreads = 2 * kTcRows + 64;  // two epilogue groups, an MMA warp, a B warp
 constexpr int kExpandYStages = 2;  // most y stages per epilogue group
 constexpr int kExpandBStages = 3;  // most B stages
+// Fixed cost of one column block of the expand (its MMAs, barriers and
+// epilogue steps), in the y rows that take as long: part of a tile's weight
+// when the expand's CTAs are dealt to tiles.
+constexpr int kExpandBlockRows = 128;
 constexpr size_t kExpandSmemMax = 220u * 1024u;
 
 struct TCShrinkParams {
@@ -69,7 +77,8 @@ struct TCExpandParams {
     const int32_t *perm, *seg_ptr, *idx;
     int *err;
     int32_t S, T, L, H2, r, min_len, max_len;
-    int32_t nb;   // column blocks per CTA
+    int32_t kw;   // weight of a tile = its rows + kw (B bytes of a column block in y rows)
+    int32_t red;  // fp32 y updated by bulk reductions in L2 (H2 % 4 == 0)
     int32_t ny;   // y stages per epilogue group (1 or 2)
     int32_t nbs;  // B stages (2 or 3)
     float scale;
@@ -409,6 +418,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     constexpr int CH = N * (int)sizeof(Ty) / 16;  // 16-byte chunks of a row's block (16)
     constexpr int RPI = kTcRows / CH;              // rows covered by one pass of a group (8)
     constexpr int E16 = 16 / (int)sizeof(Ty);      // elements per chunk
+    constexpr int NACC = 256 / N;                  // TMEM accumulator buffers (4 or 2)
     const int32_t *const seg_ptr = P.seg_ptr;
     const int32_t *const idx = P.idx;
     const int32_t *const perm = P.perm;
@@ -423,38 +433,41 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t bar_v, b_full[kExpandBStages], b_empty[kExpandBStages];
-    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], y_full[2][kExpandYStages];
-    __shared__ int s_info[4];
+    __shared__ __align__(8) uint64_t acc_full[4], acc_empty[4], y_full[2][kExpandYStages];
+    __shared__ int s_info[6];
     __shared__ int s_row[kTcRows];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
 
     const int nblk = (H2 + N - 1) / N;
-    const int b0 = (int)blockIdx.x * P.nb;
-    const int nb = min(nblk, b0 + P.nb) - b0;  // column blocks of this CTA (>= 1)
 
     if (warp == 0) {
-        find_tile(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, min_len, max_len, err,
-                  blockIdx.y, false, report, s_info);
+        find_share(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, P.kw, min_len, max_len, err,
+                   (int)blockIdx.x, (int)gridDim.x, report, s_info);
         if (lane == 0) {
             mbar_init(&bar_v, 1);
             for (int i = 0; i < nbs; ++i) {
                 mbar_init(&b_full[i], 1);
                 mbar_init(&b_empty[i], 1);
             }
-            for (int g = 0; g < 2; ++g) {
-                mbar_init(&acc_full[g], 1);
-                mbar_init(&acc_empty[g], kTcRows / 32);  // one arrival per warp of the group
-                for (int i = 0; i < ny; ++i) mbar_init(&y_full[g][i], kTcRows);  // cp.async, per thread
+            for (int b = 0; b < NACC; ++b) {
+                mbar_init(&acc_full[b], 1);
+                mbar_init(&acc_empty[b], kTcRows / 32);  // one arrival per warp of its group
             }
+            for (int g = 0; g < 2; ++g)
+                for (int i = 0; i < ny; ++i) mbar_init(&y_full[g][i], kTcRows);  // cp.async, per thread
             mbar_init_fence();
         }
     }
     __syncthreads();
-    if (s_info[0] < 0 || nb <= 0) return;
+    if (s_info[0] < 0) return;
     const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
-    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)(2 * N));
+    // this CTA's run of the tile's column blocks: an even split over its CTAs
+    const int b0 = (int)((long long)s_info[4] * nblk / s_info[5]);
+    const int nb = (int)((long long)(s_info[4] + 1) * nblk / s_info[5]) - b0;
+    if (nb <= 0) return;
+    if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)(NACC * N));
 
     uint8_t *base = align1024(dsm);
     const uint32_t v_bytes = (uint32_t)rk * 256u;   // [128 rows][r] 16-bit, as r/64 K-blocks
@@ -482,9 +495,9 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const uint32_t tmem = s_tmem;
     pdl_trigger();
 
-    if (warp == kExpandThreads / 32 - 1) {
-        // ---- copy / MMA warp: B through a ring, the tile's v once, products
-        // of block k into accumulator buffer k & 1 (the buffer of group k & 1)
+    if (warp == 2 * kTcRows / 32 + 1) {
+        // ---- B warp: B[a][:, block k] through the ring, a stage refilled as
+        // soon as the products that read it are made
         if (lane == 0) {
             auto load_b = [&](int k) {
                 const int st = k % nbs;
@@ -494,6 +507,18 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                                 (b0 + k) * N + c, 0, a, &b_full[st]);
             };
             for (int k = 0; k < min(nbs, nb); ++k) load_b(k);  // weights: before the wait
+            for (int k = nbs; k < nb; ++k) {
+                if (!mbar_wait(&b_empty[k % nbs], (uint32_t)(((k / nbs) - 1) & 1))) {
+                    set_error(err, kErrTimeout);
+                    break;
+                }
+                load_b(k);
+            }
+        }
+    } else if (warp == 2 * kTcRows / 32) {
+        // ---- MMA warp: the tile's v once, then the products of block k into
+        // accumulator buffer k % NACC (read by epilogue group k & 1)
+        if (lane == 0) {
             pdl_wait();
             mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);  // v: written by the shrink kernel
             for (int kb = 0; kb < rk / kKB; ++kb) {
@@ -508,12 +533,12 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             };
             const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, N);
             for (int k = 0; k < nb; ++k) {
-                const int st = k % nbs, g = k & 1;
+                const int st = k % nbs, ab = k % NACC;
                 pwait(&b_full[st], (uint32_t)((k / nbs) & 1));
-                if (k >= 2) pwait(&acc_empty[g], (uint32_t)(((k >> 1) - 1) & 1));
+                if (k >= NACC) pwait(&acc_empty[ab], (uint32_t)(((k / NACC) - 1) & 1));
                 tc_fence_after();
                 const uint32_t ba = smem_addr(b_stage0 + (size_t)st * b_bytes);
-                const uint32_t d = tmem + (uint32_t)(g * N);
+                const uint32_t d = tmem + (uint32_t)(ab * N);
                 uint32_t acc = 0;
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t va = smem_addr(h ? vlo_tile : vhi_tile);
@@ -526,12 +551,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                             acc = 1;
                         }
                 }
-                mma_commit(&acc_full[g]);
+                mma_commit(&acc_full[ab]);
                 mma_commit(&b_empty[st]);
-                if (k + nbs < nb) {  // refill the stage once block k's products are made
-                    pwait(&b_empty[st], (uint32_t)((k / nbs) & 1));
-                    load_b(k + nbs);
-                }
             }
             if (!ok) set_error(err, kErrTimeout);
         }
@@ -557,8 +578,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             }
             cp_async_arrive(&y_full[g][i % ny]);
         };
-        pdl_wait();  // y may be written by the previous kernel
-        for (int i = 0; i < min(ny, nmine); ++i) load_y(i);
+        const int my_row = s_row[lt];
         bool lost = false;
         auto wait = [&](uint64_t *bar, uint32_t par) {
             if (!mbar_wait(bar, par)) {
@@ -567,10 +587,48 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                 lost = true;
             }
         };
-        const int my_row = s_row[lt];
+        pdl_wait();  // y may be written by the previous kernel
+        if (P.red) {
+            // fp32 y: y += scale * acc by one bulk reduction per row and block,
+            // added in L2, so y never passes through the SM.  Stage i % ny
+            // holds scale * acc of the group's i-th block, one row per thread.
+            for (int i = 0; i < nmine; ++i) {
+                const int k = g + 2 * i, ab = k % NACC;
+                wait(&acc_full[ab], (uint32_t)((k / NACC) & 1));
+                tc_fence_after();
+                if (i >= ny) {  // the reduction that last read this stage is done with it
+                    if (ny == 2) bulk_wait_read1();
+                    else bulk_wait_read();
+                }
+                uint8_t *yr = my_y + (size_t)(i % ny) * ystage_bytes + (size_t)lt * YP;
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(ab * N + c0), v);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        sts128(yr + (c0 + 4 * q) * 4,
+                               make_uint4(__float_as_uint(scale * v[4 * q]),
+                                          __float_as_uint(scale * v[4 * q + 1]),
+                                          __float_as_uint(scale * v[4 * q + 2]),
+                                          __float_as_uint(scale * v[4 * q + 3])));
+                }
+                // the accumulator buffer is free for block k + NACC
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                fence_proxy_async();  // this thread's row -> the bulk copy unit
+                const int j = (b0 + k) * N;
+                if (!lost && my_row >= 0)
+                    bulk_s2g_add_f32(reinterpret_cast<float *>(gY) + (size_t)my_row * H2 + j, yr,
+                                     (uint32_t)min(N, H2 - j) * 4u);
+                bulk_commit();
+            }
+            bulk_wait_all();
+        } else {
+        for (int i = 0; i < min(ny, nmine); ++i) load_y(i);
         for (int i = 0; i < nmine; ++i) {
-            const int k = g + 2 * i;
-            wait(&acc_full[g], (uint32_t)(i & 1));
+            const int k = g + 2 * i, ab = k % NACC;
+            wait(&acc_full[ab], (uint32_t)((k / NACC) & 1));
             tc_fence_after();
             wait(&y_full[g][i % ny], (uint32_t)((i / ny) & 1));
             // y row in shared memory += scale * accumulator row, 32 columns at a time
@@ -578,7 +636,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             uint8_t *yr = st + (size_t)lt * YP;
             for (int c0 = 0; c0 < N; c0 += 32) {
                 float v[32];
-                tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(g * N + c0), v);
+                tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(ab * N + c0), v);
                 if (my_row >= 0) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -591,10 +649,10 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                     }
                 }
             }
-            // the accumulator buffer is free for block k + 2
+            // the accumulator buffer is free for block k + NACC
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[g]);
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
             group_sync(g);
             // write the block back: 16-byte stores, two row pieces per warp instruction
             {
@@ -613,12 +671,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             group_sync(g);  // stage i % ny has been read: refill it
             if (i + ny < nmine) load_y(i + ny);
         }
+        }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, (uint32_t)(2 * N));
+        tmem_dealloc(tmem, (uint32_t)(NACC * N));
     }
 }
 
@@ -765,10 +824,15 @@ int tc_launch_t(const TCArgs &g) {
     ep.max_len = g.max_len;
     ep.scale = g.scale;
     constexpr int N = tc_cols<Ty>();
-    const int nblk = (g.H2 + N - 1) / N;
-    // about one CTA per SM over all tiles: each CTA a run of column blocks
-    const int64_t want = std::max<int64_t>(1, g.nsm);
-    ep.nb = (int32_t)std::max<int64_t>(1, ((int64_t)nblk * g.slots + want - 1) / want);
+    // One CTA per SM (a multiple of the SM count when there are more tiles),
+    // dealt to the tiles in proportion to the bytes they move: y rows read
+    // and written, plus B once per column block (r / sizeof(y) rows' worth).
+    const int64_t nsm = std::max<int64_t>(1, g.nsm);
+    const int64_t nct = (((int64_t)g.slots + nsm - 1) / nsm) * nsm;
+    if (nct > 0x7fffffff) return (int)cudaErrorInvalidValue;
+    ep.kw = (int32_t)std::max<int64_t>(1, g.r / (int64_t)sizeof(Ty)) + kExpandBlockRows;
+    // fp32 rows of whole 16-byte pieces: y += delta by bulk reductions
+    ep.red = std::is_same<Ty, float>::value && g.H2 % 4 == 0 ? 1 : 0;
     // v once, B ring, two y stages per epilogue group: as deep as fits
     const size_t vb = (size_t)2 * g.r * 256, bstage = (size_t)g.r * N * 2;
     const size_t ystage = (size_t)kTcRows * tc_ypitch<Ty>();
@@ -778,9 +842,8 @@ int tc_launch_t(const TCArgs &g) {
     if (total() > kExpandSmemMax) ep.nbs = 2;
     if (total() > kExpandSmemMax) ep.ny = 1;
     const size_t expand_smem = total();
-    return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep,
-                  dim3((unsigned)((nblk + ep.nb - 1) / ep.nb), (unsigned)g.slots, 1), 1,
-                  expand_smem, g.stream, kExpandThreads);
+    return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep, dim3((unsigned)nct, 1, 1), 1, expand_smem,
+                  g.stream, kExpandThreads);
 }
 
 template <typename Tin>
