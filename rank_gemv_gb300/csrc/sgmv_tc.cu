@@ -8,12 +8,13 @@
 //
 // Shrink (sgmv_tc_shrink_kernel): one 128-row tile of a segment per cluster;
 //   the cluster's CL CTAs split H1.  Each CTA streams 64-column k-blocks
-//   through a 3-stage ring: X rows are gathered through perm with 16-byte
+//   through a 4-stage ring: X rows are gathered through perm with 16-byte
 //   cp.async writes into the 128-byte-swizzled K-major layout, A[a] k-blocks
 //   come by TMA (N-major, same swizzle).  One thread issues
 //   tcgen05.mma (M=128, N=r, K=16) into a TMEM accumulator; commits free the
 //   stages.  The partial v is read out of TMEM, pushed to the CTA that owns
-//   its rows through distributed shared memory, summed in rank order and
+//   its rows through distributed shared memory (into the ring's memory, once
+//   every CTA of the cluster has made its products), summed in rank order and
 //   written as two 16-bit halves, hi = round(v) and lo = round(v - hi), so
 //   the expand can run on 16-bit tensor cores and still see v to about
 //   16 significant bits.
@@ -49,16 +50,16 @@ namespace sgmv {
 constexpr int kTcThreads = 128;  // 4 warps: one TMEM lane (tile row) per thread
 constexpr int kTcRows = 128;     // M of one tile
 constexpr int kKB = 64;          // k-block: 64 16-bit elements = one 128-byte swizzle row
-constexpr int kStages = 3;       // shrink ring depth
+constexpr int kStages = 4;       // shrink ring depth
 constexpr int kShrinkProducers = 96;  // warps 1-3 of the shrink load its ring
 constexpr int kExpandThreads = 2 * kTcRows + 64;  // two epilogue groups, an MMA warp, a B warp
 constexpr int kExpandYStages = 2;  // most y stages per epilogue group
-constexpr int kExpandBStages = 3;  // most B stages
+constexpr int kExpandBStages = 8;  // most B stages
 // Fixed cost of one column block of the expand (its MMAs, barriers and
 // epilogue steps), in the y rows that take as long: part of a tile's weight
 // when the expand's CTAs are dealt to tiles.
 constexpr int kExpandBlockRows = 128;
-constexpr size_t kExpandSmemMax = 220u * 1024u;
+constexpr size_t kExpandSmemMax = 226u * 1024u;
 
 struct TCShrinkParams {
     CUtensorMap tmap_a;  // A as [L][H1][r], box {64, 64, 1}
@@ -80,7 +81,7 @@ struct TCExpandParams {
     int32_t kw;   // weight of a tile = its rows + kw (B bytes of a column block in y rows)
     int32_t red;  // fp32 y updated by bulk reductions in L2 (H2 % 4 == 0)
     int32_t ny;   // y stages per epilogue group (1 or 2)
-    int32_t nbs;  // B stages (2 or 3)
+    int32_t nbs;  // B stages (2 .. kExpandBStages)
     float scale;
 };
 
@@ -227,7 +228,6 @@ __global__ void __launch_bounds__(kTcThreads)
     if (s_info[0] < 0) return;  // same decision in every CTA of the cluster
     const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
     const bool clustered = ncl > 1;
-    if (clustered) cluster_arrive_relaxed();
     if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)rk);
 
     uint8_t *base = align1024(dsm);
@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(kTcThreads)
     const uint32_t a_bytes = kKB * rk * sizeof(Tin);       // 8 or 16 KB
     auto stage_x = [&](int st) { return base + st * (x_bytes + a_bytes); };
     auto stage_a = [&](int st) { return base + st * (x_bytes + a_bytes) + x_bytes; };
-    float *recv = reinterpret_cast<float *>(base + kStages * (x_bytes + a_bytes));
+    // partials of v from the cluster: in the ring's memory, once every CTA's
+    // products are made
+    float *recv = reinterpret_cast<float *>(base);
     const Tin *gX = static_cast<const Tin *>(xptr);
 
     const int k0 = (int)blockIdx.x * hk;
@@ -354,7 +356,9 @@ __global__ void __launch_bounds__(kTcThreads)
     // Partial v of this CTA's H1 slice -> the CTA that owns the row.
     const int rpc = kTcRows / ncl;  // rows summed by each CTA of the cluster
     const int rank = (int)blockIdx.x;
-    if (clustered) cluster_wait();
+    // every CTA of the cluster is done with its ring (and has started, so
+    // its shared memory can be written)
+    if (clustered) cluster_sync();
     for (int c0 = 0; c0 < rk; c0 += 32) {
         float v[32];
         if (nkb > 0) {
@@ -790,8 +794,8 @@ int tc_launch_t(const TCArgs &g) {
     sp.cl = cl;
     sp.min_len = g.min_len;
     sp.max_len = g.max_len;
-    const size_t shrink_smem = 1024 + (size_t)kStages * (kTcRows * kKB + kKB * g.r) * es +
-                               (size_t)kTcRows * g.r * 4;
+    const size_t shrink_smem =
+        1024 + std::max((size_t)kStages * (kTcRows * kKB + kKB * g.r) * es, (size_t)kTcRows * g.r * 4);
     int rc = launch(sgmv_tc_shrink_kernel<Tin>, sp, dim3((unsigned)cl, (unsigned)g.slots, 1), cl,
                     shrink_smem, g.stream);
     if (rc != 0) return rc;
@@ -839,8 +843,9 @@ int tc_launch_t(const TCArgs &g) {
     ep.nbs = kExpandBStages;
     ep.ny = kExpandYStages;
     auto total = [&]() { return 1024 + vb + ep.nbs * bstage + (size_t)2 * ep.ny * ystage; };
-    if (total() > kExpandSmemMax) ep.nbs = 2;
+    while (total() > kExpandSmemMax && ep.nbs > 2) --ep.nbs;
     if (total() > kExpandSmemMax) ep.ny = 1;
+    while (total() > kExpandSmemMax && ep.nbs > 2) --ep.nbs;
     const size_t expand_smem = total();
     return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep, dim3((unsigned)nct, 1, 1), 1, expand_smem,
                   g.stream, kExpandThreads);
