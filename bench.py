@@ -455,14 +455,32 @@ def distinct_vs_shared(args, dev, sgmv, wl):
             "method": f"median of {args.latency_iters}, L2 flushed (256 MB write) before each"}
 
 
+def _packed(tensors, device, pin=False):
+    """One byte buffer holding copies of `tensors` at 256-byte-aligned offsets,
+    and a view of each (so a step's inputs move in one copy)."""
+    import torch
+
+    offs, n = [], 0
+    for t in tensors:
+        n = (n + 255) // 256 * 256
+        offs.append(n)
+        n += t.nbytes
+    buf = torch.empty(n, dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [buf[o:o + t.nbytes].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    for v, t in zip(views, tensors):
+        v.copy_(t)
+    return buf, views
+
+
 def e2e(args, dev, sgmv, wl, world, seed, K, W):
     """The metric through the public API with host buffers, as a serving loop
     runs it: every step copies that step's inputs (rows, row -> adapter ids,
     y) from page-locked host memory, groups and applies, and copies y back;
-    the host waits for, and reads, each step's result.  Steps are pipelined
-    two deep: two sets of buffers, each step one CUDA-graph replay of those
-    copies and API calls, and the host waits for step s-2's result just
-    before step s reuses its buffers."""
+    the host waits for, and reads, each step's result.  Steps are pipelined:
+    D sets of buffers (D = 4, 2 for the stack), each step one CUDA-graph
+    replay of those copies and API calls, and the host waits for step s-D's
+    result just before step s reuses its buffers.  A single-projection step's
+    x, y and ids sit in one page-locked buffer and move in one copy."""
     import torch
 
     if args.workload == "llama7b-stack":
@@ -497,24 +515,23 @@ def e2e(args, dev, sgmv, wl, world, seed, K, W):
     else:
         w = wl.make(args.workload, seed)
         sets = []
-        for _ in range(2):
+        for _ in range(4):
             b = Batch(w, dev, sgmv)
-            sets.append((b, w.X.clone().pin_memory(), w.Y0.clone().pin_memory(),
-                         w.row_adapter.clone().pin_memory(), torch.empty_like(w.Y0).pin_memory()))
+            dbuf, (b.X, b.Y, b.ra) = _packed([w.X, w.Y0, w.row_adapter], dev)
+            hbuf, _ = _packed([w.X, w.Y0, w.row_adapter], "cpu", pin=True)
+            sets.append((b, dbuf, hbuf, torch.empty_like(w.Y0).pin_memory()))
 
         def make_step(st):
-            b, hx, hy, hra, hout = st
+            b, dbuf, hbuf, hout = st
 
             def one():
-                b.X.copy_(hx, non_blocking=True)
-                b.Y.copy_(hy, non_blocking=True)
-                b.ra.copy_(hra, non_blocking=True)
+                dbuf.copy_(hbuf, non_blocking=True)
                 b.step(sgmv)
                 hout.copy_(b.Y, non_blocking=True)
             return one, hout
 
-        b0, hx0, hy0, hra0, hout0 = sets[0]
-        h2d, d2h, T = hx0.nbytes + hy0.nbytes + hra0.nbytes, hout0.nbytes, w.T
+        _, _, hbuf0, hout0 = sets[0]
+        h2d, d2h, T = hbuf0.nbytes, hout0.nbytes, w.T
     steps = [make_step(st) for st in sets]
     for one, _ in steps:  # eager warm-up, then one graph per buffer set
         for _ in range(W):
@@ -525,16 +542,18 @@ def e2e(args, dev, sgmv, wl, world, seed, K, W):
     done = [torch.cuda.Event() for _ in steps]
     checksum = 0.0
 
+    D = len(steps)
+
     def run(n):
         nonlocal checksum
         for s_ in range(n):
-            i = s_ % 2
-            if s_ >= 2:
-                done[i].synchronize()                  # step s-2's result is on the host
+            i = s_ % D
+            if s_ >= D:
+                done[i].synchronize()                  # step s-D's result is on the host
                 checksum += float(outs[i].view(-1)[0])  # ... and read there
             graphs[i].replay()
             done[i].record()
-        for i in range(min(n, 2)):
+        for i in range(min(n, D)):
             done[i].synchronize()
             checksum += float(outs[i].view(-1)[0])
 
@@ -550,7 +569,7 @@ def e2e(args, dev, sgmv, wl, world, seed, K, W):
     el = max(e0.elapsed_time(e1) / 1e3, wall)
     return {"value": world * K * T / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3,
-            "pipelining": "2 steps in flight; host waits for and reads every step's result"}
+            "pipelining": f"{D} steps in flight; host waits for and reads every step's result"}
 
 
 # -------------------------------------------------- oracle (host cores)

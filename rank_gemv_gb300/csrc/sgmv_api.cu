@@ -177,10 +177,19 @@ constexpr uint32_t kStreamSmemMax = 200u * 1024u;
 // many CTAs per tile (8, 4, 2, 1) as keep CTAs x T within the SM count, each
 // with at least 64 columns of H1 and of H2.
 bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len, int32_t H1,
-                  int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l) {
+                  int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l,
+                  bool grouped) {
     if (r % 4 != 0 || r > 64 || T <= 0 || S <= 0) return false;
     const int64_t avg = ceil_div(T, S);
-    const int trows = avg <= 2 ? 1 : avg <= 4 ? 2 : avg <= 8 ? 4 : 8;
+    // The one-launch grouped form cannot see the segments.  Above 32 rows its
+    // clusters have at most two CTAs, each streaming large slices of a tile's
+    // adapter, and tiles of two rows halve that streaming for repeated
+    // adapters (measured on a Zipf batch of 64 rows: 9.1 against 10.3 us;
+    // all-distinct rows unchanged; taller tiles leave a few CTAs
+    // compute-bound).  Up to 32 rows, one-row tiles measured faster (one
+    // shared adapter, 32 rows: 4.0 against 4.4 us).  Tile height does not
+    // change any row's summation order.
+    const int trows = grouped && T > 32 ? 2 : avg <= 2 ? 1 : avg <= 4 ? 2 : avg <= 8 ? 4 : 8;
     const int64_t slots = tile_slots(T, S, seg_ptr_host, trows, 1, max_len);
     if (slots <= 0) return false;
     const int nsm = num_sms();
@@ -519,7 +528,7 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     p.err = err;
     StreamLaunch sl = {};
     if (slots > 0 &&
-        stream_shape(T, S, seg_ptr_host, cc_max_len, H1, H2, r, in_dtype, y_dtype, sl)) {
+        stream_shape(T, S, seg_ptr_host, cc_max_len, H1, H2, r, in_dtype, y_dtype, sl, false)) {
         StreamParams &q = sl.p;
         q.y = y;
         q.x = x;
@@ -618,7 +627,7 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
         int *err = error_word();
         if (!err) return SGMV_ERR_CUDA;
         StreamLaunch sl = {};
-        if (stream_shape(T, smax, nullptr, INT_MAX, H1, H2, r, in_dtype, y_dtype, sl)) {
+        if (stream_shape(T, smax, nullptr, INT_MAX, H1, H2, r, in_dtype, y_dtype, sl, true)) {
             StreamParams &q = sl.p;
             q.y = y;
             q.x = x;
