@@ -128,6 +128,26 @@ def test_ragged_dims(H1, H2):
     assert_close(y, ref, f"H1={H1} H2={H2}")
 
 
+@pytest.mark.parametrize("y_dtype", [torch.float32, torch.bfloat16])
+def test_more_tiles_than_sms(y_dtype):
+    """More 128-row tiles than SMs: the expand's grid is a multiple of the SM
+    count and its CTAs are dealt to tiles by weight; every (tile, column
+    block) must be updated exactly once, for full and ragged tiles alike."""
+    nsm = torch.cuda.get_device_properties(DEV).multi_processor_count
+    g = torch.Generator().manual_seed(11)
+    lens = []
+    while sum((n + 127) // 128 for n in lens) <= nsm + 40:
+        lens.append(int(torch.randint(129, 520, (1,), generator=g)))
+    L = len(lens)
+    ra = torch.arange(L, dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    w = wl.draw(int(sum(lens)), L, 128, 264, 64, ra, dtype=torch.bfloat16, y_dtype=y_dtype,
+                y0="randn", seed=12)
+    y = run(w)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y, ref, f"{sum((n + 127) // 128 for n in lens)} tiles, y {y_dtype}")
+
+
 def test_tensor_and_cuda_core_paths_agree():
     w = wl.make("prefill", 5, y0="randn")
     y_tc = run(w, ws=True)
