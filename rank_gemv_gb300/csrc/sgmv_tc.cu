@@ -9,7 +9,8 @@
 // Shrink (sgmv_tc_shrink_kernel): one 128-row tile of a segment per cluster;
 //   the cluster's CL CTAs split H1.  Each CTA streams 64-column k-blocks
 //   through a 4-stage ring: X rows are gathered through perm with 16-byte
-//   cp.async writes into the 128-byte-swizzled K-major layout, A[a] k-blocks
+//   cp.async writes (a warp reads four whole 128-byte row pieces per
+//   instruction) into the 128-byte-swizzled K-major layout, A[a] k-blocks
 //   come by TMA (N-major, same swizzle).  One thread issues
 //   tcgen05.mma (M=128, N=r, K=16) into a TMEM accumulator; commits free the
 //   stages.  The partial v is read out of TMEM, pushed to the CTA that owns
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kTcThreads)
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
     __shared__ int s_info[4];
+    __shared__ int s_xrow[kTcRows];  // physical row of each tile row, -1 past the tile
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
@@ -268,28 +270,21 @@ __global__ void __launch_bounds__(kTcThreads)
         }
         return row;
     };
-    const int row0 = prod >= 0 ? phys(prod) : -1;
-    const int m1 = prod + kShrinkProducers;
-    const int row1 = prod >= 0 && m1 < kTcRows ? phys(m1) : -1;
-    auto issue_x = [&](int kb) {  // every producer: the 8 chunks of its tile rows
+    if (tid < kTcRows) s_xrow[tid] = phys(tid);
+    __syncthreads();
+    // Every producer: (row, 16-byte chunk) pairs e = prod, prod + 96, ... of
+    // the 128 x 8 in a k-block, so that a warp reads 4 whole 128-byte row
+    // pieces per instruction.
+    auto issue_x = [&](int kb) {
         const int st = kb % kStages;
         uint8_t *xs = stage_x(st);
         const int kk0 = k0 + kb * kKB;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int e = prod; e < kTcRows * 8; e += kShrinkProducers) {
+            const int m = e >> 3, c = e & 7;
+            const int row = s_xrow[m];
             const int k = kk0 + c * 8;
-            const bool ok = row0 >= 0 && k < k1;
-            cp_async16(xs + sw128_offset(prod, c), ok ? gX + (size_t)row0 * H1 + k : gX,
-                       ok ? 16u : 0u);
-        }
-        if (m1 < kTcRows) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int k = kk0 + c * 8;
-                const bool ok = row1 >= 0 && k < k1;
-                cp_async16(xs + sw128_offset(m1, c), ok ? gX + (size_t)row1 * H1 + k : gX,
-                           ok ? 16u : 0u);
-            }
+            const bool ok = row >= 0 && k < k1;
+            cp_async16(xs + sw128_offset(m, c), ok ? gX + (size_t)row * H1 + k : gX, ok ? 16u : 0u);
         }
         cp_async_arrive(&full[st]);
     };
@@ -386,16 +381,29 @@ __global__ void __launch_bounds__(kTcThreads)
         __syncthreads();
     Tin *vhi = static_cast<Tin *>(vhi_ptr);
     Tin *vlo = static_cast<Tin *>(vlo_ptr);
-    for (int e = tid; e < rpc * rk; e += kTcThreads) {
-        const int mr = e / rk, col = e - (e / rk) * rk;
+    // four consecutive columns per thread, partials summed in rank order
+    const int rq = rk / 4;
+    for (int e = tid; e < rpc * rq; e += kTcThreads) {
+        const int mr = e / rq, col = 4 * (e - mr * rq);
         const int m = rank * rpc + mr;
         if (m >= nrows || lost) continue;
-        float s = 0.f;
-        for (int c = 0; c < ncl; ++c) s += ldsf(recv + (size_t)(c * rpc + mr) * rk + col);
-        const Tin hi = from_f<Tin>(s);
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < ncl; ++c) {
+            const uint4 u = lds128(recv + (size_t)(c * rpc + mr) * rk + col);
+            s[0] += __uint_as_float(u.x);
+            s[1] += __uint_as_float(u.y);
+            s[2] += __uint_as_float(u.z);
+            s[3] += __uint_as_float(u.w);
+        }
+        __align__(8) Tin hv[4], lv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            hv[q] = from_f<Tin>(s[q]);
+            lv[q] = from_f<Tin>(s[q] - to_f<Tin>(hv[q]));
+        }
         const size_t o = (size_t)(p0 + m) * rk + col;
-        vhi[o] = hi;
-        vlo[o] = from_f<Tin>(s - to_f<Tin>(hi));
+        *reinterpret_cast<uint2 *>(vhi + o) = *reinterpret_cast<const uint2 *>(hv);
+        *reinterpret_cast<uint2 *>(vlo + o) = *reinterpret_cast<const uint2 *>(lv);
     }
     tc_fence_before();
     __syncthreads();
