@@ -79,6 +79,31 @@ def test_decode_workloads(name, shuffle):
         assert torch.equal(y, y2)
 
 
+@pytest.mark.parametrize("T", [33, 47, 64])
+@pytest.mark.parametrize("r", [16, 36, 64])
+def test_grouped_batches_above_32_rows(T, r):
+    """One-launch batches above 32 rows are cut into two-row tiles: skewed ids
+    (some rows without an adapter), odd T and ranks that are not a multiple
+    of 16 must give the oracle's result, and the two-call form's bits."""
+    g = torch.Generator().manual_seed(100 * T + r)
+    L = 40
+    ra = wl.zipf_ids(g, T, L)
+    ra[torch.randperm(T, generator=g)[:3]] = -1
+    w = wl.draw(T, L, 1024, 1032, r, ra, dtype=torch.float16, y0="randn", seed=T + r)
+    y_one, out, launches = run_rows(w)
+    assert launches == 1
+    check_error_word(0)
+    check_meta(out, w)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y_one, ref, f"T={T} r={r}")
+    y_two = w.Y0.to(DEV).clone()
+    perm, seg_ptr, idx, _ = sg().sgmv_build_segments_device(w.row_adapter.to(DEV), w.L)
+    sg().sgmv_apply(y_two, w.X.to(DEV), w.A.to(DEV), w.B.to(DEV), seg_ptr, idx, w.scale,
+                    perm=perm)
+    check_error_word(0)
+    assert torch.equal(y_one, y_two)
+
+
 def test_same_bits_as_grouping_then_apply():
     w = wl.make("decode-zipf", 8, y0="randn", shuffle_rows=True)
     y_one, *_ = run_rows(w)
