@@ -101,6 +101,12 @@ class Oracle:
                                           _i32p, _i32p, _i32p, ctypes.c_int32,
                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32]
+        lib.oracle_fused_linear_lora.restype = ctypes.c_int
+        lib.oracle_fused_linear_lora.argtypes = [_f64p, _f64p, _f64p, _f64p, _f64p,
+                                                 ctypes.c_double, _i32p, _i32p, _i32p,
+                                                 ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32]
         self._lib = lib
         self.path = str(libpath)
 
@@ -198,6 +204,28 @@ class Oracle:
         return Y
 
 
+    def fused_linear_lora(self, X, W, A, B, seg_ptr, idx, scale, perm=None):
+        """float64 Y[T, H2] = X.W + scale * SGMV delta (the base output alone
+        on rows of no adapter); W is [H1, H2]."""
+        X, W, A, B = widen(X), widen(W), widen(A), widen(B)
+        T, H1 = X.shape
+        H1w, H2 = W.shape
+        L, H1a, r = A.shape
+        assert H1w == H1 and H1a == H1 and B.shape == (L, r, H2)
+        seg_ptr, idx, S, p = self._meta(seg_ptr, idx, perm, T)
+        if S and (idx.max() >= L or idx.min() < -1):
+            raise ValueError("adapter id outside [-1, L)")
+        Y = np.zeros((T, H2), np.float64)
+        rc = self._lib.oracle_fused_linear_lora(Y.ctypes.data_as(_f64p), X.ctypes.data_as(_f64p),
+                                                W.ctypes.data_as(_f64p), A.ctypes.data_as(_f64p),
+                                                B.ctypes.data_as(_f64p), float(scale),
+                                                _ptr_i32(p), _ptr_i32(seg_ptr), _ptr_i32(idx),
+                                                S, T, H1, H2, r)
+        if rc != 0:
+            raise MemoryError("oracle temporary allocation failed")
+        return Y
+
+
 _default: Oracle | None = None
 
 
@@ -222,3 +250,7 @@ def sgmv_expand(Y, v, B, seg_ptr, idx, scale, perm=None):
 
 def sgmv_apply(Y, X, A, B, seg_ptr, idx, scale, perm=None, *, widened=False):
     return default().sgmv_apply(Y, X, A, B, seg_ptr, idx, scale, perm, widened=widened)
+
+
+def fused_linear_lora(X, W, A, B, seg_ptr, idx, scale, perm=None):
+    return default().fused_linear_lora(X, W, A, B, seg_ptr, idx, scale, perm)

@@ -153,3 +153,32 @@ int oracle_sgmv_apply(double *Y, const double *X, const double *A,
     free(v);
     return 0;
 }
+
+/*
+ * Fused base linear + LoRA: the LoRA layer of [Article] §2.1, y = xW + xAB,
+ * in one call, as [Q&A] §3.2 ("Fused Kernel": the LoRA transform merged into
+ * the base model's linear layer) describes it:
+ *   Y[t][j] = sum_h X[t][h] * W[h][j]                          every row t,
+ *   then the SGMV update above for every segment with an adapter.
+ * W is [H1][H2] (x W, like x A and v B).  Y [T][H2] is overwritten: rows of
+ * no adapter hold the base output alone.  Returns 0, or 1 if the temporary
+ * of the update cannot be allocated.
+ */
+int oracle_fused_linear_lora(double *Y, const double *X, const double *W,
+                             const double *A, const double *B, double scale,
+                             const int32_t *perm, const int32_t *seg_ptr,
+                             const int32_t *idx, int32_t S, int32_t T,
+                             int32_t H1, int32_t H2, int32_t r)
+{
+    for (int32_t t = 0; t < T; ++t) {
+        const double *x = X + (size_t)t * H1;
+        double *y = Y + (size_t)t * H2;
+        for (int32_t j = 0; j < H2; ++j) {
+            double acc = 0.0;
+            for (int32_t h = 0; h < H1; ++h)
+                acc += x[h] * W[(size_t)h * H2 + j];
+            y[j] = acc;
+        }
+    }
+    return oracle_sgmv_apply(Y, X, A, B, scale, perm, seg_ptr, idx, S, T, H1, H2, r);
+}

@@ -274,3 +274,49 @@ def pin_grouping_invariants_large(o):
         pass
     else:
         raise AssertionError("id == L accepted")
+
+
+# -- fused base linear + LoRA (y = xW + xAB) ------------------------------------
+# "Punica: when LoRA fine-tuned models need multi-tenant serving", §2.1: the
+# LoRA layer is y = xW + xAB = x(W + AB), so a row on adapter a must equal x
+# times the merged weight W + scale * A[a] B[a] (numpy matmul), and a row of no
+# adapter x W alone.
+
+
+@pin
+def pin_fused_rows_equal_the_merged_weight(o):
+    rng = _rng(20)
+    T, L, H1, H2, r, scale = 23, 4, 24, 40, 5, 0.75
+    X, A, B, _ = _rand_problem(rng, T, L, H1, H2, r)
+    W = rng.standard_normal((H1, H2)) / np.sqrt(H1)
+    ra = rng.integers(-1, L, size=T).astype(np.int32)
+    perm, seg_ptr, idx = _group_with_numpy(ra)
+    Y = o.fused_linear_lora(X, W, A, B, seg_ptr, idx, scale, perm)
+    for t in range(T):
+        Wt = W if ra[t] < 0 else W + scale * (A[ra[t]] @ B[ra[t]])
+        assert np.allclose(Y[t], X[t] @ Wt, rtol=1e-12, atol=1e-12), t
+
+
+@pin
+def pin_fused_without_adapters_is_the_base_product(o):
+    rng = _rng(21)
+    T, L, H1, H2, r = 9, 2, 17, 12, 3
+    X, A, B, _ = _rand_problem(rng, T, L, H1, H2, r)
+    W = rng.standard_normal((H1, H2))
+    Y = o.fused_linear_lora(X, W, A, B, [0, T], [-1], 2.0)
+    assert np.allclose(Y, X @ W, rtol=1e-12, atol=1e-12)
+    # and rows outside every segment keep the base output too
+    Y2 = o.fused_linear_lora(X, W, A, B, [0, 4], [1], 2.0)
+    assert np.allclose(Y2[4:], X[4:] @ W, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Y2[:4], X[:4] @ (W + 2.0 * A[1] @ B[1]), rtol=1e-12, atol=1e-12)
+
+
+@pin
+def pin_fused_closed_form(o):
+    # all-ones inputs: every base output is H1, every LoRA delta scale * H1 * r
+    T, L, H1, H2, r, scale = 5, 3, 6, 7, 4, 0.5
+    X, W = np.ones((T, H1)), np.ones((H1, H2))
+    A, B = np.ones((L, H1, r)), np.ones((L, r, H2))
+    Y = o.fused_linear_lora(X, W, A, B, [0, 2, 5], [2, -1], scale)
+    assert np.array_equal(Y[:2], np.full((2, H2), H1 + scale * H1 * r))
+    assert np.array_equal(Y[2:], np.full((3, H2), float(H1)))

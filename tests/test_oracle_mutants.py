@@ -34,6 +34,11 @@ MUTANTS = {
     "grouping in descending id order": ("for (int32_t id = -1; id < L; ++id)",
                                         "for (int32_t id = L - 1; id >= -1; --id)"),
     "segment id off by one": ("idx[s] = id;", "idx[s] = id + 1;"),
+    "fused base dropped": ("y[j] = acc;", "y[j] = 0.0;"),
+    "fused W transposed": ("acc += x[h] * W[(size_t)h * H2 + j];",
+                           "acc += x[h] * W[(size_t)j * H1 + h];"),
+    "fused LoRA update dropped": ("return oracle_sgmv_apply(Y, X, A, B, scale, perm,",
+                                  "return 0 * oracle_sgmv_apply(Y, X, A, B, 0.0 * scale, perm,"),
 }
 
 
