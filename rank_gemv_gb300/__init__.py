@@ -13,8 +13,8 @@ __version__ = "0.1.0"
 _BINDING_NAMES = {
     "sgmv_status_string", "sgmv_max_segments", "sgmv_build_segments",
     "sgmv_build_segments_device", "sgmv_workspace_bytes", "sgmv_shrink", "sgmv_expand",
-    "sgmv_apply", "sgmv_apply_rows", "sgmv_apply_noalloc", "sgmv_get_device_error", "sgmv_last_launch_count", "SgmvError",
-    "load_library",
+    "sgmv_apply", "sgmv_apply_rows", "sgmv_apply_noalloc", "sgmv_load_adapter",
+    "sgmv_get_device_error", "sgmv_last_launch_count", "SgmvError", "load_library",
 }
 
 

@@ -39,6 +39,15 @@ def test_every_declared_function_is_exported(lib):
     assert sorted(sgmv.SIGNATURES) == names
 
 
+def test_package_exposes_every_binding_function(lib):
+    import rank_gemv_gb300
+
+    for n in declared_functions():
+        if n == "sgmv_last_error_string":
+            continue  # folded into SgmvError's message
+        assert callable(getattr(rank_gemv_gb300, n)), n
+
+
 def test_status_strings(lib):
     from rank_gemv_gb300 import sgmv
 
