@@ -4,18 +4,26 @@
 One step = one pass of the whole path over one batch through the C ABI:
 sgmv_apply_rows groups the batch's rows by adapter, gathers x, shrinks,
 expands and scatters into y (one kernel for decode batches; grouping kernel +
-CUDA-core + tensor-core kernels for prefill).  The llama7b-stack workload runs
-it for all 224 projections of one decode step.
+CUDA-core + tensor-core kernels for prefill).  The default workload,
+llama7b-stack, is one decode step of a Llama-2-7B LoRA stack: all 224
+projections (32 layers x q, k, v, o, gate, up, down), 128 rows on 128
+distinct adapters, ~11.2 GB of algorithmic traffic per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the fp64 oracle on the host cores
 
-Prints one JSON line (rank 0).  `value` is rows/s with inputs resident in HBM;
-inputs are rotated over enough copies that one pass over them exceeds twice
-the L2 cache, and the K timed steps run as CUDA-graph replays.  `e2e` is the
-same metric with each step's inputs copied from pinned host memory and its
-result read back.  With N > 1 (torchrun) every rank runs an independent
-replica: the path has no exchange step.
+Prints one JSON line (rank 0).  `value` is rows/s with inputs resident in HBM:
+inputs are rotated over enough copies that one pass touches more than twice
+the L2 cache, the K timed steps run as CUDA-graph replays, and the K-step
+region is timed `--repeats` times (each bracketed by a barrier and a device
+synchronisation); `value` comes from the median region.  `roofline` gives the
+update call's time back to back (the figure `frac` uses) and alone after an
+L2 flush.  `workloads` times the other named workloads the same way, with
+each decode workload's read-only floor.  `e2e` is the same metric through
+the public API with each step's inputs copied from pinned host memory and its
+result read back, called eagerly (and, for comparison, as graph replays).
+With N > 1 (torchrun) every rank runs an independent replica: the path has no
+exchange step.
 """
 from __future__ import annotations
 
@@ -34,32 +42,39 @@ if ROOT not in sys.path:
 METRIC = "SGMV shrink+expand rows/s and achieved HBM GB/s (% of GB300 roofline)"
 UNIT = "rows/s"
 FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = ["tiny", "decode-distinct", "decode-shared", "decode-zipf", "prefill", "llama7b-q",
+             "llama7b-stack"]
+# the other workloads timed beside the headline one (the small case the oracle
+# finishes in seconds, the two decode batches and their shared-adapter twin,
+# and prefill)
+SIDE_WORKLOADS = ["tiny", "decode-distinct", "decode-shared", "decode-zipf", "prefill"]
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--repeats", type=int, default=5,
+                   help="timed regions of --steps steps each; value from the median one")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode-distinct",
-                   choices=["tiny", "decode-distinct", "decode-shared", "decode-zipf", "prefill",
-                            "llama7b-q", "llama7b-stack"])
+    p.add_argument("--workload", default="llama7b-stack", choices=WORKLOADS)
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--cpu-seconds", type=float, default=10.0,
-                   help="host-core budget of the oracle baseline sample")
+    p.add_argument("--cpu-seconds", type=float, default=6.0,
+                   help="host-core budget of each oracle baseline sample (one thread, all cores)")
     p.add_argument("--soak-seconds", type=float, default=1.0,
                    help="load before the timed region while clocks are sampled")
-    p.add_argument("--latency-iters", type=int, default=50)
+    p.add_argument("--latency-iters", type=int, default=30,
+                   help="L2-flushed single calls per isolated timing (median)")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip e2e, cpu baseline and latency (for profiling runs)")
+                   help="skip the side workloads, e2e and the cpu baseline (profiling runs)")
     p.add_argument("--load", action="store_true",
                    help="on-demand adapter loading instead: one Llama-2-7B adapter (224 "
                         "projections) from pinned host memory, alone and during the stack's SGMV")
     p.add_argument("--figure", action="store_true",
                    help="the pages' micro-benchmark instead: latency of the base layer alone, "
                         "with a per-adapter loop and with SGMV, over batch sizes and adapter counts")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 # ---------------------------------------------------------------- helpers
@@ -78,6 +93,13 @@ def measured_peak():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
 
 
 # Sources of the C ABI's host-side argument checks and dispatch: they launch
@@ -117,11 +139,20 @@ def profiled_traffic(workload):
     return None
 
 
-def config_of(name, w, n_copies=None, l2_note=None):
+def config_of(name, w, l2_note=None):
     cfg = {"workload": name, "T": w.T, "L": w.L, "H1": w.H1, "H2": w.H2, "r": w.r,
            "inputs": str(w.dtype).replace("torch.", ""),
            "y": str(w.y_dtype).replace("torch.", ""),
            "segments": int(len(set(w.row_adapter.tolist()))), "parallelism": "replicas"}
+    if l2_note:
+        cfg["l2"] = l2_note
+    return cfg
+
+
+def stack_config(l2_note=None):
+    cfg = {"workload": "llama7b-stack", "T": 128, "L": 128, "r": 16, "layers": 32,
+           "projections": 7, "inputs": "float16", "y": "float16", "segments": 128,
+           "parallelism": "replicas"}
     if l2_note:
         cfg["l2"] = l2_note
     return cfg
@@ -184,6 +215,13 @@ def gpu_id_for(dev):
     return str(dev.index or 0)
 
 
+def rotation_copies(touched_bytes, l2_bytes, cap=256):
+    """Input copies to rotate over so that one pass touches more than twice the
+    L2 cache (at most `cap`; tiny batches then stay in L2, which the caller
+    states)."""
+    return int(min(cap, max(2, -(-2 * l2_bytes // max(1, touched_bytes)))))
+
+
 # ------------------------------------------------------- our implementation
 class Batch:
     """Device copy of one batch plus its metadata buffers."""
@@ -205,9 +243,6 @@ class Batch:
                      torch.empty(self.smax + 1, dtype=torch.int32, device=dev),
                      torch.empty(max(self.smax, 1), dtype=torch.int32, device=dev),
                      torch.empty(1, dtype=torch.int32, device=dev))
-
-    def group(self, sgmv):
-        sgmv.sgmv_build_segments_device(self.ra, self.w.L, out=self.meta)
 
     n_apply = 1  # update calls per step
 
@@ -252,9 +287,6 @@ class StackBatch:
                      torch.empty(self.smax, dtype=torch.int32, device=dev),
                      torch.empty(1, dtype=torch.int32, device=dev))
 
-    def group(self, sgmv):
-        sgmv.sgmv_build_segments_device(self.ra, self.L, out=self.meta)
-
     n_apply = 224
 
     def apply(self, sgmv):
@@ -274,19 +306,24 @@ class StackBatch:
     def step(self, sgmv):
         self.apply(sgmv)
 
+    def update_one(self, sgmv, i):
+        perm, seg_ptr, idx, _ = self.meta
+        X, A, B, Y = self.projs[i]
+        sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
+
     def update(self, sgmv):
         """All 224 update calls on the grouping of the last step (roofline)."""
-        perm, seg_ptr, idx, _ = self.meta
-        for X, A, B, Y in self.projs:
-            sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
+        for i in range(len(self.projs)):
+            self.update_one(sgmv, i)
+
+    @staticmethod
+    def proj_bytes(H1, H2, T=128, L=128, r=16):
+        return L * (H1 * r + r * H2) * 2 + T * H1 * 2 + 2 * T * H2 * 2
 
     def bytes_moved(self):
         from rank_gemv_gb300 import workloads as wl
 
-        tot = 0
-        for _, H1, H2 in wl.LLAMA7B_PROJ:
-            tot += self.L * (H1 * self.r + self.r * H2) * 2 + self.T * H1 * 2 + 2 * self.T * H2 * 2
-        return tot * wl.LLAMA7B_LAYERS
+        return sum(self.proj_bytes(H1, H2) for _, H1, H2 in wl.LLAMA7B_PROJ) * wl.LLAMA7B_LAYERS
 
 
 def capture(fns):
@@ -303,6 +340,9 @@ def capture(fns):
 
 
 def timed_replays(graph_full, n_per_graph, graph_rem, K):
+    """Seconds of K steps: K // n replays of the rotation graph and one of the
+    remainder graph, CUDA events on the replaying stream, synchronised on both
+    sides."""
     import torch
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -314,12 +354,56 @@ def timed_replays(graph_full, n_per_graph, graph_rem, K):
         graph_rem.replay()
     end.record()
     torch.cuda.synchronize()
-    return start.elapsed_time(end) / 1e3  # seconds
+    return start.elapsed_time(end) / 1e3
+
+
+def timed_regions(graph_full, n_per_graph, graph_rem, K, repeats, world):
+    """`repeats` timed regions of exactly K steps, each bracketed by a barrier
+    (N > 1) and a device synchronisation; returns their seconds."""
+    out = []
+    for _ in range(repeats):
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        out.append(timed_replays(graph_full, n_per_graph, graph_rem, K))
+    return out
+
+
+def isolated_us(fn, flush, iters):
+    """Median device time (us) of fn() alone: before each call a write larger
+    than L2 evicts its inputs, and CUDA events bracket the call."""
+    import torch
+
+    ts = []
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+def back_to_back_us(fns, calls, repeats=3):
+    """Per-call device time (us) of `calls` calls back to back: a graph of one
+    rotation over fns replayed; median of `repeats` timings."""
+    n = len(fns)
+    g = capture(fns)
+    reps = max(1, calls // n)
+    times = [timed_replays(g, 1, None, reps) for _ in range(repeats)]
+    return statistics.median(times) / (reps * n) * 1e6
+
+
+def hbm(bytes_, us, peak):
+    gbs = bytes_ / (us * 1e-6) / 1e9
+    return gbs, gbs / peak
 
 
 def run_ours(args, rank, world, local):
     import torch
-    import torch.distributed as dist
 
     from rank_gemv_gb300 import build as _build
     from rank_gemv_gb300 import sgmv
@@ -329,9 +413,11 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     _build.build()
     sgmv.load_library()
-    K, W = args.steps, max(3, args.warmup)
+    K, W, R = args.steps, max(3, args.warmup), max(1, args.repeats)
     seed = args.seed + rank
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+    peak, peak_kind = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     if args.workload == "llama7b-stack":
         stack = StackBatch(seed, dev, sgmv)
@@ -344,21 +430,22 @@ def run_ours(args, rank, world, local):
         w0 = wl.make(args.workload, seed)
         T = w0.T
         bytes_step = w0.bytes_moved()
-        per_copy = (w0.X.nbytes + w0.A.nbytes + w0.B.nbytes + 2 * w0.Y0.nbytes)
-        n_copies = max(2, -(-2 * l2 // per_copy))
+        n_copies = rotation_copies(bytes_step, l2)
         batches = [Batch(w0, dev, sgmv) for _ in range(n_copies)]
-        l2_note = (f"rotating {n_copies} input copies, {n_copies * per_copy / 1e6:.0f} MB per "
-                   f"rotation > 2 x L2 ({l2 / 1e6:.0f} MB)")
+        touched = n_copies * bytes_step
+        l2_note = (f"rotating {n_copies} input copies, {touched / 1e6:.0f} MB touched per "
+                   f"rotation" + (f" > 2 x L2 ({l2 / 1e6:.0f} MB)" if touched > 2 * l2
+                                  else f", inside L2 ({l2 / 1e6:.0f} MB)"))
 
     if world > 1:
+        import torch.distributed as dist
+
         dist.barrier()
 
     # warm-up (eager), then the graphs of one rotation and of the remainder
     for i in range(W):
         batches[i % len(batches)].step(sgmv)
-    # kernels per step, as reported by the library
-    launches_apply = batches[0].apply(sgmv)
-    launches_step = launches_apply
+    launches_step = batches[0].apply(sgmv)  # kernels per step, as the library reports them
     n_apply = batches[0].n_apply
     torch.cuda.synchronize()
     assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during warm-up"
@@ -371,30 +458,42 @@ def run_ours(args, rank, world, local):
     batches[0].update(sgmv)
     per_call = sgmv.sgmv_last_launch_count()
 
-    # soak under the clock sampler, then the timed steps
+    # soak under the clock sampler, then the timed regions
     sampler = ClockSampler(gpu_id_for(dev))
     t_end = time.perf_counter() + args.soak_seconds
     while time.perf_counter() < t_end:
         g_full.replay()
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed = timed_replays(g_full, n, g_rem, K)
+    regions = timed_regions(g_full, n, g_rem, K, R, world)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    kernel_s = timed_replays(k_full, n, k_rem, K)
+    kregions = timed_regions(k_full, n, k_rem, K, R, 1)
     assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during timing"
 
-    elapsed, kernel_s = max_over_ranks([elapsed, kernel_s], world, dev)
+    elapsed, kernel_s = max_over_ranks([statistics.median(regions), statistics.median(kregions)],
+                                       world, dev)
     value = replica_throughput(world, K, T, elapsed)
-    peak, peak_kind = measured_peak()
-    # roofline of one update call (the streaming kernel for decode batches;
-    # streaming + tensor-core shrink + expand for prefill), timed alone in a
-    # graph of K steps' worth of calls
-    apply_s = kernel_s / (K * n_apply)
+    # roofline of one update call, back to back (as a decode step runs its
+    # calls) and alone after an L2 flush
+    apply_us = kernel_s / (K * n_apply) * 1e6
     bytes_apply = bytes_step / n_apply
-    achieved = bytes_apply / apply_s / 1e9
+    achieved, frac = hbm(bytes_apply, apply_us, peak)
+    if args.workload == "llama7b-stack":
+        iso = {}
+        for name, i in (("q", 0), ("gate", 4), ("down", 6)):
+            _, H1, H2 = wl.LLAMA7B_PROJ[i]
+            us = isolated_us(lambda i=i: stack.update_one(sgmv, i), flush, args.latency_iters)
+            iso[name] = {"us": us, "bytes": StackBatch.proj_bytes(H1, H2),
+                         "frac": hbm(StackBatch.proj_bytes(H1, H2), us, peak)[1]}
+        # a layer has four q-shaped, two gate-shaped and one down-shaped call
+        iso_us = (4 * iso["q"]["us"] + 2 * iso["gate"]["us"] + iso["down"]["us"]) / 7
+        iso_note = "per projection shape (layer 0), L2 flushed before each; mean over a layer's 7 calls"
+    else:
+        iso = None
+        iso_us = isolated_us(lambda: batches[0].update(sgmv), flush, args.latency_iters)
+        iso_note = "L2 flushed before each call"
+    iso_gbs, iso_frac = hbm(bytes_apply, iso_us, peak)
     if args.workload == "prefill":
         kname = "sgmv_tc_shrink_kernel + sgmv_tc_expand_kernel (tensor cores; the streaming kernel gets no short segment)"
     elif w0 is not None and w0.T <= 64:
@@ -405,22 +504,38 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(args.workload, w0, l2_note=l2_note) if w0 is not None else {
-            "workload": "llama7b-stack", "T": T, "L": 128, "r": 16, "layers": 32,
-            "projections": 7, "inputs": "float16", "y": "float16", "segments": 128,
-            "parallelism": "replicas", "l2": l2_note},
+        "config": config_of(args.workload, w0, l2_note) if w0 is not None else stack_config(l2_note),
+        "repeats": {"n": R, "ms_per_step": [t / K * 1e3 for t in regions],
+                    "value_from": "median region"},
         "hbm_gbs": bytes_step * K / elapsed / 1e9,
         "bytes_per_step": bytes_step,
         "roofline": {"bound": "hbm", "kernel": kname, "kernels_per_call": per_call,
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": profiled_traffic(args.workload), "source_hash": source_hash(),
-                     "bytes_per_call": bytes_apply, "call_us": apply_s * 1e6},
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": frac,
+                     "peak_kind": peak_kind, "traffic": profiled_traffic(args.workload),
+                     "source_hash": source_hash(), "bytes_per_call": bytes_apply,
+                     "call_us": apply_us,
+                     "frac_uses": f"call_us: {n_apply * K} update calls back to back in CUDA "
+                                  f"graphs, median of {R} regions",
+                     "isolated": {"call_us": iso_us, "achieved": iso_gbs, "frac": iso_frac,
+                                  "method": f"median of {args.latency_iters}; {iso_note}",
+                                  **({"by_shape": iso} if iso else {})}},
         "gpu_launches": K * launches_step,
         "clocks": clocks,
     }
-    if args.workload == "decode-distinct" and not args.no_extras:
-        out["latency_us"] = distinct_vs_shared(args, dev, sgmv, wl)
+    if not args.no_extras and rank == 0:
+        del g_full, g_rem, k_full, k_rem
+        torch.cuda.synchronize()
+        side = {}
+        for name in SIDE_WORKLOADS:
+            if name != args.workload:
+                side[name] = measure_workload(name, args, dev, sgmv, wl, l2, peak, flush)
+        if "decode-distinct" in side and "decode-shared" in side:
+            d, s = side["decode-distinct"], side["decode-shared"]
+            side["distinct_vs_shared"] = {
+                "isolated_step_ratio": d["isolated"]["step_us"] / s["isolated"]["step_us"],
+                "back_to_back_step_ratio": d["back_to_back"]["step_us"] / s["back_to_back"]["step_us"],
+                "target": 1.3}
+        out["workloads"] = side
     if not args.no_extras:
         out["e2e"] = e2e(args, dev, sgmv, wl, world, seed, K, W)
     if rank == 0 and world == 1 and not args.no_extras:
@@ -429,30 +544,57 @@ def run_ours(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
-def distinct_vs_shared(args, dev, sgmv, wl):
-    """Median latency of one step with L2 flushed before it, for the batch of
-    32 distinct adapters and for the same batch on one shared adapter."""
+def measure_workload(name, args, dev, sgmv, wl, l2, peak, flush):
+    """One named workload beside the headline: the update call (and the whole
+    step, grouping included) back to back over rotating input copies and alone
+    after an L2 flush; for decode batches (up to 64 rows) also the read-only
+    floor of the same bytes with the streaming kernel's launch shape."""
     import torch
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    res = {}
-    for name in ("decode-distinct", "decode-shared"):
-        b = Batch(wl.make(name, args.seed), dev, sgmv)
-        for _ in range(5):
-            b.step(sgmv)
-        ts = []
-        for i in range(args.latency_iters):
-            flush.fill_(i & 0xFF)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            b.step(sgmv)
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e3)
-        res[name] = statistics.median(ts)
-    return {"distinct": res["decode-distinct"], "shared": res["decode-shared"],
-            "ratio": res["decode-distinct"] / res["decode-shared"],
-            "method": f"median of {args.latency_iters}, L2 flushed (256 MB write) before each"}
+    w = wl.make(name, args.seed)
+    nbytes = w.bytes_moved()
+    n_copies = rotation_copies(nbytes, l2)
+    batches = [Batch(w, dev, sgmv) for _ in range(n_copies)]
+    for b in batches:
+        b.step(sgmv)
+    torch.cuda.synchronize()
+    assert sgmv.sgmv_get_device_error(dev) == 0, f"device error word set on {name}"
+    calls = max(4 * n_copies, 200)
+    res = {"T": w.T, "bytes_per_call": nbytes,
+           "inputs": f"{n_copies} rotating copies, {n_copies * nbytes / 1e6:.0f} MB touched per "
+                     "rotation" + (" (> 2 x L2)" if n_copies * nbytes > 2 * l2 else " (inside L2)")}
+    b2b_call = back_to_back_us([(lambda b=b: b.update(sgmv)) for b in batches], calls)
+    b2b_step = back_to_back_us([(lambda b=b: b.step(sgmv)) for b in batches], calls)
+    iso_call = isolated_us(lambda: batches[0].update(sgmv), flush, args.latency_iters)
+    iso_step = isolated_us(lambda: batches[0].step(sgmv), flush, args.latency_iters)
+    g1, f1 = hbm(nbytes, b2b_call, peak)
+    g2, f2 = hbm(nbytes, iso_call, peak)
+    res["back_to_back"] = {"call_us": b2b_call, "gbs": g1, "frac": f1, "step_us": b2b_step,
+                           "rows_per_s": w.T / (b2b_step * 1e-6)}
+    res["isolated"] = {"call_us": iso_call, "gbs": g2, "frac": f2, "step_us": iso_step}
+    if w.T <= 64 and w.r % 4 == 0 and w.r <= 64:
+        nb = (nbytes + 15) // 16 * 16
+        src = torch.zeros(n_copies * nb // 4, dtype=torch.int32, device=dev)
+        srcs = [src[i * nb // 4:(i + 1) * nb // 4] for i in range(n_copies)]
+        shape = {}
+
+        def floor(s):
+            shape["grid"] = sgmv.sgmv_read_floor(s, nb, w.T, w.L, w.H1, w.H2, w.r, w.dtype,
+                                                 w.y_dtype)
+        floor(srcs[0])
+        fb = back_to_back_us([(lambda s=s: floor(s)) for s in srcs], calls)
+        fi = isolated_us(lambda: floor(srcs[0]), flush, args.latency_iters)
+        res["floor"] = {"ctas": shape["grid"][0], "cluster": shape["grid"][1],
+                        "back_to_back_us": fb, "isolated_us": fi,
+                        "frac_back_to_back": hbm(nb, fb, peak)[1],
+                        "frac_isolated": hbm(nb, fi, peak)[1],
+                        "call_over_floor_back_to_back": b2b_call / fb,
+                        "call_over_floor_isolated": iso_call / fi}
+        del src, srcs
+    assert sgmv.sgmv_get_device_error(dev) == 0, f"device error word set on {name}"
+    del batches
+    torch.cuda.empty_cache()
+    return res
 
 
 def _packed(tensors, device, pin=False):
@@ -477,10 +619,15 @@ def e2e(args, dev, sgmv, wl, world, seed, K, W):
     runs it: every step copies that step's inputs (rows, row -> adapter ids,
     y) from page-locked host memory, groups and applies, and copies y back;
     the host waits for, and reads, each step's result.  Steps are pipelined:
-    D sets of buffers (D = 4, 2 for the stack), each step one CUDA-graph
-    replay of those copies and API calls, and the host waits for step s-D's
-    result just before step s reuses its buffers.  A single-projection step's
-    x, y and ids sit in one page-locked buffer and move in one copy."""
+    D sets of buffers (D = 4, 2 for the stack), and the host waits for step
+    s-D's result just before step s reuses its buffers.  Each step is issued
+    eagerly through the Python binding (`value`: argument checks, tensor-map
+    encoding and launches inside the loop), and, for comparison, as one
+    CUDA-graph replay of the same copies and calls (`graphed`).  A
+    single-projection step's x, y and ids sit in one page-locked buffer and
+    move in one copy.  `breakdown_us` times the parts alone: the copies in
+    and out (device time), the step's kernels (device time), and the host
+    time of issuing the step's API calls."""
     import torch
 
     if args.workload == "llama7b-stack":
@@ -494,22 +641,23 @@ def e2e(args, dev, sgmv, wl, world, seed, K, W):
             hra = stack.ra.cpu().pin_memory()
             sets.append((stack, hx, hy, hout, hra))
 
-        def make_step(st):
+        def parts(st):
             stack, hx, hy, hout, hra = st
 
-            def one():
+            def h2d():
                 stack.ra.copy_(hra, non_blocking=True)
                 for (X, _, _, Y), a, b in zip(stack.projs, hx, hy):
                     X.copy_(a, non_blocking=True)
                     Y.copy_(b, non_blocking=True)
-                stack.step(sgmv)
+
+            def d2h():
                 for (_, _, _, Y), o in zip(stack.projs, hout):
                     o.copy_(Y, non_blocking=True)
-            return one, hout[0]
+            return h2d, (lambda: stack.step(sgmv)), d2h, hout[0]
 
         stack0, hx0, hy0, hout0, hra0 = sets[0]
-        h2d = sum(h.nbytes for h in hx0) + sum(h.nbytes for h in hy0) + hra0.nbytes
-        d2h = sum(h.nbytes for h in hout0)
+        h2d_b = sum(h.nbytes for h in hx0) + sum(h.nbytes for h in hy0) + hra0.nbytes
+        d2h_b = sum(h.nbytes for h in hout0)
         T = stack0.T
         K = min(K, 20)
     else:
@@ -521,95 +669,192 @@ def e2e(args, dev, sgmv, wl, world, seed, K, W):
             hbuf, _ = _packed([w.X, w.Y0, w.row_adapter], "cpu", pin=True)
             sets.append((b, dbuf, hbuf, torch.empty_like(w.Y0).pin_memory()))
 
-        def make_step(st):
+        def parts(st):
             b, dbuf, hbuf, hout = st
-
-            def one():
-                dbuf.copy_(hbuf, non_blocking=True)
-                b.step(sgmv)
-                hout.copy_(b.Y, non_blocking=True)
-            return one, hout
+            return ((lambda: dbuf.copy_(hbuf, non_blocking=True)), (lambda: b.step(sgmv)),
+                    (lambda: hout.copy_(b.Y, non_blocking=True)), hout)
 
         _, _, hbuf0, hout0 = sets[0]
-        h2d, d2h, T = hbuf0.nbytes, hout0.nbytes, w.T
-    steps = [make_step(st) for st in sets]
-    for one, _ in steps:  # eager warm-up, then one graph per buffer set
+        h2d_b, d2h_b, T = hbuf0.nbytes, hout0.nbytes, w.T
+    steps = []
+    for st in sets:
+        h2d, kern, d2h, out = parts(st)
+
+        def one(h2d=h2d, kern=kern, d2h=d2h):
+            h2d()
+            kern()
+            d2h()
+        steps.append((one, out, h2d, kern, d2h))
+    for one, *_ in steps:  # eager warm-up
         for _ in range(W):
             one()
     torch.cuda.synchronize()
-    graphs = [capture([one]) for one, _ in steps]
-    outs = [out for _, out in steps]
+    graphs = [capture([one]) for one, *_ in steps]
+    outs = [s[1] for s in steps]
     done = [torch.cuda.Event() for _ in steps]
     checksum = 0.0
-
     D = len(steps)
 
-    def run(n):
+    def run(n, graphed):
         nonlocal checksum
         for s_ in range(n):
             i = s_ % D
             if s_ >= D:
                 done[i].synchronize()                  # step s-D's result is on the host
                 checksum += float(outs[i].view(-1)[0])  # ... and read there
-            graphs[i].replay()
+            if graphed:
+                graphs[i].replay()
+            else:
+                steps[i][0]()
             done[i].record()
         for i in range(min(n, D)):
             done[i].synchronize()
             checksum += float(outs[i].view(-1)[0])
 
-    run(W)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.perf_counter()
-    e0.record()
-    run(K)
-    e1.record()
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    el = max(e0.elapsed_time(e1) / 1e3, wall)
-    return {"value": world * K * T / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3,
-            "pipelining": f"{D} steps in flight; host waits for and reads every step's result"}
+    def timed(graphed):
+        run(W, graphed)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record()
+        run(K, graphed)
+        e1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        return max(e0.elapsed_time(e1) / 1e3, wall)
+
+    el = timed(False)
+    el_g = timed(True)
+    assert sgmv.sgmv_get_device_error(dev) == 0, "device error word set during e2e"
+
+    # the parts alone
+    _, _, h2d, kern, d2h = steps[0]
+
+    def dev_us(fn, iters=10):
+        ts = []
+        for _ in range(iters):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    def host_us(fn, iters=10):
+        ts = []
+        for _ in range(iters):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t0) * 1e6)
+            torch.cuda.synchronize()
+        return statistics.median(ts)
+
+    breakdown = {"h2d_us": dev_us(h2d), "d2h_us": dev_us(d2h), "kernels_us": dev_us(kern),
+                 "api_host_us": host_us(kern),
+                 "h2d_gbs": h2d_b / (dev_us(h2d) * 1e3), "d2h_gbs": d2h_b / (dev_us(d2h) * 1e3)}
+    return {"value": world * K * T / el, "unit": UNIT, "h2d_bytes_per_step": h2d_b,
+            "d2h_bytes_per_step": d2h_b, "steps": K, "ms_per_step": el / K * 1e3,
+            "method": "eager API calls each step (Python binding -> C ABI), copies from/to "
+                      f"page-locked host memory, {D} steps in flight; host waits for and reads "
+                      "every step's result",
+            "graphed": {"value": world * K * T / el_g, "ms_per_step": el_g / K * 1e3,
+                        "method": "the same step as one CUDA-graph replay (API calls "
+                                  "captured once, so host-side checks and launches are not "
+                                  "in the loop)"},
+            "breakdown_us": breakdown}
 
 
 # -------------------------------------------------- oracle (host cores)
+def oracle_tasks(perm, seg_ptr, idx, n_tasks):
+    """Split the sorted positions of a grouped batch into about n_tasks ranges
+    of consecutive positions; each task is (rows, seg_ptr, idx) of an
+    independent SGMV problem on those rows (the segments clipped to the
+    range, positions re-based to 0)."""
+    import numpy as np
+
+    total = int(seg_ptr[-1]) if len(seg_ptr) else 0
+    n_tasks = max(1, min(n_tasks, total))
+    cuts = [round(i * total / n_tasks) for i in range(n_tasks + 1)]
+    tasks = []
+    for p0, p1 in zip(cuts[:-1], cuts[1:]):
+        if p1 <= p0:
+            continue
+        sp, ix = [0], []
+        for s in range(len(idx)):
+            a, b = max(int(seg_ptr[s]), p0), min(int(seg_ptr[s + 1]), p1)
+            if a < b:
+                ix.append(int(idx[s]))
+                sp.append(sp[-1] + b - a)
+        tasks.append((np.asarray(perm[p0:p1], dtype=np.int64), np.asarray(sp, np.int32),
+                      np.asarray(ix, np.int32)))
+    return tasks
+
+
+def oracle_apply_parallel(o, pool, Y, X, A, B, perm, seg_ptr, idx, scale, n_tasks):
+    """The oracle's SGMV update of a grouped batch, as independent oracle calls
+    on ranges of its rows run by the threads of `pool` (the C code releases
+    the interpreter lock).  Every output element is computed by the same
+    oracle arithmetic as in one call, so the result is identical to
+    o.sgmv_apply(Y, X, A, B, seg_ptr, idx, scale, perm=perm)."""
+    out = Y.copy()
+
+    def one(task):
+        rows, sp, ix = task
+        out[rows] = o.sgmv_apply(Y[rows], X[rows], A, B, sp, ix, scale, widened=True)
+
+    list(pool.map(one, oracle_tasks(perm, seg_ptr, idx, n_tasks)))
+    return out
+
+
 def _oracle_sample(name, seed):
-    """(step function, rows per step, rows/s scale, sample description) for the
-    oracle on a bounded sample of the workload."""
+    """(problems, metric rows per pass, description) of a bounded sample of the
+    workload for the oracle; a problem is (Y, X, A, B, row_adapter, L, scale)
+    widened to float64."""
     import oracle
     from rank_gemv_gb300 import workloads as wl
 
     if name == "llama7b-stack":
-        rows = 16
-        projs = [wl.stack_projection(seed, 0, p) for p in range(len(wl.LLAMA7B_PROJ))]
-        ra = wl.stack_row_adapter(128)[:rows]
-        widened = [tuple(oracle.widen(t[:rows] if i in (0, 3) else t) for i, t in enumerate(pr))
-                   for pr in projs]
-
-        def step():
-            perm, seg_ptr, idx = oracle.build_segments(ra, 128)
-            for X, A, B, Y in widened:
-                oracle.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, widened=True)
-
-        # one layer of 7 projections stands for 1/32 of a pass
-        return step, rows / 32.0, f"{rows} of 128 rows, layer 0 (7 of 224 projections)"
+        problems = []
+        for p in range(len(wl.LLAMA7B_PROJ)):
+            X, A, B, Y = wl.stack_projection(seed, 0, p)
+            problems.append((oracle.widen(Y), oracle.widen(X), oracle.widen(A), oracle.widen(B),
+                             wl.stack_row_adapter(128), 128, 1.0))
+        # one layer of 7 projections on all 128 rows stands for 1/32 of a pass
+        return problems, 128 / 32.0, "all 128 rows of layer 0 (7 of 224 projections = 1/32 of a step)"
     w = wl.make(name, seed)
     per_row = w.H1 * w.r + w.r * w.H2
-    rows = int(max(1, min(w.T, 20e6 // per_row)))
-    X, A, B, Y = (oracle.widen(w.X[:rows]), oracle.widen(w.A), oracle.widen(w.B),
-                  oracle.widen(w.Y0[:rows]))
-    ra = w.row_adapter[:rows]
+    rows = int(max(1, min(w.T, 4e8 // per_row)))
+    problems = [(oracle.widen(w.Y0[:rows]), oracle.widen(w.X[:rows]), oracle.widen(w.A),
+                 oracle.widen(w.B), w.row_adapter[:rows], w.L, w.scale)]
+    desc = "whole batch" if rows == w.T else f"first {rows} of {w.T} rows"
+    return problems, float(rows), desc
+
+
+def oracle_step(problems, threads):
+    """One oracle pass (grouping + fp64 update of every problem) on `threads`
+    host threads; returns the step function and a closer for its pool."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    o = oracle.default()
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
 
     def step():
-        perm, seg_ptr, idx = oracle.build_segments(ra, w.L)
-        oracle.sgmv_apply(Y, X, A, B, seg_ptr, idx, w.scale, perm=perm, widened=True)
+        for Y, X, A, B, ra, L, scale in problems:
+            perm, seg_ptr, idx = o.build_segments(ra, L)
+            if pool is None:
+                o.sgmv_apply(Y, X, A, B, seg_ptr, idx, scale, perm=perm, widened=True)
+            else:
+                oracle_apply_parallel(o, pool, Y, X, A, B, perm, seg_ptr, idx, scale,
+                                      4 * threads)
 
-    desc = "whole batch" if rows == w.T else f"first {rows} of {w.T} rows"
-    return step, float(rows), desc
+    return step, (pool.shutdown if pool is not None else (lambda: None))
 
 
-def cpu_baseline(args, budget_s):
-    step, rows, desc = _oracle_sample(args.workload, args.seed)
+def _time_passes(step, budget_s):
     step()
     n, t0 = 0, time.perf_counter()
     while True:
@@ -617,10 +862,29 @@ def cpu_baseline(args, budget_s):
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
-            break
-    return {"value": n * rows / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{desc}; {n} oracle passes (grouping + fp64 apply, one thread) "
-                      f"in {el:.1f} s"}
+            return n, el
+
+
+def cpu_baseline(args, budget_s):
+    """The oracle on the host cores: all cores (`value`, `cores` = threads
+    used) and one thread, each for about budget_s seconds."""
+    problems, rows, desc = _oracle_sample(args.workload, args.seed)
+    nthr = host_threads()
+    res = {}
+    for threads in (nthr, 1):
+        step, close = oracle_step(problems, threads)
+        try:
+            n, el = _time_passes(step, budget_s)
+        finally:
+            close()
+        res[threads] = (n * rows / el, n, el)
+    v, n, el = res[nthr]
+    v1, n1, el1 = res[1]
+    return {"value": v, "unit": UNIT, "cores": nthr, "kind": "oracle",
+            "sample": f"{desc}; {n} oracle passes (grouping + fp64 update, {nthr} threads over "
+                      f"ranges of rows) in {el:.1f} s",
+            "single_core": {"value": v1, "cores": 1,
+                            "sample": f"{n1} passes on one thread in {el1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
@@ -628,24 +892,30 @@ def run_reference(args, rank, world):
         return
     from rank_gemv_gb300 import workloads as wl
 
-    step, rows, desc = _oracle_sample(args.workload, args.seed)
-    W = max(3, args.warmup)
-    for _ in range(W):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    el = time.perf_counter() - t0
+    problems, rows, desc = _oracle_sample(args.workload, args.seed)
+    nthr = host_threads()
+    step, close = oracle_step(problems, nthr)
+    try:
+        W = max(3, args.warmup)
+        for _ in range(W):
+            step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        el = time.perf_counter() - t0
+    finally:
+        close()
     value = args.steps * rows / el
     w = None if args.workload == "llama7b-stack" else wl.make(args.workload, args.seed)
-    cfg = config_of(args.workload, w) if w is not None else {"workload": "llama7b-stack"}
-    sample = f"{desc}; one oracle pass (grouping + fp64 apply, one thread) per step"
+    cfg = config_of(args.workload, w) if w is not None else stack_config()
+    sample = (f"{desc}; one oracle pass (grouping + fp64 update, {nthr} threads over ranges of "
+              "rows) per step")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": W, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": cfg,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthr, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)

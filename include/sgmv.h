@@ -58,7 +58,11 @@
  * Ownership and execution: the caller owns every buffer; the library never
  * allocates device memory.  Calls are asynchronous on `stream` (a
  * cudaStream_t, NULL = legacy default stream), take no locks and keep no
- * state except the device error word.  Kernels are launched with
+ * state except the device error word.  The device addresses of the library's
+ * own device variables (the error word, the scratch of sgmv_apply_noalloc)
+ * are looked up once per device and kept: after cudaDeviceReset, or any other
+ * teardown of a device's primary context, the library must not be used again
+ * on that device in the same process.  Kernels are launched with
  * programmatic dependent launch: a kernel may start while the previous
  * kernel on the stream finishes, and before it waits for that kernel it
  * reads only A, B, row_adapter and the segment metadata.  So those inputs must
@@ -216,13 +220,16 @@ int sgmv_apply_rows(void *y, int y_dtype, const void *x, const void *A, const vo
  * Arguments and results are those of sgmv_apply, without the workspace: the
  * scratch for the tensor-core path is a fixed 4 MiB array inside the
  * library's device image, held by every GPU that loads the library until the
- * process exits.  Problems whose sgmv_workspace_bytes(T, H1, H2, r) exceeds
- * 4 MiB are refused with SGMV_ERR_WORKSPACE before anything is launched.
- * The first call on a device looks the array's device address up
- * (cudaGetSymbolAddress, no allocation); make that first call before any
- * stream capture.  All calls share the one array and it keeps the last call's
- * contents (nothing in it has to start at zero), so calls that overlap on the
- * GPU -- on different streams, or from different threads -- race on it.
+ * process exits.  Only problems that can reach the tensor-core path (r = 64
+ * or 128 and T >= 64) use it; those whose sgmv_workspace_bytes(T, H1, H2, r)
+ * exceeds 4 MiB are refused with SGMV_ERR_WORKSPACE before anything is
+ * launched.  Every other problem runs on the CUDA cores without scratch,
+ * whatever its size.  The first such call on a device looks the array's
+ * device address up (cudaGetSymbolAddress, no allocation); make that first
+ * call before any stream capture.  All calls share the one array and it keeps
+ * the last call's contents (nothing in it has to start at zero), so calls
+ * that overlap on the GPU -- on different streams, or from different threads
+ * -- race on it.
  */
 int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const void *B,
                        int in_dtype, float scale, const int32_t *perm, const int32_t *seg_ptr,
@@ -249,6 +256,36 @@ int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const
 int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, const void *A_src,
                       const void *B_src, int32_t L, int32_t H1, int32_t H2, int32_t r,
                       void *stream);
+
+/*
+ * Diagnostics (no counterpart on the pages).
+ *
+ * sgmv_read_floor: the floor of a decode-sized SGMV launch on this GPU.  Reads
+ * `bytes` (a multiple of 16) of device memory at `src` (16-byte aligned) and
+ * nothing else, spread evenly over the grid, cluster size, ring depth and
+ * copy size that the streaming kernel gets from sgmv_apply_rows for a batch
+ * of T rows over L adapters with these dimensions, types and rank (the
+ * one-launch grouped form up to 64 rows; sgmv_apply on the device grouping
+ * otherwise).  Pass the batch's algorithmic bytes to time what merely
+ * bringing them on chip costs with that launch shape.  *ctas and *cluster
+ * (each may be NULL) receive the grid's CTA count and cluster size.
+ * SGMV_ERR_UNSUPPORTED when the streaming kernel does not apply (r not a
+ * multiple of 4, or above 64).  Asynchronous on `stream`; writes nothing.
+ */
+int sgmv_read_floor(const void *src, size_t bytes, int32_t T, int32_t L, int32_t H1, int32_t H2,
+                    int32_t r, int in_dtype, int y_dtype, int32_t *ctas, int32_t *cluster,
+                    void *stream);
+
+/*
+ * sgmv_debug_inject_wait_timeout: for tests of the device-side timeout path.
+ * While enabled (non-zero) on the calling thread, every streaming-kernel
+ * launch it makes takes the timeout path at each compute thread's first wait
+ * for a staged chunk, as if that wait had run out: SGMV_ERR_TIMEOUT is set in
+ * the device error word, the chunk is then awaited with the full limit (so
+ * the kernel still ends normally, with every copy landed) and the thread
+ * writes no y.  Other kernels are unaffected.  Returns SGMV_OK.
+ */
+int sgmv_debug_inject_wait_timeout(int enable);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's sticky

@@ -19,6 +19,7 @@ using namespace sgmv;
 
 thread_local char g_last_error[256] = "";
 thread_local int g_launches = 0;  // kernels launched by this thread's last call
+thread_local int g_inject_timeout = 0;  // sgmv_debug_inject_wait_timeout
 
 void note(const char *what, cudaError_t e) {
     snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, cudaGetErrorString(e));
@@ -140,6 +141,7 @@ int num_sms() {
 // copy brings a whole chunk; otherwise as [L][r][H2], one copy per 256 columns.
 int stream_launch(int in_dtype, StreamLaunch &l) {
     StreamParams &p = l.p;
+    p.inject = g_inject_timeout;
     const bool bf16 = in_dtype == SGMV_BF16;
     const cuuint64_t es = 2;
     p.b4d = 0;
@@ -166,6 +168,12 @@ int stream_launch(int in_dtype, StreamLaunch &l) {
 constexpr uint32_t kStreamSmemBudget = 110u * 1024u;
 constexpr uint32_t kStreamSmemMax = 200u * 1024u;
 
+}  // namespace
+
+void sgmv::note_cuda_error(const char *what, cudaError_t e) { note(what, e); }
+
+int *sgmv::device_error_word() { return error_word(); }
+
 // Launch shape of the streaming kernel for a batch of T rows in S segments
 // (the last max_len rows long at most), or false when the kernel does not
 // apply (r not a multiple of 4 or above 64, or more tiles per cluster than its
@@ -176,9 +184,9 @@ constexpr uint32_t kStreamSmemMax = 200u * 1024u;
 // -- depends on T and the dimensions only, never on the segmentation: as
 // many CTAs per tile (8, 4, 2, 1) as keep CTAs x T within the SM count, each
 // with at least 64 columns of H1 and of H2.
-bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len, int32_t H1,
-                  int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l,
-                  bool grouped) {
+bool sgmv::stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len,
+                        int32_t H1, int32_t H2, int32_t r, int in_dtype, int y_dtype,
+                        StreamLaunch &l, bool grouped) {
     if (r % 4 != 0 || r > 64 || T <= 0 || S <= 0) return false;
     const int64_t avg = ceil_div(T, S);
     // The one-launch grouped form cannot see the segments.  Above 32 rows its
@@ -244,6 +252,8 @@ bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max
     l.y_dtype = y_dtype;
     return true;
 }
+
+namespace {
 
 void stage_sizes(CCParams &p, int mode, int elem);
 
@@ -721,6 +731,44 @@ int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, co
     return cuda_status("adapter B copy",
                        cudaMemcpyAsync(static_cast<uint8_t *>(B_pool) + (size_t)slot * b_bytes,
                                        B_src, b_bytes, cudaMemcpyDefault, s));
+}
+
+int sgmv_debug_inject_wait_timeout(int enable) {
+    g_inject_timeout = enable ? 1 : 0;
+    return SGMV_OK;
+}
+
+int sgmv_read_floor(const void *src, size_t bytes, int32_t T, int32_t L, int32_t H1, int32_t H2,
+                    int32_t r, int in_dtype, int y_dtype, int32_t *ctas, int32_t *cluster,
+                    void *stream) {
+    g_launches = 0;
+    int st = check_common(T, L, r, 0, nullptr, nullptr, nullptr, in_dtype);
+    if (st != SGMV_OK) return st;
+    if ((st = check_dim(H1)) != SGMV_OK) return st;
+    if ((st = check_dim(H2)) != SGMV_OK) return st;
+    if (y_dtype != SGMV_F16 && y_dtype != SGMV_BF16 && y_dtype != SGMV_F32)
+        return SGMV_ERR_INVALID_ARG;
+    if (!src || bytes == 0 || T == 0) return SGMV_ERR_INVALID_ARG;
+    if (!aligned16(src) || bytes % 16 != 0) return SGMV_ERR_ALIGNMENT;
+    // the shape sgmv_apply_rows gives the streaming kernel for this batch:
+    // the one-launch grouped form up to kGroupMaxT rows, else sgmv_apply on
+    // the device grouping (sgmv_max_segments(T, L) segments, no host copy)
+    const int32_t smax = sgmv_max_segments(T, L);
+    StreamLaunch sl = {};
+    if (!stream_shape(T, smax, nullptr, INT_MAX, H1, H2, r, in_dtype, y_dtype, sl,
+                      T <= kGroupMaxT))
+        return SGMV_ERR_UNSUPPORTED;
+    int *err = error_word();
+    if (!err) return SGMV_ERR_CUDA;
+    const uint32_t chunk = sl.p.stage_bytes / 16u * 16u;
+    st = cuda_status("read floor kernel",
+                     read_floor_launch(src, (uint64_t)bytes, sl.p.cl, sl.p.G, sl.p.nst, chunk, err,
+                                       static_cast<cudaStream_t>(stream)));
+    if (st != SGMV_OK) return st;
+    g_launches = 1;
+    if (ctas) *ctas = sl.p.cl * sl.p.G;
+    if (cluster) *cluster = sl.p.cl;
+    return SGMV_OK;
 }
 
 int sgmv_get_device_error(void *stream) {

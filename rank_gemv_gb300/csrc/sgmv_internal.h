@@ -180,6 +180,7 @@ struct StreamParams {
     uint32_t red_off, recv_off, v_off, tab_off, smem_bytes;
     int32_t min_len, max_len;
     float scale;
+    int32_t inject;              // 1: diagnostic launch with an injected wait timeout
 };
 
 struct StreamLaunch {
@@ -194,5 +195,22 @@ struct StreamLaunch {
 // Launch the streaming kernel; returns a cudaError_t value.
 int stream_launch_f16(const StreamLaunch &l);
 int stream_launch_bf16(const StreamLaunch &l);
+
+// Launch shape of the streaming kernel (see sgmv_api.cu); false when the
+// kernel does not apply to the problem.
+bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len, int32_t H1,
+                  int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l,
+                  bool grouped);
+
+// Read-only kernel with a given grid, cluster size and ring (sgmv_floor.cu);
+// returns a cudaError_t value.
+int read_floor_launch(const void *src, uint64_t bytes, int cl, int G, int nst, uint32_t chunk,
+                      int *err, cudaStream_t stream);
+
+// Records a failed CUDA call for sgmv_last_error_string (calling thread).
+void note_cuda_error(const char *what, cudaError_t e);
+
+// Sticky device error word of the current device, or nullptr (error noted).
+int *device_error_word();
 
 }  // namespace sgmv

@@ -78,10 +78,13 @@ struct RingIter {
 };
 
 // Bounded wait of a compute thread; after a timeout the error word is set, the
-// wait is repeated once (copies still in flight land before the CTA moves on)
-// and the thread stops writing y.
-__device__ __forceinline__ void stream_wait(uint64_t *bar, uint32_t parity, bool &lost, int *err) {
-    if (!mbar_wait(bar, parity)) {
+// wait is repeated once with the full limit (copies still in flight land
+// before the CTA moves on) and the thread stops writing y.  `fail` takes the
+// timeout path without polling first (the injected timeout of a diagnostic
+// launch); the repeated wait is the same as after a real timeout.
+__device__ __forceinline__ void stream_wait(uint64_t *bar, uint32_t parity, bool &lost, int *err,
+                                            bool fail = false) {
+    if (fail || !mbar_wait(bar, parity)) {
         set_error(err, kErrTimeout);
         mbar_wait(bar, parity);
         lost = true;
@@ -97,7 +100,7 @@ template <typename Tin, int RK, int R, int CW>
 __device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes, uint32_t act_off,
                                               int nst, int &q, int nA, int hlen, int hn, int rk,
                                               uint64_t *full, uint64_t *empty, float *red,
-                                              bool &lost, int *err) {
+                                              bool &lost, int *err, bool inject) {
     constexpr int KQ = RK / 4, HL = 32 / KQ, HSTR = CW * HL;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int kq = lane % KQ, hl = lane / KQ;
@@ -110,7 +113,7 @@ __device__ __forceinline__ void stream_shrink(uint8_t *sm, uint32_t stage_bytes,
         for (int u = 0; u < 4; ++u) acc[t][u] = 0.f;
     for (int i = 0; i < nA; ++i, ++q) {
         const int s = q % nst;
-        stream_wait(&full[s], (uint32_t)((q / nst) & 1), lost, err);
+        stream_wait(&full[s], (uint32_t)((q / nst) & 1), lost, err, inject && q == 0);
         const int nh = min(hn, hlen - i * hn);
         const uint8_t *base = sm + (size_t)s * stage_bytes;
         const Tin *As = reinterpret_cast<const Tin *>(base);
@@ -226,6 +229,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
     const uint32_t stage_bytes = P.stage_bytes, act_off = P.act_off;
     const float scale = P.scale;
     int *const err = P.err;
+    // diagnostic launches only: the first ring wait of every compute thread
+    // reports a timeout (the chunk is still awaited before it is used)
+    const bool inject = P.inject != 0;
 
     extern __shared__ __align__(128) uint8_t sm[];
     __shared__ __align__(8) uint64_t full[kStreamMaxStages], empty[kStreamMaxStages], vfull[2];
@@ -611,16 +617,16 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                 const int n = (int)lds32(tab + 4 * m + 1);
                 if (n <= 1)
                     stream_shrink<Tin, RK, 1, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
-                                              full, empty, red, lost, err);
+                                              full, empty, red, lost, err, inject);
                 else if (n <= 2)
                     stream_shrink<Tin, RK, 2, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
-                                              full, empty, red, lost, err);
+                                              full, empty, red, lost, err, inject);
                 else if (n <= 4)
                     stream_shrink<Tin, RK, 4, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
-                                              full, empty, red, lost, err);
+                                              full, empty, red, lost, err, inject);
                 else
                     stream_shrink<Tin, RK, 8, CW>(sm, stage_bytes, act_off, nst, q, nA, h1 - h0, hn, rk,
-                                              full, empty, red, lost, err);
+                                              full, empty, red, lost, err, inject);
                 consumers_sync<CW>();
                 // this CTA's partial of v, four consecutive k per thread
                 part = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -46,6 +46,9 @@ SIGNATURES = {
     "sgmv_apply_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp,
                                   _i32, _i32, _i32, _i32, _i32, _vp]),
     "sgmv_load_adapter": (_int, [_vp, _vp, _int, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
+    "sgmv_read_floor": (_int, [_vp, _sz, _i32, _i32, _i32, _i32, _i32, _int, _int, _i32p, _i32p,
+                               _vp]),
+    "sgmv_debug_inject_wait_timeout": (_int, [_int]),
     "sgmv_get_device_error": (_int, [_vp]),
 }
 
@@ -258,6 +261,27 @@ def sgmv_load_adapter(A_pool, B_pool, slot, A_src, B_src, stream=None):
     _check(load_library().sgmv_load_adapter(
         _ptr(A_pool), _ptr(B_pool), _DTYPES[A_pool.dtype], int(slot), _ptr(A_src), _ptr(B_src),
         L, H1, H2, r, st), "sgmv_load_adapter")
+
+
+def sgmv_read_floor(src, nbytes, T, L, H1, H2, r, in_dtype=torch.float16, y_dtype=None):
+    """Read ``nbytes`` of the device tensor ``src`` with the streaming kernel's
+    launch shape for a T-row batch (see include/sgmv.h); returns
+    (ctas, cluster) of the grid it launched."""
+    y_dtype = in_dtype if y_dtype is None else y_dtype
+    if nbytes > src.numel() * src.element_size():
+        raise ValueError("nbytes beyond the source tensor")
+    ctas, cl = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load_library().sgmv_read_floor(
+        _ptr(src), int(nbytes), T, L, H1, H2, r, _DTYPES[in_dtype], _DTYPES[y_dtype],
+        ctypes.byref(ctas), ctypes.byref(cl), _stream(src.device)), "sgmv_read_floor")
+    return ctas.value, cl.value
+
+
+def sgmv_debug_inject_wait_timeout(enable: bool) -> None:
+    """Make this thread's streaming-kernel launches take the timeout path at
+    their first wait (tests of device-side timeout reporting)."""
+    _check(load_library().sgmv_debug_inject_wait_timeout(1 if enable else 0),
+           "sgmv_debug_inject_wait_timeout")
 
 
 def sgmv_get_device_error(device=None) -> int:

@@ -178,3 +178,25 @@ def test_load_adapter_rejects_bad_arguments(lib, kw):
     assert lib.sgmv_load_adapter(args["A"], args["B"], args["in_dt"], args["slot"], args["a"],
                                  args["b"], args["L"], args["H1"], args["H2"], args["r"],
                                  None) == 1
+
+
+def test_read_floor_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(src=A16, n=1 << 20, T=32, L=32, H1=4096, H2=4096, r=16, in_dt=0, y_dt=0)
+        a.update(kw)
+        return lib.sgmv_read_floor(a["src"], a["n"], a["T"], a["L"], a["H1"], a["H2"], a["r"],
+                                   a["in_dt"], a["y_dt"], None, None, None)
+    assert call(src=None) == 1
+    assert call(n=0) == 1
+    assert call(T=0) == 1
+    assert call(src=MIS) == 3
+    assert call(n=(1 << 20) + 8) == 3   # not a whole number of 16-byte pieces
+    assert call(H1=20) == 3
+    assert call(r=6) == 2               # the streaming kernel takes r % 4 == 0 only
+    assert call(r=129) == 2
+    assert call(y_dt=9) == 1
+
+
+def test_timeout_injection_switch(lib):
+    assert lib.sgmv_debug_inject_wait_timeout(1) == 0
+    assert lib.sgmv_debug_inject_wait_timeout(0) == 0

@@ -24,3 +24,44 @@ def test_packed_views_hold_the_tensors_without_overlap():
     # writing through the buffer is seen by the views (one copy moves all three)
     buf.zero_()
     assert not x.any() and not y.any() and not r.any()
+
+
+def test_parallel_oracle_is_the_one_call_oracle():
+    """The all-core CPU baseline runs the unmodified oracle on ranges of rows
+    from several threads; the result must be the single call's, bit for bit,
+    however the positions are cut (ranges inside a segment, across segments,
+    more ranges than rows)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(3)
+    T, L, H1, H2, r = 50, 6, 32, 24, 4
+    ra = rng.integers(-1, L, T).astype(np.int32)
+    X = rng.standard_normal((T, H1))
+    A = rng.standard_normal((L, H1, r))
+    B = rng.standard_normal((L, r, H2))
+    Y = rng.standard_normal((T, H2))
+    o = oracle.default()
+    perm, sp, ix = o.build_segments(ra, L)
+    ref = o.sgmv_apply(Y, X, A, B, sp, ix, 0.5, perm=perm, widened=True)
+    with ThreadPoolExecutor(4) as pool:
+        for n in (1, 3, 7, 50, 80):
+            tasks = bench.oracle_tasks(perm, sp, ix, n)
+            rows = np.concatenate([t[0] for t in tasks])
+            assert np.array_equal(np.sort(rows), np.arange(T))  # every row once
+            got = bench.oracle_apply_parallel(o, pool, Y, X, A, B, perm, sp, ix, 0.5, n)
+            assert np.array_equal(got, ref)
+
+
+def test_rotation_copies():
+    assert bench.rotation_copies(9_175_040, 126 << 20) == 29
+    assert bench.rotation_copies(300 << 20, 126 << 20) == 2
+    assert bench.rotation_copies(90_000, 126 << 20) == 256   # capped: stays in L2
+
+
+def test_default_workload_is_the_full_stack():
+    args = bench.parse_args([])
+    assert args.workload == "llama7b-stack" and args.gpus == 1 and args.warmup >= 3
