@@ -237,6 +237,41 @@ int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const
                        int32_t L, int32_t H1, int32_t H2, int32_t r, void *stream);
 
 /*
+ * Bytes of device workspace sgmv_fused_linear_lora needs: v [T][r] fp32.
+ */
+size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r);
+
+/*
+ * The whole LoRA layer in one pass over its weights: the base linear layer and
+ * the SGMV update together ([Article] §2.1: a LoRA layer computes
+ * y = xW + xAB; [Q&A] §3.2, "Fused Kernel": the LoRA transform is merged into
+ * the base model's linear layer so that memory is read fewer times):
+ *   y[t][j] = round( sum_h x[t][h] * W[h][j]
+ *                    + scale * sum_k v[p][k] * B[idx[s]][k][j] )
+ *   with v[p] = x[t] . A[idx[s]], for physical row t = perm[p] of position p
+ *   in segment s with idx[s] >= 0; rows in no segment with an adapter get
+ *   the base product alone.
+ * Every row t in [0, T) of y is overwritten (y is the layer's output; it must
+ * not overlap x, W, A or B); the sums are fp32 and y is rounded once.
+ *   W  [H1][H2]  device, in_dtype (f16 / bf16), row-major
+ *   x, A, B, perm, seg_ptr, idx, S, L, r as for sgmv_apply; y as for
+ *   sgmv_apply but written, not updated.
+ *   workspace  device, >= sgmv_fused_workspace_bytes(T, r) bytes, 16-byte
+ *              aligned (holds v between the two kernels); may be NULL when
+ *              S == 0.
+ * Decode batches: 1 <= T <= 128 rows and r <= 64 (SGMV_ERR_UNSUPPORTED
+ * otherwise).  Two kernels on `stream`: the CUDA-core shrink writes v, then a
+ * tensor-core kernel streams W and the adapters' B slices once and makes
+ * every element of y.  Errors as for sgmv_apply (host checks, device error
+ * word).
+ */
+int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, const void *A,
+                           const void *B, int in_dtype, float scale, const int32_t *perm,
+                           const int32_t *seg_ptr, const int32_t *idx, int32_t S, int32_t T,
+                           int32_t L, int32_t H1, int32_t H2, int32_t r, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * Loads one adapter into slot `slot` of the stacked pools: A_src [H1][r] into
  * A_pool[slot] and B_src [r][H2] into B_pool[slot], as two asynchronous copies
  * on `stream`.  Page: [Review] "Punica: Multi-Tenant LoRA Serving" (nubint.ai

@@ -733,6 +733,69 @@ int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, co
                                        B_src, b_bytes, cudaMemcpyDefault, s));
 }
 
+size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r) {
+    if (T <= 0 || r <= 0) return 0;
+    return ((size_t)T * (size_t)r * 4u + 255u) / 256u * 256u;
+}
+
+int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, const void *A,
+                           const void *B, int in_dtype, float scale, const int32_t *perm,
+                           const int32_t *seg_ptr, const int32_t *idx, int32_t S, int32_t T,
+                           int32_t L, int32_t H1, int32_t H2, int32_t r, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    g_launches = 0;
+    int st = check_common(T, L, r, S, seg_ptr, idx, nullptr, in_dtype);
+    if (st != SGMV_OK) return st;
+    if ((st = check_dim(H1)) != SGMV_OK) return st;
+    if ((st = check_dim(H2)) != SGMV_OK) return st;
+    if (y_dtype != SGMV_F16 && y_dtype != SGMV_BF16 && y_dtype != SGMV_F32)
+        return SGMV_ERR_INVALID_ARG;
+    if (T > kFusedMaxT || r > kFusedMaxR) return SGMV_ERR_UNSUPPORTED;
+    if (T == 0) return SGMV_OK;
+    if (!y || !x || !W || !A || !B) return SGMV_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(W) || !aligned16(A) || !aligned16(B))
+        return SGMV_ERR_ALIGNMENT;
+    if (S > 0) {
+        if (!workspace || workspace_bytes < sgmv_fused_workspace_bytes(T, r))
+            return SGMV_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SGMV_ERR_ALIGNMENT;
+    }
+    int *err = error_word();
+    if (!err) return SGMV_ERR_CUDA;
+    int launches = 0;
+    if (S > 0) {
+        // v = x . A[idx] by sorted position, fp32, into the workspace
+        st = sgmv_shrink(static_cast<float *>(workspace), x, A, in_dtype, perm, seg_ptr, idx, S,
+                         nullptr, T, L, H1, r, stream);
+        if (st != SGMV_OK) return st;
+        launches = g_launches;
+    }
+    FusedArgs g = {};
+    g.y = y;
+    g.x = x;
+    g.W = W;
+    g.B = B;
+    g.v = static_cast<const float *>(workspace);
+    g.perm = perm;
+    g.seg_ptr = seg_ptr;
+    g.idx = idx;
+    g.err = err;
+    g.S = S;
+    g.T = T;
+    g.L = L;
+    g.H1 = H1;
+    g.H2 = H2;
+    g.r = r;
+    g.scale = scale;
+    g.in_dtype = in_dtype;
+    g.y_dtype = y_dtype;
+    g.nsm = num_sms();
+    g.stream = static_cast<cudaStream_t>(stream);
+    st = cuda_status("fused linear + LoRA kernel", fused_launch(g));
+    g_launches = st == SGMV_OK ? launches + 1 : launches;
+    return st;
+}
+
 int sgmv_debug_inject_wait_timeout(int enable) {
     g_inject_timeout = enable ? 1 : 0;
     return SGMV_OK;

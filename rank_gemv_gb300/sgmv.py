@@ -45,6 +45,9 @@ SIGNATURES = {
                                _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sgmv_apply_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp,
                                   _i32, _i32, _i32, _i32, _i32, _vp]),
+    "sgmv_fused_workspace_bytes": (_sz, [_i32, _i32]),
+    "sgmv_fused_linear_lora": (_int, [_vp, _int, _vp, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp,
+                                      _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
     "sgmv_load_adapter": (_int, [_vp, _vp, _int, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
     "sgmv_read_floor": (_int, [_vp, _sz, _i32, _i32, _i32, _i32, _i32, _int, _int, _i32p, _i32p,
                                _vp]),
@@ -240,6 +243,36 @@ def sgmv_apply_noalloc(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_h
         _ptr(y), _DTYPES[y.dtype], _ptr(x), _ptr(A), _ptr(B), _DTYPES[x.dtype], float(scale),
         _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")), _ptr(_meta(idx, "idx")),
         _nseg(idx, S), _ptr(sph), T, L, H1, H2, r, _stream(x.device)), "sgmv_apply_noalloc")
+    return y
+
+
+def sgmv_fused_workspace_bytes(T: int, r: int) -> int:
+    return int(load_library().sgmv_fused_workspace_bytes(T, r))
+
+
+def sgmv_fused_linear_lora(y, x, W, A, B, seg_ptr, idx, scale=1.0, perm=None, S=None,
+                           workspace=None):
+    """y = x @ W + scale * SGMV delta (the LoRA layer in one pass), written
+    into y; returns y.  ``workspace`` (uint8 device tensor of at least
+    sgmv_fused_workspace_bytes(T, r) bytes) holds v; one is allocated when
+    None."""
+    T, H1 = x.shape
+    L, _, r = A.shape
+    H2 = y.shape[1]
+    if tuple(W.shape) != (H1, H2):
+        raise ValueError("W must be [H1, H2]")
+    if W.dtype != x.dtype:
+        raise TypeError("W and x types differ")
+    nseg = _nseg(idx, S) if idx is not None else 0
+    if workspace is None and nseg > 0:
+        workspace = torch.empty(sgmv_fused_workspace_bytes(T, r), dtype=torch.uint8,
+                                device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().sgmv_fused_linear_lora(
+        _ptr(y), _DTYPES[y.dtype], _ptr(x), _ptr(W), _ptr(A), _ptr(B), _DTYPES[x.dtype],
+        float(scale), _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")),
+        _ptr(_meta(idx, "idx")), nseg, T, L, H1, H2, r, _ptr(workspace), ws_bytes,
+        _stream(x.device)), "sgmv_fused_linear_lora")
     return y
 
 

@@ -149,6 +149,14 @@ def make(name: str, seed: int = 0, *, y_dtype=None, y0="zeros", shuffle_rows=Fal
                 generator=g, meta={"seed": seed})
 
 
+def base_weight(H1: int, H2: int, *, dtype=F16, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Weight W [H1, H2] of the base linear layer for the fused layer
+    y = x W + LoRA delta, W ~ N(0, 1/H1) (variance), so that x W has RMS
+    about 1 like the delta."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    return _normal(g, (H1, H2), H1 ** -0.5, dtype, device)
+
+
 def stack_seed(seed: int, layer: int, proj: int) -> int:
     return 1000 * seed + 7 * layer + proj
 

@@ -200,3 +200,31 @@ def test_read_floor_rejects_bad_arguments(lib):
 def test_timeout_injection_switch(lib):
     assert lib.sgmv_debug_inject_wait_timeout(1) == 0
     assert lib.sgmv_debug_inject_wait_timeout(0) == 0
+
+
+def test_fused_linear_lora_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(y=A16, y_dt=0, x=A16, W=A16, A=A16, B=A16, in_dt=0, perm=None, seg=A16,
+                 idx=A16, S=1, T=4, L=2, H1=64, H2=64, r=16, ws=A16, wsb=1 << 20)
+        a.update(kw)
+        return lib.sgmv_fused_linear_lora(a["y"], a["y_dt"], a["x"], a["W"], a["A"], a["B"],
+                                          a["in_dt"], 1.0, a["perm"], a["seg"], a["idx"], a["S"],
+                                          a["T"], a["L"], a["H1"], a["H2"], a["r"], a["ws"],
+                                          a["wsb"], None)
+    assert call(T=129) == 2            # decode batches only
+    assert call(r=65) == 2
+    assert call(r=0) == 1
+    assert call(H1=20) == 3
+    assert call(H2=12) == 3
+    assert call(W=None) == 1
+    assert call(W=MIS) == 3
+    assert call(y=MIS) == 3
+    assert call(in_dt=2) == 1
+    assert call(y_dt=4) == 1
+    assert call(ws=None, wsb=0) == 6   # v needs the workspace
+    assert call(wsb=16) == 6
+    assert call(ws=MIS) == 3
+    assert call(T=0, x=None, y=None) == 0
+    assert lib.sgmv_fused_workspace_bytes(128, 16) == 128 * 16 * 4
+    assert lib.sgmv_fused_workspace_bytes(3, 5) == 256
+    assert lib.sgmv_fused_workspace_bytes(0, 16) == 0

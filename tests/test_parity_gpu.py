@@ -208,6 +208,23 @@ def test_shrink_and_expand_separately(r):
                  "shrink+expand")
 
 
+@pytest.mark.parametrize("T,L,H1,r", [(128, 128, 4096, 16), (128, 2, 4096, 16), (128, 128, 11008, 16),
+                                       (64, 128, 4096, 64)])
+def test_shrink_at_decode_shapes(T, L, H1, r):
+    """The standalone shrink at the Llama-2-7B projections' input widths, one
+    row per adapter or a few shared adapters with rows of no adapter."""
+    g = torch.Generator().manual_seed(T + L + H1 + r)
+    ids = (torch.randperm(T, generator=g) % L).to(torch.int32) if L >= T else \
+        torch.randint(-1, L, (T,), generator=g, dtype=torch.int32)
+    w = wl.draw(T, L, H1, 64, r, ids, seed=H1 + r)
+    perm, seg_ptr, idx, _ = device_grouping(w.row_adapter, w.L)
+    o_perm, o_seg, o_idx = oracle.build_segments(w.row_adapter, w.L)
+    v = torch.full((w.T, r), float("nan"), device=DEV)
+    sg().sgmv_shrink(v, w.X.to(DEV), w.A.to(DEV), seg_ptr, idx, perm=perm)
+    check_error_word(0)
+    assert_close(v, oracle.sgmv_shrink(w.X, w.A, o_seg, o_idx, perm=o_perm), "shrink v")
+
+
 # ---- device grouping ------------------------------------------------------
 @pytest.mark.parametrize("T,L", [(1, 1), (8, 4), (32, 32), (64, 128), (100, 1), (2304, 8),
                                  (5000, 3000), (20000, 37), (777, 32767)])
