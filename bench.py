@@ -71,6 +71,10 @@ def parse_args(argv=None):
     p.add_argument("--load", action="store_true",
                    help="on-demand adapter loading instead: one Llama-2-7B adapter (224 "
                         "projections) from pinned host memory, alone and during the stack's SGMV")
+    p.add_argument("--fused", action="store_true",
+                   help="the fused LoRA layer instead: y = x W + LoRA delta in one pass "
+                        "(sgmv_fused_linear_lora) against cuBLAS x W alone and x W + SGMV, "
+                        "over batch sizes and the Llama-2-7B projection shapes")
     p.add_argument("--figure", action="store_true",
                    help="the pages' micro-benchmark instead: latency of the base layer alone, "
                         "with a per-adapter loop and with SGMV, over batch sizes and adapter counts")
@@ -529,6 +533,9 @@ def run_ours(args, rank, world, local):
         for name in SIDE_WORKLOADS:
             if name != args.workload:
                 side[name] = measure_workload(name, args, dev, sgmv, wl, l2, peak, flush)
+        fl = fused_layer_point(sgmv, wl, dev, 4096, 4096, 128, args.seed + 5, args.latency_iters,
+                               flush, l2, peak)
+        side["fused-linear-lora-q"] = fl
         if "decode-distinct" in side and "decode-shared" in side:
             d, s = side["decode-distinct"], side["decode-shared"]
             side["distinct_vs_shared"] = {
@@ -981,6 +988,105 @@ def figure_point(sgmv, dev, W, A, B, T, n_adapters, seed):
     return {"base": base, "naive": naive, "sgmv": with_sgmv}, err, (x, ids, y)
 
 
+def fused_layer_point(sgmv, wl, dev, H1, H2, T, seed, iters, flush, l2, peak):
+    """The LoRA layer y = x W + (x A[a]) B[a] for T decode rows, each on its own
+    adapter out of 128 (r = 16, fp16): cuBLAS x W alone ("base"), x W then
+    sgmv_apply ("two_step", the grouping built once and reused, as a model's
+    layers reuse it), and sgmv_fused_linear_lora ("fused", same grouping).
+    Each method alone after an L2 flush (median of `iters`) and back to back
+    over rotating copies of the weights whose pass exceeds twice the L2."""
+    import torch
+
+    L, r = 128, 16
+    per_copy = H1 * H2 * 2 + L * (H1 * r + r * H2) * 2
+    n_copies = rotation_copies(per_copy, l2, cap=8)
+    sets = []
+    for c in range(n_copies):
+        X, A, B = _fused_inputs(wl, dev, H1, H2, T, L, r, seed + c)
+        W = wl.base_weight(H1, H2, seed=seed + 31 + c, device=dev)
+        sets.append((X, A, B, W, torch.empty(T, H2, dtype=torch.float16, device=dev)))
+    g = torch.Generator().manual_seed(seed)
+    ra = torch.randperm(L, generator=g)[:T].to(torch.int32).to(dev)
+    perm, seg_ptr, idx, _ = sgmv.sgmv_build_segments_device(ra, L)
+    ws = torch.empty(sgmv.sgmv_fused_workspace_bytes(T, r), dtype=torch.uint8, device=dev)
+
+    def base(st):
+        X, A, B, W, y = st
+        torch.matmul(X, W, out=y)
+
+    def two_step(st):
+        X, A, B, W, y = st
+        torch.matmul(X, W, out=y)
+        sgmv.sgmv_apply(y, X, A, B, seg_ptr, idx, 1.0, perm=perm)
+
+    def fused(st):
+        X, A, B, W, y = st
+        sgmv.sgmv_fused_linear_lora(y, X, W, A, B, seg_ptr, idx, 1.0, perm=perm, workspace=ws)
+
+    two_step(sets[0])
+    y_two = sets[0][4].float().clone()
+    fused(sets[0])
+    y_fused = sets[0][4].float()
+    rms = y_two.pow(2).mean().sqrt().item()
+    err = (y_two - y_fused).abs().max().item() / max(rms, 1e-30)
+    nbytes = (H1 * H2 + T * (H1 * r + r * H2) + T * H1 + T * H2) * 2
+    out = {"T": T, "H1": H1, "H2": H2, "adapters": T, "r": r, "unit": "us",
+           "bytes_per_call": nbytes, "max_diff_over_rms": err}
+    for name, fn in (("base", base), ("two_step", two_step), ("fused", fused)):
+        for _ in range(3):
+            fn(sets[0])
+        torch.cuda.synchronize()
+        graph = capture([lambda: fn(sets[0])])
+        out[name] = isolated_us(graph.replay, flush, iters)
+        out[name + "_back_to_back"] = back_to_back_us([(lambda st=st: fn(st)) for st in sets],
+                                                      max(8 * n_copies, 64))
+    assert sgmv.sgmv_get_device_error(dev) == 0
+    out["fused_frac"] = hbm(nbytes, out["fused"], peak)[1]
+    out["fused_frac_back_to_back"] = hbm(nbytes, out["fused_back_to_back"], peak)[1]
+    out["fused_over_two_step"] = out["fused"] / out["two_step"]
+    return out
+
+
+def _fused_inputs(wl, dev, H1, H2, T, L, r, seed):
+    """x [T, H1], A [L, H1, r], B [L, r, H2] (fp16, the workloads' distributions),
+    drawn on the device."""
+    import torch
+
+    g = torch.Generator(device=dev).manual_seed(seed)
+    X = wl._normal(g, (T, H1), 1.0, wl.F16, dev)
+    A = wl._normal(g, (L, H1, r), H1 ** -0.5, wl.F16, dev)
+    B = wl._normal(g, (L, r, H2), r ** -0.5, wl.F16, dev)
+    return X, A, B
+
+
+def run_fused(args):
+    """The fused LoRA layer ("Punica: when LoRA fine-tuned models need
+    multi-tenant serving", omica.com.cn article, §2.1: y = xW + xAB; "How to
+    deploy several LoRA adapters without reloading the base model", aivaro.ru,
+    §3.2, fused kernel) on one GB300: for each point, the layer with cuBLAS x W
+    alone, with x W then SGMV, and fused.  Prints one JSON line per point."""
+    import torch
+
+    from rank_gemv_gb300 import build as _build
+    from rank_gemv_gb300 import sgmv
+    from rank_gemv_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    sgmv.load_library()
+    peak, _ = measured_peak()
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    points = [(4096, 4096, T) for T in (1, 8, 32, 64, 128)]
+    points += [(4096, 11008, 128), (11008, 4096, 128)]
+    for i, (H1, H2, T) in enumerate(points):
+        out = fused_layer_point(sgmv, wl, dev, H1, H2, T, args.seed + 97 * i, args.latency_iters,
+                                flush, l2, peak)
+        out["bench"] = "fused_linear_lora"
+        print(json.dumps(out), flush=True)
+
+
 def run_figure(args):
     """The pages' micro-benchmark (the "Punica: when LoRA fine-tuned models need
     multi-tenant serving" article, §2.2 figure): one Llama-2-7B q projection,
@@ -1144,6 +1250,10 @@ def main():
     if args.figure:
         if rank == 0:
             run_figure(args)
+        return
+    if args.fused:
+        if rank == 0:
+            run_fused(args)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -237,7 +237,10 @@ int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const
                        int32_t L, int32_t H1, int32_t H2, int32_t r, void *stream);
 
 /*
- * Bytes of device workspace sgmv_fused_linear_lora needs: v [T][r] fp32.
+ * Bytes of device workspace sgmv_fused_linear_lora needs: v [T][r] fp32, then
+ * the 16-bit v tiles of the adapter terms (at most ceil(T / (32 / rp)) tiles,
+ * or 2T for rp = 64, of [round16(T)][64] elements each, rp = r rounded up to
+ * 16, 32 or 64).
  */
 size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r);
 
@@ -257,12 +260,14 @@ size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r);
  *   x, A, B, perm, seg_ptr, idx, S, L, r as for sgmv_apply; y as for
  *   sgmv_apply but written, not updated.
  *   workspace  device, >= sgmv_fused_workspace_bytes(T, r) bytes, 16-byte
- *              aligned (holds v between the two kernels); may be NULL when
- *              S == 0.
+ *              aligned (holds v and its tiles between the kernels); may be NULL
+ *              when S == 0.
  * Decode batches: 1 <= T <= 128 rows and r <= 64 (SGMV_ERR_UNSUPPORTED
- * otherwise).  Two kernels on `stream`: the CUDA-core shrink writes v, then a
- * tensor-core kernel streams W and the adapters' B slices once and makes
- * every element of y.  Errors as for sgmv_apply (host checks, device error
+ * otherwise).  Three kernels on `stream` (one when S == 0): the CUDA-core
+ * shrink writes v; a small kernel lays scale * v out as block-diagonal 16-bit
+ * tiles (each value as a high and a low half); a tensor-core kernel streams W
+ * and the adapters' B slices once and makes every element of y, base and
+ * adapter terms in one fp32 accumulation.  Errors as for sgmv_apply (host checks, device error
  * word).
  */
 int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, const void *A,

@@ -733,9 +733,13 @@ int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, co
                                        B_src, b_bytes, cudaMemcpyDefault, s));
 }
 
+// Workspace of the fused layer: v [T][r] fp32, then the pair table and the v
+// tiles, each part 256-byte aligned.
+size_t fused_v_bytes(int32_t T, int32_t r) { return ((size_t)T * (size_t)r * 4u + 255u) / 256u * 256u; }
+
 size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r) {
     if (T <= 0 || r <= 0) return 0;
-    return ((size_t)T * (size_t)r * 4u + 255u) / 256u * 256u;
+    return fused_v_bytes(T, r) + fused_prep_bytes(T, r);
 }
 
 int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, const void *A,
@@ -775,7 +779,7 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
     g.x = x;
     g.W = W;
     g.B = B;
-    g.v = static_cast<const float *>(workspace);
+    g.v = S > 0 ? static_cast<const float *>(workspace) : nullptr;
     g.perm = perm;
     g.seg_ptr = seg_ptr;
     g.idx = idx;
@@ -789,10 +793,12 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
     g.scale = scale;
     g.in_dtype = in_dtype;
     g.y_dtype = y_dtype;
+    g.prep = S > 0 ? static_cast<uint8_t *>(workspace) + fused_v_bytes(T, r) : nullptr;
     g.nsm = num_sms();
+    g.x_early = launches > 0;
     g.stream = static_cast<cudaStream_t>(stream);
-    st = cuda_status("fused linear + LoRA kernel", fused_launch(g));
-    g_launches = st == SGMV_OK ? launches + 1 : launches;
+    st = cuda_status("fused linear + LoRA kernels", fused_launch(g));
+    g_launches = st == SGMV_OK ? launches + (S > 0 ? 2 : 1) : launches;
     return st;
 }
 

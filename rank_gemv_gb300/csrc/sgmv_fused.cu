@@ -10,38 +10,50 @@
 // the base model's linear layer so that memory is read fewer times).
 //
 // For decode batches (T <= 128 rows) the layer is a stream over W (H1 x H2)
-// and the adapters' B slices with little arithmetic per byte.  After the
-// shrink v = x . A[a] (a CUDA-core launch of its own, writing v to a small
-// workspace), this kernel makes every output element of y once, on the
-// tensor cores, in the transposed ("swap AB") form that suits few rows:
+// and the adapters' B slices with little arithmetic per byte.  Three launches
+// on the stream, chained by programmatic dependent launch:
+//   1. the shrink v = x . A[a] (the CUDA-core kernel of sgmv_shrink), fp32
+//      by sorted position into the workspace;
+//   2. sgmv_fused_prep_kernel: the adapter terms' work list and operands
+//      (below) into the workspace;
+//   3. sgmv_fused_kernel: every output element of y, once, on the tensor
+//      cores, in the transposed ("swap AB") form that suits few rows:
 //
-//   D[j, t] = sum_h W[h, j] x[t, h]  +  sum over segments s of
-//             sum_k B[a_s][k, j] (scale v[t, k] if row t is in s, else 0)
+//   D[j, t] = sum_h W[h, j] x[t, h]  +  sum_k B[a_t][k, j] (scale v[t, k])
 //
 // with M = 128 columns j of W per tile (W and B tiles are MN-major A
 // operands, loaded by TMA with 128-byte swizzle), N = the batch's rows
 // rounded up to 16 (x rows are the K-major B operand) and fp32 accumulation
-// in tensor memory.  The LoRA terms are extra MMAs over blocks of up to 64
-// rows: for every (segment, 64-row block) pair with a row in both, B[a]^T
-// times a tile of scale * v that is zero outside the segment, as two 16-bit
-// halves (hi = round(scale v), lo = round(scale v - hi)) so v keeps about 16
-// significant bits.  The whole layer -- base and LoRA -- is one accumulation,
-// rounded once to y's type.  Accumulator addresses stay at multiples of 64
-// columns and accumulator reads at multiples of 32 (the placements the other
-// tensor-core kernels here use).
+// in tensor memory, where accumulator column t is row t of the batch.
 //
-// Decomposition: one tile of 128 columns per cluster of CL CTAs; CTA `rank`
-// takes an even share of H1's 64-column k-blocks and every CL-th LoRA pair,
-// so all CTAs stream about the same bytes.  The partial accumulators are
-// exchanged through distributed shared memory (each CTA owns every CL-th
-// group of 32 rows of the tile) and summed in rank order: deterministic.
+// Adapter terms.  The rows of the batch fall into 16-row chunks (accumulator
+// columns 16c .. 16c + 15).  A "pair" is one segment with an adapter and one
+// chunk holding at least one of its rows; there are at most T pairs.  For
+// each pair the prep kernel writes a 16 x 64 tile of 16-bit values: row n is
+// batch row 16c + n, holding scale * v of that row if the row is in the
+// segment, else 0, as two halves (hi = round(scale v), lo = round(scale v -
+// hi)) so that v keeps about 16 significant bits.  The pair's term is then a
+// handful of N = 16 MMAs into accumulator columns 16c .., with the segment's
+// B slice (r rows, padded to rp = 16, 32 or 64) as the A operand, once
+// against the hi half and once against the lo half.  The whole layer -- base
+// and adapter terms -- is one fp32 accumulation, rounded once to y's type.
 //
-// Warps: 0-3 read the accumulator (one TMEM lane, i.e. one column j, per
-// thread) and write y; lane 0 of warp 0 also issues the MMAs; warp 4 fills
-// the ring in order: TMA loads (W before griddepcontrol.wait, x after it)
-// and the v tiles (v is written by the shrink launched just before).  Each
-// barrier has one waiting role that takes its phases in order.  Every
-// mbarrier wait is bounded.
+// Decomposition of the fused kernel: one tile of 128 columns per cluster of
+// CL CTAs; CTA `rank` takes an even share of H1's 64-column k-blocks and
+// every CL-th group of pairs, so all CTAs stream about the same bytes.  The
+// partial accumulators are exchanged through distributed shared memory (each
+// CTA owns every CL-th group of 32 rows of the tile) and summed in rank
+// order: deterministic.
+//
+// Warps of the fused kernel: 0-3 read the accumulator (one TMEM lane, i.e.
+// one column j, per thread) and write y; before that, warp 3 issues the MMAs
+// and warp 2 reads the pair table; warp 4 fills the ring in order (W before
+// griddepcontrol.wait, and x too when the shrink was launched before it,
+// since that kernel waits for x's producer first; the adapter operands after
+// the wait).  The issuing warps wait as a whole and one lane issues: a warp
+// whose other lanes sit in a suspended mbarrier wait holds up a lane that
+// branched away from them.  Each barrier has one waiting role that takes its
+// phases in order.  Every mbarrier wait is bounded.
 #include <cuda.h>
 
 #include <algorithm>
@@ -57,224 +69,372 @@ namespace {
 
 constexpr int kFusedThreads = 160;
 constexpr int kFusedCols = 128;               // columns of W per tile (M of every MMA)
-constexpr int kFusedMaxStages = 8;
-constexpr uint32_t kFusedStage = 32768;       // bytes of one ring stage
-constexpr uint32_t kFusedXOff = 16384;        // x tile, or the v tiles, at this offset
-constexpr uint32_t kFusedVloOff = kFusedXOff + 8192;  // v tiles hold up to 64 rows
+constexpr int kFusedMaxStages = 16;
+constexpr uint32_t kFusedXOff = 16384;        // x tile at this offset of a stage
 constexpr uint32_t kFusedWBytes = 2u * 64u * 128u;  // two 64-column halves of a k-block of W
+constexpr int kFusedMaxPairs = 128;           // at most T pairs, T <= 128
+constexpr int kFusedMaxPPI = 8;               // pairs per ring stage
+constexpr int kPrepThreads = 256;
+constexpr int kPrepMaxCtas = 32;
 
-struct FusedParams {
-    CUtensorMap tmap_w;  // W as [H1][H2], box {64, 64}, 128-byte swizzle
-    CUtensorMap tmap_x;  // x as [T][H1], box {64, npad}
-    CUtensorMap tmap_b;  // B as [L][r][H2], box {64, r16, 1}
-    void *y;
-    const float *v;      // [T][r] fp32 by sorted position
+__host__ __device__ inline int fused_rp(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
+// 16 x 64 tiles of v per pair: hi and lo share one tile for rp <= 32
+__host__ __device__ inline int fused_ntile(int rp) { return rp <= 32 ? 1 : 2; }
+// bytes of a pair's B slice (both 64-column halves) and of its v tiles
+__host__ __device__ inline uint32_t fused_abytes(int rp) { return 2u * (uint32_t)rp * 128u; }
+__host__ __device__ inline uint32_t fused_vbytes(int rp) { return (uint32_t)fused_ntile(rp) * 2048u; }
+// the pair table: [0] = pairs, then (adapter, chunk) per pair; 256-byte rounded
+__host__ __device__ inline size_t fused_ptab_bytes(int T) {
+    return ((size_t)(1 + 2 * T) * 4u + 255u) / 256u * 256u;
+}
+
+// ---- work list and v tiles -------------------------------------------------
+struct PrepParams {
+    const float *v;          // [T][r] fp32 by sorted position (the shrink's output)
     const int32_t *perm, *seg_ptr, *idx;
     int *err;
-    int32_t S, T, L, H1, H2, r;
-    int32_t r16;   // r rounded up to 16 (K of the LoRA MMAs)
-    int32_t npad;  // T rounded up to 16 (N of the base MMAs)
-    int32_t cl;    // CTAs per cluster (split of H1)
-    int32_t kbt;   // 64-column k-blocks of H1
-    int32_t nst;   // ring stages
-    uint32_t tmem_cols;
+    int32_t *ptab;           // pair table
+    void *vt;                // [pair][ntile][16][64] 16-bit
+    int32_t S, T, L, r, rp;
+    int32_t early;           // 1: the metadata may be read before griddepcontrol.wait
     float scale;
 };
+
+// Every CTA lists the slots (segments with an adapter and rows, in segment
+// order), maps each position to its slot and each row to its position, and
+// numbers the pairs: slot by slot, chunks in ascending order.  CTA 0 writes
+// the pair table and reports bad metadata; all CTAs then write every
+// gridDim.x-th 16-byte chunk of the pairs' v tiles.
+template <typename Tin>
+__global__ void __launch_bounds__(kPrepThreads) sgmv_fused_prep_kernel(const PrepParams P) {
+    // the fused kernel may start its base k-blocks now: it reads what this
+    // kernel writes only after its own griddepcontrol.wait
+    pdl_trigger();
+    if (!P.early) pdl_wait();  // the metadata may come from the kernel just before
+    const int T = P.T, S = P.S, L = P.L, r = P.r, rp = P.rp;
+    __shared__ int s_b[128], s_e[128], s_a[128];
+    __shared__ unsigned s_mask[128];
+    __shared__ int s_rowslot[128], s_rowpos[128];
+    __shared__ int s_pslot[kFusedMaxPairs], s_pchunk[kFusedMaxPairs];
+    __shared__ int s_wsum[kPrepThreads / 32];
+    __shared__ int s_nslot, s_np;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool report = blockIdx.x == 0;
+    if (tid < 128) {
+        s_rowslot[tid] = -1;
+        s_mask[tid] = 0u;
+    }
+    if (warp == 0) {
+        int n = 0;
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s = s0 + lane;
+            int b = 0, e = 0, a = -1;
+            bool ok = false;
+            if (s < S) {
+                b = P.seg_ptr[s];
+                e = P.seg_ptr[s + 1];
+                a = P.idx[s];
+                const bool seg_good = b >= 0 && e >= b && e <= T;
+                if (report && !seg_good) set_error(P.err, kErrBadSegments);
+                if (report && seg_good && e > b && (a < -1 || a >= L)) set_error(P.err, kErrBadIndex);
+                ok = seg_good && e > b && a >= 0 && a < L;
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            const int i = n + __popc(m & ((1u << lane) - 1u));
+            if (ok && i < 128) {
+                s_b[i] = b;
+                s_e[i] = e;
+                s_a[i] = a;
+            }
+            n += __popc(m);
+        }
+        if (lane == 0) s_nslot = min(n, 128);  // slots hold disjoint rows: n <= T
+    }
+    __syncthreads();
+    const int nslot = s_nslot;
+    if (tid < T) {
+        // position p: the last slot starting at or before it, if it ends after it
+        const int p = tid;
+        int lo = 0, hi = nslot - 1, i = -1;
+        while (lo <= hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_b[mid] <= p) {
+                i = mid;
+                lo = mid + 1;
+            } else {
+                hi = mid - 1;
+            }
+        }
+        if (i >= 0 && p < s_e[i]) {
+            const int t = P.perm ? P.perm[p] : p;
+            if (t < 0 || t >= T) {
+                if (report) set_error(P.err, kErrBadIndex);
+            } else {
+                s_rowslot[t] = i;
+                s_rowpos[t] = p;
+                atomicOr(&s_mask[i], 1u << (t >> 4));
+            }
+        }
+    }
+    __syncthreads();
+    // pairs: exclusive prefix over slots of their chunk counts
+    const int cnt = tid < nslot ? __popc(s_mask[tid]) : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int woff = 0;
+    for (int w = 0; w < warp; ++w) woff += s_wsum[w];
+    if (tid < nslot) {
+        unsigned m = s_mask[tid];
+        for (int k = woff + incl - cnt; m != 0u; ++k) {
+            s_pslot[k] = tid;
+            s_pchunk[k] = __ffs(m) - 1;
+            m &= m - 1u;
+        }
+    }
+    if (tid == kPrepThreads - 1) s_np = woff + incl;
+    __syncthreads();
+    const int np = min(s_np, kFusedMaxPairs);
+    // Written only after the wait: the kernel before this one on the stream
+    // (the last fused kernel) may still read the workspace until then.
+    if (P.early) pdl_wait();  // also: v is written by the shrink
+    if (report) {
+        for (int k = tid; k < np; k += kPrepThreads) {
+            P.ptab[1 + 2 * k] = s_a[s_pslot[k]];
+            P.ptab[2 + 2 * k] = s_pchunk[k];
+        }
+        if (tid == 0) P.ptab[0] = np;
+    }
+    const int ntile = fused_ntile(rp);
+    const int per_pair = ntile * 16 * 8;  // 16-byte chunks
+    const float scale = P.scale;
+    Tin *const out = static_cast<Tin *>(P.vt);
+    for (int e = blockIdx.x * kPrepThreads + tid; e < np * per_pair; e += gridDim.x * kPrepThreads) {
+        const int k = e / per_pair, rem = e - k * per_pair;
+        const int tile = rem >> 7, n = (rem >> 3) & 15, c8 = rem & 7;
+        const int t = 16 * s_pchunk[k] + n;
+        __align__(16) Tin hv[8];
+        if (t < T && s_rowslot[t] == s_pslot[k]) {
+            const float *vr = P.v + (size_t)s_rowpos[t] * r;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int col = 8 * c8 + u;
+                const int h = rp <= 32 ? col >> 5 : tile;
+                const int kk = rp <= 32 ? col & 31 : col;
+                const float f = kk < r ? scale * vr[kk] : 0.f;
+                const Tin hi = from_f<Tin>(f);
+                hv[u] = h ? from_f<Tin>(f - to_f<Tin>(hi)) : hi;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) hv[u] = from_f<Tin>(0.f);
+        }
+        *reinterpret_cast<uint4 *>(out + ((size_t)(k * ntile + tile) * 16 + n) * 64 + 8 * c8) =
+            *reinterpret_cast<const uint4 *>(hv);
+    }
+}
+
+// ---- the fused layer -------------------------------------------------------
+struct FusedParams {
+    CUtensorMap tmap_w;   // W as [H1][H2], box {64, 64}, 128-byte swizzle
+    CUtensorMap tmap_x;   // x as [T][H1], box {64, npad}
+    CUtensorMap tmap_b;   // B as [L][r][H2], box {64, rp, 1}
+    CUtensorMap tmap_v;   // v tiles as [T * ntile * 16][64], box {64, ppi * ntile * 16}
+    void *y;
+    const int32_t *ptab;
+    int *err;
+    int32_t T, H1, H2;
+    int32_t rp;       // r rounded up to 16, 32 or 64
+    int32_t npad;     // T rounded up to 16 (N of the base MMAs)
+    int32_t cl;       // CTAs per cluster (split of the tile's k-blocks)
+    int32_t kbt;      // 64-column k-blocks of H1
+    int32_t nst;      // ring stages
+    int32_t ppi;      // pairs per ring stage
+    int32_t x_early;  // 1: x may be read before griddepcontrol.wait
+    int32_t lora;     // 1: the pair table and v tiles were written (segments given)
+    uint32_t stage_bytes;  // >= 16 KB of W + the x tile, and >= ppi pairs' operands
+    uint32_t tmem_cols;
+};
+
+constexpr int kItemLora = 1, kItemEnd = 2;
 
 template <typename Tin, typename Ty>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     sgmv_fused_kernel(const __grid_constant__ FusedParams P) {
-    const int T = P.T, S = P.S, L = P.L, H2 = P.H2, r = P.r, r16 = P.r16, npad = P.npad;
-    const int C = P.cl, kbt = P.kbt, nst = P.nst;
-    const float scale = P.scale;
+    const int T = P.T, H2 = P.H2, rp = P.rp, npad = P.npad;
+    const int C = P.cl, kbt = P.kbt, nst = P.nst, ppi = P.ppi;
     int *const err = P.err;
-    const int32_t *const seg_ptr = P.seg_ptr;
-    const int32_t *const idx = P.idx;
-    const int32_t *const perm = P.perm;
 
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t full[kFusedMaxStages], empty[kFusedMaxStages], done, red_full;
-    __shared__ int s_rowseg[128];   // segment of physical row t (-1: no adapter)
-    __shared__ int s_rowpos[128];   // its sorted position
-    __shared__ int s_pseg[128];     // LoRA pairs: segment ...
-    __shared__ int s_pblk[128];     // ... and 64-row block
-    __shared__ int s_npairs, s_lost, s_wcnt[4];
+    __shared__ __align__(8) uint64_t full[kFusedMaxStages], empty[kFusedMaxStages], done, red_full,
+        tab_ready;
+    __shared__ int s_pa[kFusedMaxPairs], s_pc[kFusedMaxPairs];  // pair table
+    __shared__ int s_kind[kFusedMaxStages], s_cnt[kFusedMaxStages];
+    __shared__ int s_chunk[kFusedMaxStages][kFusedMaxPPI];
+    __shared__ int s_np, s_lost;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = (int)blockIdx.x;
     const int j0 = (int)blockIdx.y * kFusedCols;
-    const bool report = rank == 0 && blockIdx.y == 0;
 
     // The next kernel on the stream may start now: it reads nothing this one
     // writes before its own griddepcontrol.wait.
     pdl_trigger();
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
-            mbar_init(&full[s], 2);   // base: W + x copies; LoRA: B copy + the v tiles
+            mbar_init(&full[s], 2);   // two arrivals: W + x, or B slices + v tiles, or the end
             mbar_init(&empty[s], 1);  // the MMAs that read the stage are done
         }
         mbar_init(&done, 1);
-        mbar_init(&red_full, 1);
+        mbar_init(&red_full, 1);  // the owner's arrival with the bytes it expects
+        mbar_init(&tab_ready, 1);
         mbar_init_fence();
         s_lost = 0;
     }
-    if (tid < 128) {
-        s_rowseg[tid] = -1;
-        s_rowpos[tid] = 0;
-    }
     __syncthreads();
-    // Rows of every segment with an adapter (segment metadata may be read
-    // before the wait).  Bad segments and ids are skipped and reported.
-    for (int s = tid; s < S; s += kFusedThreads) {
-        const int b = seg_ptr[s], e = seg_ptr[s + 1], a = idx[s];
-        if (b < 0 || e < b || e > T) {
-            if (report) set_error(err, kErrBadSegments);
-            continue;
+    // This CTA's k-blocks of H1 depend on its rank only: the first stages of
+    // W (and of x, when it may be read now) are requested before the rest of
+    // the set-up, which then overlaps their latency.
+    const int kb0 = (int)((long long)rank * kbt / C), kb1 = (int)((long long)(rank + 1) * kbt / C);
+    const int nbase = kb1 - kb0;  // >= 1: the host keeps CL <= kbt
+    const int pre = min(nst, nbase);
+    const bool x_early = P.x_early != 0;
+    uint8_t *const ring = align1024(dsm);
+    const uint32_t stage_bytes = P.stage_bytes;
+    auto stage = [&](int s) { return ring + (size_t)s * stage_bytes; };
+    const uint32_t xbytes = (uint32_t)npad * 128u;
+    const uint32_t abytes = fused_abytes(rp), vbytes = fused_vbytes(rp);
+    auto issue_w = [&](int q) {
+        const int s = q % nst;
+        mbar_arrive_expect_tx(&full[s], kFusedWBytes);
+        tma_load_2d(stage(s), &P.tmap_w, j0, (kb0 + q) * 64, &full[s]);
+        tma_load_2d(stage(s) + 8192, &P.tmap_w, j0 + 64, (kb0 + q) * 64, &full[s]);
+    };
+    auto issue_x = [&](int q) {
+        const int s = q % nst;
+        mbar_arrive_expect_tx(&full[s], xbytes);
+        tma_load_2d(stage(s) + kFusedXOff, &P.tmap_x, (kb0 + q) * 64, 0, &full[s]);
+    };
+    if (warp == 4 && lane == 0)
+        for (int q = 0; q < pre; ++q) {
+            issue_w(q);
+            if (x_early) issue_x(q);
         }
-        if (e == b || a == -1) continue;
-        if (a < -1 || a >= L) {
-            if (report) set_error(err, kErrBadIndex);
-            continue;
-        }
-        for (int p = b; p < e; ++p) {
-            const int row = perm ? perm[p] : p;
-            if (row < 0 || row >= T) {
-                if (report) set_error(err, kErrBadIndex);
-                continue;
-            }
-            s_rowseg[row] = s;
-            s_rowpos[row] = p;
-        }
-    }
-    __syncthreads();
     if (warp == 0) tmem_alloc(&s_tmem, P.tmem_cols);  // a converged warp, as the instruction needs
-    // LoRA pairs: (segment, 64-row block) with a row in both, one per row t
-    // that is its segment's first row in its block, in order of t
-    int first = 0;
-    if (tid < T) {
-        const int sg = s_rowseg[tid];
-        if (sg >= 0) {
-            first = 1;
-            for (int u = tid & ~63; u < tid; ++u)
-                if (s_rowseg[u] == sg) {
-                    first = 0;
-                    break;
-                }
-        }
-    }
-    const unsigned fb = warp < 4 ? __ballot_sync(0xffffffffu, first) : 0u;
-    if (warp < 4 && lane == 0) s_wcnt[warp] = __popc(fb);
-    __syncthreads();
-    if (first) {
-        int i = __popc(fb & ((1u << lane) - 1u));
-        for (int w = 0; w < warp; ++w) i += s_wcnt[w];
-        s_pseg[i] = s_rowseg[tid];
-        s_pblk[i] = tid >> 6;
-    }
-    if (tid == 0) s_npairs = s_wcnt[0] + s_wcnt[1] + s_wcnt[2] + s_wcnt[3];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const int npairs = s_npairs;
-    const int kb0 = (int)((long long)rank * kbt / C), kb1 = (int)((long long)(rank + 1) * kbt / C);
-    const int nbase = kb1 - kb0;  // >= 1: the host keeps CL <= kbt
-    const int nmine = npairs > rank ? (npairs - rank + C - 1) / C : 0;
-    const int total = nbase + nmine;
-    uint8_t *const ring = align1024(dsm);
-    auto stage = [&](int s) { return ring + (size_t)s * kFusedStage; };
 
-    if (warp == 4) {
-        // ---- producer warp: fills the ring in item order.  Lane 0 issues the
-        // TMA copies -- W k-blocks (weights, before the wait), x tiles (after
-        // it), the B tiles of this CTA's LoRA pairs -- and for a LoRA pair the
-        // whole warp writes the v tiles: rows of the pair's block that belong
-        // to its segment get scale * v, the others 0; K-major, 128-byte
-        // swizzle, as hi and lo 16-bit halves.  A stage is waited for by this
-        // warp alone and in order, so a parity wait never meets a barrier two
-        // phases ahead.
-        const uint32_t xbytes = (uint32_t)npad * 128u, bbytes = 2u * (uint32_t)r16 * 128u;
-        auto issue_w = [&](int q) {
-            const int s = q % nst;
-            mbar_arrive_expect_tx(&full[s], kFusedWBytes);
-            tma_load_2d(stage(s), &P.tmap_w, j0, (kb0 + q) * 64, &full[s]);
-            tma_load_2d(stage(s) + 8192, &P.tmap_w, j0 + 64, (kb0 + q) * 64, &full[s]);
-        };
-        auto issue_x = [&](int q) {
-            const int s = q % nst;
-            mbar_arrive_expect_tx(&full[s], xbytes);
-            tma_load_2d(stage(s) + kFusedXOff, &P.tmap_x, (kb0 + q) * 64, 0, &full[s]);
-        };
-        auto issue_b = [&](int q) {
-            const int s = q % nst;
-            const int a = idx[s_pseg[rank + (q - nbase) * C]];
-            mbar_arrive_expect_tx(&full[s], bbytes);
-            tma_load_3d(stage(s), &P.tmap_b, j0, 0, a, &full[s]);
-            tma_load_3d(stage(s) + r16 * 128, &P.tmap_b, j0 + 64, 0, a, &full[s]);
-        };
-        const int pre = min(nst, nbase);  // base items only (pre <= nbase)
-        if (lane == 0)
-            for (int q = 0; q < pre; ++q) issue_w(q);
-        pdl_wait();  // x may be written by an earlier kernel, v by the shrink
-        if (lane == 0)
-            for (int q = 0; q < pre; ++q) issue_x(q);
-        const float *const v = P.v;
-        const int cpr = r16 / 8;  // 16-byte chunks per v-tile row
-        for (int q = pre; q < total; ++q) {
-            const int s = q % nst;
-            if (q >= nst) {
-                // lane 0 waits for the MMAs of item q - nst; the warp follows
-                int ok = 1;
-                if (lane == 0) {
-                    const uint32_t ph = (uint32_t)(((q / nst) - 1) & 1);
-                    if (!mbar_wait(&empty[s], ph)) {
-                        set_error(err, kErrTimeout);
-                        ok = mbar_wait(&empty[s], ph) ? 1 : 0;
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            }
-            if (q < nbase) {
-                if (lane == 0) {
-                    issue_w(q);
-                    issue_x(q);
-                }
-                continue;
-            }
-            if (lane == 0) issue_b(q);
-            const int pr = rank + (q - nbase) * C;
-            const int sg = s_pseg[pr], blk = s_pblk[pr];
-            const int nrow = min(64, npad - 64 * blk);  // rows of the block's tile
-            uint8_t *hi = stage(s) + kFusedXOff, *lo = stage(s) + kFusedVloOff;
-            fence_proxy_async();  // the tensor cores' reads of this stage come first
-            for (int e = lane; e < nrow * cpr; e += 32) {
-                const int m = e / cpr, c = e - (e / cpr) * cpr;
-                const int t = 64 * blk + m;
-                const bool mine = t < T && s_rowseg[t] == sg;
-                const float *vr = v + (size_t)(mine ? s_rowpos[t] : 0) * r;
-                __align__(16) Tin hv[8], lv[8];
-#pragma unroll
-                for (int k8 = 0; k8 < 8; ++k8) {
-                    const int k = 8 * c + k8;
-                    const float f = (mine && k < r) ? scale * vr[k] : 0.f;
-                    hv[k8] = from_f<Tin>(f);
-                    lv[k8] = from_f<Tin>(f - to_f<Tin>(hv[k8]));
-                }
-                sts128(hi + sw128_offset(m, c), *reinterpret_cast<const uint4 *>(hv));
-                sts128(lo + sw128_offset(m, c), *reinterpret_cast<const uint4 *>(lv));
-            }
-            fence_proxy_async();  // generic-proxy writes -> the tensor cores
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[s]);
+    if (warp == 2 && P.lora) {
+        // ---- the pair table, read by a warp that is idle until the epilogue
+        pdl_wait();  // the table is written by the kernel just before
+        const int np = min(P.ptab[0], kFusedMaxPairs);
+        for (int k = lane; k < np; k += 32) {
+            s_pa[k] = P.ptab[1 + 2 * k];
+            s_pc[k] = P.ptab[2 + 2 * k];
         }
-    } else if (tid == 0) {
-        // ---- MMA issuer
+        if (lane == 0) s_np = np;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tab_ready);
+    } else if (warp == 4) {
+        // ---- producer: the whole warp takes the ring's phases in item order
+        // (base k-blocks, then this CTA's groups of pairs, then an end marker)
+        // and lane 0 issues the copies; the first stages were requested above.
+        // (All lanes wait: a warp whose other lanes sit in a suspended wait
+        // would hold up the issuing lane.)
+        bool stop = false;
+        auto wait_empty = [&](int q) {
+            if (q < nst) return true;
+            const int s = q % nst;
+            const uint32_t ph = (uint32_t)(((q / nst) - 1) & 1);
+            if (mbar_wait(&empty[s], ph)) return true;
+            set_error(err, kErrTimeout);
+            return mbar_wait(&empty[s], ph);
+        };
+        if (!x_early) {
+            pdl_wait();  // x may be written by the kernel just before
+            if (lane == 0)
+                for (int q = 0; q < pre; ++q) issue_x(q);
+        }
+        int q = pre;
+        for (; q < nbase; ++q) {
+            if (!wait_empty(q)) {
+                stop = true;
+                break;
+            }
+            // the stage's expected bytes first, then three lanes issue a copy each
+            const int s = q % nst;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], kFusedWBytes);
+                mbar_arrive_expect_tx(&full[s], xbytes);
+            }
+            __syncwarp();
+            if (lane < 2)
+                tma_load_2d(stage(s) + lane * 8192, &P.tmap_w, j0 + lane * 64, (kb0 + q) * 64,
+                            &full[s]);
+            else if (lane == 2)
+                tma_load_2d(stage(s) + kFusedXOff, &P.tmap_x, (kb0 + q) * 64, 0, &full[s]);
+            __syncwarp();
+        }
+        if (!stop && P.lora) {
+            pdl_wait();  // the v tiles: written by the kernel just before
+            if (!mbar_wait(&tab_ready, 0)) {
+                set_error(err, kErrTimeout);
+                stop = !mbar_wait(&tab_ready, 0);
+            }
+            const int np = stop ? 0 : s_np;
+            const int nitems = (np + ppi - 1) / ppi;
+            for (int it = rank; it < nitems; it += C, ++q) {
+                if (!wait_empty(q)) {
+                    stop = true;
+                    break;
+                }
+                // the stage's expected bytes first, then one lane per copy: lanes
+                // 2i and 2i + 1 the two halves of pair i's B slice, lane 31 the
+                // v tiles of all ppi pairs in one box (past the last pair: unused)
+                const int s = q % nst, k0 = it * ppi, n = min(ppi, np - k0);
+                uint8_t *const st = stage(s);
+                if (lane == 0) {
+                    s_kind[s] = kItemLora;
+                    s_cnt[s] = n;
+                    for (int i = 0; i < n; ++i) s_chunk[s][i] = s_pc[k0 + i];
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)n * abytes);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)ppi * vbytes);
+                }
+                __syncwarp();
+                if (lane < 2 * n) {
+                    const int i = lane >> 1, h = lane & 1;
+                    tma_load_3d(st + i * abytes + h * rp * 128, &P.tmap_b, j0 + h * 64, 0,
+                                s_pa[k0 + i], &full[s]);
+                } else if (lane == 31) {
+                    tma_load_2d(st + ppi * abytes, &P.tmap_v, 0, k0 * (int)(vbytes / 128u),
+                                &full[s]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!stop && wait_empty(q) && lane == 0) {
+            const int s = q % nst;
+            s_kind[s] = kItemEnd;
+            mbar_arrive(&full[s]);
+            mbar_arrive(&full[s]);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ---- MMA issuer: the whole warp waits, lane 0 issues
+        // one accumulator [128 columns of W][npad rows]
         const bool bf16 = std::is_same<Tin, __nv_bfloat16>::value;
-        const uint32_t id_base = idesc_f16_amn(bf16, kFusedCols, npad);
-        const uint32_t id_lora0 = idesc_f16_amn(bf16, kFusedCols, min(64, npad));
-        const uint32_t id_lora1 = idesc_f16_amn(bf16, kFusedCols, max(16, npad - 64));
+        const uint32_t idesc = idesc_f16_amn(bf16, kFusedCols, npad);
+        const uint32_t idesc16 = idesc_f16_amn(bf16, kFusedCols, 16);
+        const uint32_t lo_off = rp <= 32 ? 64u : 2048u;  // the lo half of a pair's v
         bool lost = false;
-        for (int q = 0; q < total; ++q) {
+        for (int q = 0;; ++q) {
             const int s = q % nst;
             const uint32_t ph = (uint32_t)((q / nst) & 1);
             if (!mbar_wait(&full[s], ph)) {
@@ -282,30 +442,39 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 lost = true;
                 if (!mbar_wait(&full[s], ph)) break;
             }
-            fence_proxy_async();
             tc_fence_after();
             const uint32_t sa = smem_addr(stage(s));
-            if (q < nbase) {
+            const int kind = q < nbase ? 0 : s_kind[s];
+            if (kind == kItemEnd) break;
+            if (lane == 0) {
+                if (kind == 0) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tmem, sw128_desc(sa + kk * 2048, 8192, 1024),
-                            sw128_desc(sa + kFusedXOff + kk * 32, 16, 1024), id_base,
-                            (q | kk) != 0);
-            } else {
-                // rows 64 blk .. of the accumulator: columns at a multiple of 64
-                const int blk = s_pblk[rank + (q - nbase) * C];
-                const uint32_t d = tmem + (uint32_t)(64 * blk);
-                const uint32_t id_lora = blk ? id_lora1 : id_lora0;
-                for (int h = 0; h < 2; ++h)
-                    for (int kk = 0; kk < r16 / 16; ++kk)
-                        mma_f16(d, sw128_desc(sa + kk * 2048, (uint32_t)r16 * 128u, 1024),
-                                sw128_desc(sa + (h ? kFusedVloOff : kFusedXOff) + kk * 32, 16, 1024),
-                                id_lora, 1);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(tmem, sw128_desc(sa + kk * 2048, 8192, 1024),
+                                sw128_desc(sa + kFusedXOff + kk * 32, 16, 1024), idesc,
+                                (q | kk) != 0);
+                } else {
+                    const int n = s_cnt[s];
+                    for (int i = 0; i < n; ++i) {
+                        const uint32_t d = tmem + 16u * (uint32_t)s_chunk[s][i];
+                        const uint32_t a = sa + i * abytes, v = sa + ppi * abytes + i * vbytes;
+                        for (int kk = 0; kk < rp / 16; ++kk) {
+                            const uint64_t ad = sw128_desc(a + kk * 2048, rp * 128, 1024);
+                            mma_f16(d, ad, sw128_desc(v + kk * 32, 16, 1024), idesc16, 1);
+                            mma_f16(d, ad, sw128_desc(v + lo_off + kk * 32, 16, 1024), idesc16,
+                                    1);
+                        }
+                    }
+                }
+                mma_commit(&empty[s]);
             }
-            mma_commit(&empty[s]);
+            __syncwarp();
         }
-        mma_commit(&done);
-        if (lost) s_lost = 1;
+        if (lane == 0) {
+            mma_commit(&done);
+            if (lost) s_lost = 1;
+        }
+        __syncwarp();
     }
 
     // ---- epilogue: warps 0-3, thread tid = TMEM lane tid = column j0 + tid
@@ -325,7 +494,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     __syncwarp();  // the aligned TMEM loads below need the whole warp
     // The accumulator is read in groups of 32 columns (rows t), 32 columns
     // per tcgen05.ld at multiples of 32; columns past npad are allocated and
-    // hold nothing used.
+    // hold nothing used.  Every group holds at least one row t < T.
     const int ngrp = (npad + 31) / 32;
     const int nown = rank < ngrp ? (ngrp - rank + C - 1) / C : 0;
     const int nown_max = (ngrp + C - 1) / C;
@@ -347,57 +516,76 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
     } else {
         // Partials of group g go to CTA g % C, slot (rank, g / C): eight
-        // [128][4] float quads, so that 32 lanes store 512 contiguous bytes.
+        // [128][4] float quads, so that 32 lanes access 512 contiguous bytes;
+        // only the quads that hold rows t < T are sent.  Each CTA first
+        // stages its partials in its own shared memory, then one thread
+        // sends every group with one bulk copy into its owner's ring.
         float *const recv = reinterpret_cast<float *>(ring);
-        auto slot = [&](int src, int lg, int q) {
-            return recv + ((size_t)((src * nown_max + lg) * 8 + q) * 128 + tid) * 4;
-        };
-        if (tid == 0 && nown > 0) mbar_arrive_expect_tx(&red_full, (uint32_t)(C * nown) * 16384u);
-        // every CTA's MMAs are done and its ring is idle: peers may write into it
-        cluster_sync();
-        lost = lost || s_lost != 0;
+        float *const stg = recv + (size_t)C * nown_max * 4096;
+        auto nq_of = [&](int g) { return min(8, (T - g * 32 + 3) >> 2); };
         if (tid < 128) {
             for (int g = 0; g < ngrp; ++g) {
                 float f[32];
                 tmem_ld32(lane_addr + (uint32_t)(g * 32), f);
-                const uint32_t owner = (uint32_t)(g % C);
-                const uint32_t rbar = peer_addr(&red_full, owner);
+                const int nq = nq_of(g);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    st_async4(peer_addr(slot(rank, g / C, q), owner), f[4 * q], f[4 * q + 1],
-                              f[4 * q + 2], f[4 * q + 3], rbar);
+                    if (q < nq)
+                        sts128(stg + ((size_t)(g * 8 + q) * 128 + tid) * 4, f[4 * q], f[4 * q + 1],
+                               f[4 * q + 2], f[4 * q + 3]);
             }
-            if (nown > 0) {
-                if (!mbar_wait_cluster(&red_full, 0)) {
-                    set_error(err, kErrTimeout);
-                    lost = true;
-                    mbar_wait_cluster(&red_full, 0);
-                }
-                for (int lg = 0; lg < nown; ++lg) {
-                    const int g = rank + lg * C;
+            fence_proxy_async();  // the staged partials: read by the copies below
+        }
+        if (tid == 0 && nown > 0) {
+            uint32_t bytes = 0;
+            for (int lg = 0; lg < nown; ++lg) bytes += (uint32_t)(C * nq_of(rank + lg * C)) * 2048u;
+            mbar_arrive_expect_tx(&red_full, bytes);
+        }
+        // every CTA's MMAs are done, its ring is idle (peers may write into
+        // it), its partials are staged and its expected bytes are set
+        cluster_sync();
+        lost = lost || s_lost != 0;
+        if (tid == 0)
+            for (int g = 0; g < ngrp; ++g) {
+                const uint32_t o = (uint32_t)(g % C);
+                float *const dst = recv + (size_t)(rank * nown_max + g / C) * 4096;
+                bulk_s2peer(peer_addr(dst, o), stg + (size_t)g * 4096, (uint32_t)nq_of(g) * 2048u,
+                            peer_addr(&red_full, o));
+            }
+        if (tid < 128 && nown > 0) {
+            if (!mbar_wait(&red_full, 0)) {
+                set_error(err, kErrTimeout);
+                lost = true;
+                mbar_wait(&red_full, 0);
+            }
+            for (int lg = 0; lg < nown; ++lg) {
+                const int g = rank + lg * C;
+                const int nq = nq_of(g);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int src = 0; src < C; ++src) {
-                            const uint4 u = lds128(slot(src, lg, q));
-                            acc[0] += __uint_as_float(u.x);
-                            acc[1] += __uint_as_float(u.y);
-                            acc[2] += __uint_as_float(u.z);
-                            acc[3] += __uint_as_float(u.w);
-                        }
-                        if (!lost && j < H2) {
+                for (int q = 0; q < 8; ++q) {
+                    if (q >= nq) break;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int src = 0; src < C; ++src) {
+                        const uint4 u =
+                            lds128(recv + ((size_t)((src * nown_max + lg) * 8 + q) * 128 + tid) * 4);
+                        acc[0] += __uint_as_float(u.x);
+                        acc[1] += __uint_as_float(u.y);
+                        acc[2] += __uint_as_float(u.z);
+                        acc[3] += __uint_as_float(u.w);
+                    }
+                    if (!lost && j < H2) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int t = g * 32 + 4 * q + e;
-                                if (t < T) gY[(size_t)t * H2 + j] = from_f<Ty>(acc[e]);
-                            }
+                        for (int e = 0; e < 4; ++e) {
+                            const int t = g * 32 + 4 * q + e;
+                            if (t < T) gY[(size_t)t * H2 + j] = from_f<Ty>(acc[e]);
                         }
                     }
                 }
             }
         }
-        // No closing cluster barrier: each CTA has waited for every push
-        // addressed to it before it gets here.
+        // No CTA leaves while a copy it sent may still read its staging area
+        // (every owner has received everything when it arrives here).
+        cluster_sync();
     }
     tc_fence_before();
     __syncthreads();
@@ -413,22 +601,23 @@ int fused_launch_t(const FusedArgs &g) {
     FusedParams p;
     memset(&p, 0, sizeof p);
     p.y = g.y;
-    p.v = g.v;
-    p.perm = g.perm;
-    p.seg_ptr = g.seg_ptr;
-    p.idx = g.idx;
     p.err = g.err;
-    p.S = g.S;
     p.T = g.T;
-    p.L = g.L;
     p.H1 = g.H1;
     p.H2 = g.H2;
-    p.r = g.r;
-    p.r16 = (g.r + 15) / 16 * 16;
+    p.rp = fused_rp(g.r);
     p.npad = (g.T + 15) / 16 * 16;
+    // x may be read before the wait when the shrink was launched before this
+    // kernel: the shrink waits for the kernel before it (which may write x)
+    // before it lets the next kernels start
+    p.x_early = g.x_early ? 1 : 0;
+    p.lora = g.prep ? 1 : 0;
     p.kbt = (g.H1 + 63) / 64;
-    p.scale = g.scale;
     p.tmem_cols = p.npad <= 32 ? 32u : p.npad <= 64 ? 64u : 128u;
+    const uint32_t abytes = fused_abytes(p.rp), vbytes = fused_vbytes(p.rp);
+    p.stage_bytes = std::max(kFusedXOff + (uint32_t)p.npad * 128u, abytes + vbytes);  // 1024 | both
+    p.ppi = (int)std::min<uint32_t>((uint32_t)std::min(kFusedMaxPPI, (int)g.T),
+                                    p.stage_bytes / (abytes + vbytes));
     const cuuint64_t es = 2;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)g.H2, (cuuint64_t)g.H1};
@@ -447,9 +636,20 @@ int fused_launch_t(const FusedArgs &g) {
     {
         const cuuint64_t dims[3] = {(cuuint64_t)g.H2, (cuuint64_t)g.r, (cuuint64_t)g.L};
         const cuuint64_t strides[2] = {(cuuint64_t)g.H2 * es, (cuuint64_t)g.r * g.H2 * es};
-        const cuuint32_t box[3] = {64, (cuuint32_t)p.r16, 1};
+        const cuuint32_t box[3] = {64, (cuuint32_t)p.rp, 1};  // rows r .. rp-1 read as 0
         if (!tmap_encode(&p.tmap_b, bf16, 3, g.B, dims, strides, box, true))
             return (int)cudaErrorInvalidValue;
+    }
+    const int ntile = fused_ntile(p.rp);
+    uint8_t *const vt = g.prep ? static_cast<uint8_t *>(g.prep) + fused_ptab_bytes(g.T) : nullptr;
+    if (g.prep) {
+        // rows past the T pairs' tiles read as 0 (a box may run past the last pair)
+        const cuuint64_t dims[2] = {64, (cuuint64_t)g.T * ntile * 16};
+        const cuuint64_t strides[1] = {128};
+        const cuuint32_t box[2] = {64, (cuuint32_t)(p.ppi * ntile * 16)};
+        if (!tmap_encode(&p.tmap_v, bf16, 2, vt, dims, strides, box, true))
+            return (int)cudaErrorInvalidValue;
+        p.ptab = static_cast<const int32_t *>(g.prep);
     }
     // Cluster size: the split of H1 that keeps the most SMs busy over whole
     // waves of one CTA per SM (ties: the smaller split), each CTA with at
@@ -470,23 +670,55 @@ int fused_launch_t(const FusedArgs &g) {
     p.cl = best;
     auto kernel = sgmv_fused_kernel<Tin, Ty>;
     // ring stages: what the per-block limit leaves beside the kernel's static
-    // shared memory and the 1024-byte alignment slack
+    // shared memory and the 1024-byte alignment slack; the exchange of the
+    // partials reuses the ring and needs (CL * ceil(groups / CL) + groups) *
+    // 16 KB of it
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return (int)e;
     const size_t smem_max = 227u * 1024u;
-    if (smem_max < fa.sharedSizeBytes + 1024u + kFusedStage) return (int)cudaErrorInvalidValue;
     p.nst = (int)std::min<size_t>(kFusedMaxStages,
-                                  (smem_max - fa.sharedSizeBytes - 1024u) / kFusedStage);
-    const size_t smem = (size_t)p.nst * kFusedStage + 1024u;
+                                  (smem_max - fa.sharedSizeBytes - 1024u) / p.stage_bytes);
+    const int ngrp = (p.npad + 31) / 32;
+    const size_t red_bytes = ((size_t)p.cl * ((ngrp + p.cl - 1) / p.cl) + ngrp) * 16384u;
+    if (p.nst < 2 || (size_t)p.nst * p.stage_bytes < red_bytes) return (int)cudaErrorInvalidValue;
+    const size_t smem = (size_t)p.nst * p.stage_bytes + 1024u;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
+    cudaLaunchAttribute attrs[2];
+    // the work list and v tiles first (after the shrink)
+    if (g.prep) {
+        PrepParams vp;
+        vp.v = g.v;
+        vp.perm = g.perm;
+        vp.seg_ptr = g.seg_ptr;
+        vp.idx = g.idx;
+        vp.err = g.err;
+        vp.ptab = static_cast<int32_t *>(g.prep);
+        vp.vt = vt;
+        vp.S = g.S;
+        vp.T = g.T;
+        vp.L = g.L;
+        vp.r = g.r;
+        vp.rp = p.rp;
+        vp.early = g.x_early ? 1 : 0;
+        vp.scale = g.scale;
+        cudaLaunchConfig_t vc = {};
+        vc.gridDim = dim3((unsigned)std::min(kPrepMaxCtas, (int)g.T), 1, 1);
+        vc.blockDim = dim3(kPrepThreads, 1, 1);
+        vc.stream = g.stream;
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        vc.attrs = attrs;
+        vc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&vc, sgmv_fused_prep_kernel<Tin>, vp);
+        if (e != cudaSuccess) return (int)e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.cl, (unsigned)ntiles, 1);
     cfg.blockDim = dim3(kFusedThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = g.stream;
-    cudaLaunchAttribute attrs[2];
     int na = 0;
     if (p.cl > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
@@ -513,6 +745,11 @@ int fused_launch_in(const FusedArgs &g) {
 }
 
 }  // namespace
+
+size_t fused_prep_bytes(int32_t T, int32_t r) {
+    if (T <= 0 || r <= 0) return 0;
+    return fused_ptab_bytes(T) + (size_t)T * fused_vbytes(fused_rp(r));
+}
 
 int fused_launch(const FusedArgs &g) {
     return g.in_dtype == 0 ? fused_launch_in<__half>(g) : fused_launch_in<__nv_bfloat16>(g);

@@ -214,7 +214,8 @@ struct FusedArgs {
     const void *x;
     const void *W;
     const void *B;
-    const float *v;
+    const float *v;      // the shrink's output [T][r] fp32, or nullptr (no segments)
+    void *prep;          // workspace for the pair table and v tiles (fused_prep_bytes), or nullptr
     const int32_t *perm;
     const int32_t *seg_ptr;
     const int32_t *idx;
@@ -223,8 +224,13 @@ struct FusedArgs {
     float scale;
     int in_dtype, y_dtype;
     int32_t nsm;
+    bool x_early;        // a kernel that waits for x's producer was launched just before
     cudaStream_t stream;
 };
+
+// Bytes of the fused layer's pair table and v tiles (a bound over any
+// segmentation of T rows).
+size_t fused_prep_bytes(int32_t T, int32_t r);
 
 // Rows the fused kernel takes (the N of its base MMAs) and the largest rank.
 constexpr int kFusedMaxT = 128;

@@ -254,8 +254,8 @@ def sgmv_fused_linear_lora(y, x, W, A, B, seg_ptr, idx, scale=1.0, perm=None, S=
                            workspace=None):
     """y = x @ W + scale * SGMV delta (the LoRA layer in one pass), written
     into y; returns y.  ``workspace`` (uint8 device tensor of at least
-    sgmv_fused_workspace_bytes(T, r) bytes) holds v; one is allocated when
-    None."""
+    sgmv_fused_workspace_bytes(T, r) bytes) holds v and its tiles; one is
+    allocated when None."""
     T, H1 = x.shape
     L, _, r = A.shape
     H2 = y.shape[1]

@@ -225,6 +225,10 @@ def test_fused_linear_lora_rejects_bad_arguments(lib):
     assert call(wsb=16) == 6
     assert call(ws=MIS) == 3
     assert call(T=0, x=None, y=None) == 0
-    assert lib.sgmv_fused_workspace_bytes(128, 16) == 128 * 16 * 4
-    assert lib.sgmv_fused_workspace_bytes(3, 5) == 256
+    # v [T][r] fp32, the pair table (1 + 2T int32) and T pairs' v tiles
+    # ([16][64] 16-bit, two of them for r > 32), each part 256-byte rounded
+    assert lib.sgmv_fused_workspace_bytes(128, 16) == 128 * 16 * 4 + 1280 + 128 * 2048
+    assert lib.sgmv_fused_workspace_bytes(3, 5) == 256 + 256 + 3 * 2048
+    assert lib.sgmv_fused_workspace_bytes(100, 32) == 100 * 32 * 4 + 1024 + 100 * 2048
+    assert lib.sgmv_fused_workspace_bytes(7, 64) == 7 * 64 * 4 + 256 + 7 * 4096
     assert lib.sgmv_fused_workspace_bytes(0, 16) == 0
