@@ -1008,7 +1008,7 @@ def fused_layer_point(sgmv, wl, dev, H1, H2, T, seed, iters, flush, l2, peak):
     g = torch.Generator().manual_seed(seed)
     ra = torch.randperm(L, generator=g)[:T].to(torch.int32).to(dev)
     perm, seg_ptr, idx, _ = sgmv.sgmv_build_segments_device(ra, L)
-    ws = torch.empty(sgmv.sgmv_fused_workspace_bytes(T, r), dtype=torch.uint8, device=dev)
+    ws = torch.empty(sgmv.sgmv_fused_workspace_bytes(T, H2, r), dtype=torch.uint8, device=dev)
 
     def base(st):
         X, A, B, W, y = st

@@ -237,12 +237,13 @@ int sgmv_apply_noalloc(void *y, int y_dtype, const void *x, const void *A, const
                        int32_t L, int32_t H1, int32_t H2, int32_t r, void *stream);
 
 /*
- * Bytes of device workspace sgmv_fused_linear_lora needs: v [T][r] fp32, then
- * the 16-bit v tiles of the adapter terms (at most ceil(T / (32 / rp)) tiles,
- * or 2T for rp = 64, of [round16(T)][64] elements each, rp = r rounded up to
- * 16, 32 or 64).
+ * Bytes of device workspace sgmv_fused_linear_lora needs: v [T][r] fp32, the
+ * pair table and the 16-bit v tiles of the adapter terms (at most T tiles of
+ * [16][64] elements, two per pair for r > 32), and an fp32 scratch area for
+ * the partial sums of tiles split across a cluster (at most 8 x
+ * ceil(H2 / 128) x round32(T) x 128 floats); each part 256-byte aligned.
  */
-size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r);
+size_t sgmv_fused_workspace_bytes(int32_t T, int32_t H2, int32_t r);
 
 /*
  * The whole LoRA layer in one pass over its weights: the base linear layer and
@@ -259,9 +260,8 @@ size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r);
  *   W  [H1][H2]  device, in_dtype (f16 / bf16), row-major
  *   x, A, B, perm, seg_ptr, idx, S, L, r as for sgmv_apply; y as for
  *   sgmv_apply but written, not updated.
- *   workspace  device, >= sgmv_fused_workspace_bytes(T, r) bytes, 16-byte
- *              aligned (holds v and its tiles between the kernels); may be NULL
- *              when S == 0.
+ *   workspace  device, >= sgmv_fused_workspace_bytes(T, H2, r) bytes, 16-byte
+ *              aligned (holds v, its tiles and partial sums between the kernels).
  * Decode batches: 1 <= T <= 128 rows and r <= 64 (SGMV_ERR_UNSUPPORTED
  * otherwise).  Three kernels on `stream` (one when S == 0): the CUDA-core
  * shrink writes v; a small kernel lays scale * v out as block-diagonal 16-bit

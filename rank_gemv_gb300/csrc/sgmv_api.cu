@@ -733,13 +733,13 @@ int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, co
                                        B_src, b_bytes, cudaMemcpyDefault, s));
 }
 
-// Workspace of the fused layer: v [T][r] fp32, then the pair table and the v
-// tiles, each part 256-byte aligned.
+// Workspace of the fused layer: v [T][r] fp32, the pair table and the v tiles,
+// then the fp32 partials of split tiles; each part 256-byte aligned.
 size_t fused_v_bytes(int32_t T, int32_t r) { return ((size_t)T * (size_t)r * 4u + 255u) / 256u * 256u; }
 
-size_t sgmv_fused_workspace_bytes(int32_t T, int32_t r) {
-    if (T <= 0 || r <= 0) return 0;
-    return fused_v_bytes(T, r) + fused_prep_bytes(T, r);
+size_t sgmv_fused_workspace_bytes(int32_t T, int32_t H2, int32_t r) {
+    if (T <= 0 || H2 <= 0 || r <= 0) return 0;
+    return fused_v_bytes(T, r) + fused_prep_bytes(T, r) + fused_part_bytes(T, H2);
 }
 
 int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, const void *A,
@@ -759,11 +759,9 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
     if (!y || !x || !W || !A || !B) return SGMV_ERR_INVALID_ARG;
     if (!aligned16(y) || !aligned16(x) || !aligned16(W) || !aligned16(A) || !aligned16(B))
         return SGMV_ERR_ALIGNMENT;
-    if (S > 0) {
-        if (!workspace || workspace_bytes < sgmv_fused_workspace_bytes(T, r))
-            return SGMV_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return SGMV_ERR_ALIGNMENT;
-    }
+    if (!workspace || workspace_bytes < sgmv_fused_workspace_bytes(T, H2, r))
+        return SGMV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SGMV_ERR_ALIGNMENT;
     int *err = error_word();
     if (!err) return SGMV_ERR_CUDA;
     int launches = 0;
@@ -794,6 +792,8 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
     g.in_dtype = in_dtype;
     g.y_dtype = y_dtype;
     g.prep = S > 0 ? static_cast<uint8_t *>(workspace) + fused_v_bytes(T, r) : nullptr;
+    g.part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + fused_v_bytes(T, r) +
+                                       fused_prep_bytes(T, r));
     g.nsm = num_sms();
     g.x_early = launches > 0;
     g.stream = static_cast<cudaStream_t>(stream);

@@ -41,9 +41,10 @@
 // Decomposition of the fused kernel: one tile of 128 columns per cluster of
 // CL CTAs; CTA `rank` takes an even share of H1's 64-column k-blocks and
 // every CL-th group of pairs, so all CTAs stream about the same bytes.  The
-// partial accumulators are exchanged through distributed shared memory (each
-// CTA owns every CL-th group of 32 rows of the tile) and summed in rank
-// order: deterministic.
+// partial accumulators meet in an fp32 scratch area of the workspace (in L2:
+// distributed shared memory moves them several times slower on this part);
+// after a cluster barrier each CTA sums, in rank order, every CL-th group of
+// 32 rows of the tile: deterministic.
 //
 // Warps of the fused kernel: 0-3 read the accumulator (one TMEM lane, i.e.
 // one column j, per thread) and write y; before that, warp 3 issues the MMAs
@@ -76,6 +77,7 @@ constexpr int kFusedMaxPairs = 128;           // at most T pairs, T <= 128
 constexpr int kFusedMaxPPI = 8;               // pairs per ring stage
 constexpr int kPrepThreads = 256;
 constexpr int kPrepMaxCtas = 32;
+constexpr int kFusedMaxCl = 8;                // CTAs per cluster (portable limit)
 
 __host__ __device__ inline int fused_rp(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
 // 16 x 64 tiles of v per pair: hi and lo share one tile for rp <= 32
@@ -246,6 +248,7 @@ struct FusedParams {
     CUtensorMap tmap_b;   // B as [L][r][H2], box {64, rp, 1}
     CUtensorMap tmap_v;   // v tiles as [T * ntile * 16][64], box {64, ppi * ntile * 16}
     void *y;
+    float *part;      // [tiles][CL][npad][128] fp32 partials (CL > 1)
     const int32_t *ptab;
     int *err;
     int32_t T, H1, H2;
@@ -271,8 +274,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     int *const err = P.err;
 
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t full[kFusedMaxStages], empty[kFusedMaxStages], done, red_full,
-        tab_ready;
+    __shared__ __align__(8) uint64_t full[kFusedMaxStages], empty[kFusedMaxStages], done, tab_ready;
     __shared__ int s_pa[kFusedMaxPairs], s_pc[kFusedMaxPairs];  // pair table
     __shared__ int s_kind[kFusedMaxStages], s_cnt[kFusedMaxStages];
     __shared__ int s_chunk[kFusedMaxStages][kFusedMaxPPI];
@@ -291,7 +293,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             mbar_init(&empty[s], 1);  // the MMAs that read the stage are done
         }
         mbar_init(&done, 1);
-        mbar_init(&red_full, 1);  // the owner's arrival with the bytes it expects
         mbar_init(&tab_ready, 1);
         mbar_init_fence();
         s_lost = 0;
@@ -496,8 +497,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // per tcgen05.ld at multiples of 32; columns past npad are allocated and
     // hold nothing used.  Every group holds at least one row t < T.
     const int ngrp = (npad + 31) / 32;
-    const int nown = rank < ngrp ? (ngrp - rank + C - 1) / C : 0;
-    const int nown_max = (ngrp + C - 1) / C;
     if (C == 1) {
         __syncthreads();  // s_lost
         lost = lost || s_lost != 0;
@@ -515,77 +514,65 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             }
         }
     } else {
-        // Partials of group g go to CTA g % C, slot (rank, g / C): eight
-        // [128][4] float quads, so that 32 lanes access 512 contiguous bytes;
-        // only the quads that hold rows t < T are sent.  Each CTA first
-        // stages its partials in its own shared memory, then one thread
-        // sends every group with one bulk copy into its owner's ring.
-        float *const recv = reinterpret_cast<float *>(ring);
-        float *const stg = recv + (size_t)C * nown_max * 4096;
+        // This CTA's partials into the tile's scratch slot `rank`, as [group]
+        // [8 quads of rows][128 columns][4 rows] so that a warp moves 512
+        // contiguous bytes per access (quads holding rows t < T only); a
+        // cluster barrier; then groups g = rank, rank + CL, ... summed over
+        // the CL slots in rank order, with every load of a group in flight
+        // at once (the loads are latency-bound, not bandwidth-bound).
+        float4 *const part = reinterpret_cast<float4 *>(P.part) + (size_t)blockIdx.y * C * ngrp * 1024;
         auto nq_of = [&](int g) { return min(8, (T - g * 32 + 3) >> 2); };
         if (tid < 128) {
             for (int g = 0; g < ngrp; ++g) {
                 float f[32];
                 tmem_ld32(lane_addr + (uint32_t)(g * 32), f);
                 const int nq = nq_of(g);
+                float4 *const dst = part + ((size_t)rank * ngrp + g) * 1024 + tid;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    if (q < nq)
-                        sts128(stg + ((size_t)(g * 8 + q) * 128 + tid) * 4, f[4 * q], f[4 * q + 1],
-                               f[4 * q + 2], f[4 * q + 3]);
+                    if (q < nq) dst[q * 128] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
             }
-            fence_proxy_async();  // the staged partials: read by the copies below
         }
-        if (tid == 0 && nown > 0) {
-            uint32_t bytes = 0;
-            for (int lg = 0; lg < nown; ++lg) bytes += (uint32_t)(C * nq_of(rank + lg * C)) * 2048u;
-            mbar_arrive_expect_tx(&red_full, bytes);
-        }
-        // every CTA's MMAs are done, its ring is idle (peers may write into
-        // it), its partials are staged and its expected bytes are set
+        // release / acquire at cluster scope: the partials are visible after it
         cluster_sync();
         lost = lost || s_lost != 0;
-        if (tid == 0)
-            for (int g = 0; g < ngrp; ++g) {
-                const uint32_t o = (uint32_t)(g % C);
-                float *const dst = recv + (size_t)(rank * nown_max + g / C) * 4096;
-                bulk_s2peer(peer_addr(dst, o), stg + (size_t)g * 4096, (uint32_t)nq_of(g) * 2048u,
-                            peer_addr(&red_full, o));
-            }
-        if (tid < 128 && nown > 0) {
-            if (!mbar_wait(&red_full, 0)) {
-                set_error(err, kErrTimeout);
-                lost = true;
-                mbar_wait(&red_full, 0);
-            }
-            for (int lg = 0; lg < nown; ++lg) {
-                const int g = rank + lg * C;
+        if (tid < 128)
+            for (int g = rank; g < ngrp; g += C) {
                 const int nq = nq_of(g);
+                float4 acc[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (q >= nq) break;
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int src = 0; src < C; ++src) {
-                        const uint4 u =
-                            lds128(recv + ((size_t)((src * nown_max + lg) * 8 + q) * 128 + tid) * 4);
-                        acc[0] += __uint_as_float(u.x);
-                        acc[1] += __uint_as_float(u.y);
-                        acc[2] += __uint_as_float(u.z);
-                        acc[3] += __uint_as_float(u.w);
-                    }
-                    if (!lost && j < H2) {
+                for (int q = 0; q < 8; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int s0 = 0; s0 < C; s0 += 4) {
+                    float4 u[4][8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (s0 + i < C && q < nq)
+                                u[i][q] = __ldcg(part + ((size_t)(s0 + i) * ngrp + g) * 1024 + q * 128 + tid);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (s0 + i < C && q < nq) {
+                                acc[q].x += u[i][q].x;
+                                acc[q].y += u[i][q].y;
+                                acc[q].z += u[i][q].z;
+                                acc[q].w += u[i][q].w;
+                            }
+                }
+                if (!lost && j < H2) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float a4[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int t = g * 32 + 4 * q + e;
-                            if (t < T) gY[(size_t)t * H2 + j] = from_f<Ty>(acc[e]);
+                            if (t < T) gY[(size_t)t * H2 + j] = from_f<Ty>(a4[e]);
                         }
                     }
                 }
             }
-        }
-        // No CTA leaves while a copy it sent may still read its staging area
-        // (every owner has received everything when it arrives here).
-        cluster_sync();
     }
     tc_fence_before();
     __syncthreads();
@@ -658,7 +645,7 @@ int fused_launch_t(const FusedArgs &g) {
     const int nsm = std::max(1, g.nsm);
     int best = 1;
     double best_eff = -1.0;
-    for (int c = 1; c <= std::min(8, p.kbt); ++c) {
+    for (int c = 1; c <= std::min(kFusedMaxCl, p.kbt); ++c) {
         const long long ctas = (long long)ntiles * c;
         const long long waves = (ctas + nsm - 1) / nsm;
         const double eff = (double)ctas / (double)(waves * nsm);
@@ -668,20 +655,17 @@ int fused_launch_t(const FusedArgs &g) {
         }
     }
     p.cl = best;
+    p.part = g.part;
     auto kernel = sgmv_fused_kernel<Tin, Ty>;
     // ring stages: what the per-block limit leaves beside the kernel's static
-    // shared memory and the 1024-byte alignment slack; the exchange of the
-    // partials reuses the ring and needs (CL * ceil(groups / CL) + groups) *
-    // 16 KB of it
+    // shared memory and the 1024-byte alignment slack
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return (int)e;
     const size_t smem_max = 227u * 1024u;
     p.nst = (int)std::min<size_t>(kFusedMaxStages,
                                   (smem_max - fa.sharedSizeBytes - 1024u) / p.stage_bytes);
-    const int ngrp = (p.npad + 31) / 32;
-    const size_t red_bytes = ((size_t)p.cl * ((ngrp + p.cl - 1) / p.cl) + ngrp) * 16384u;
-    if (p.nst < 2 || (size_t)p.nst * p.stage_bytes < red_bytes) return (int)cudaErrorInvalidValue;
+    if (p.nst < 2) return (int)cudaErrorInvalidValue;
     const size_t smem = (size_t)p.nst * p.stage_bytes + 1024u;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return (int)e;
@@ -749,6 +733,12 @@ int fused_launch_in(const FusedArgs &g) {
 size_t fused_prep_bytes(int32_t T, int32_t r) {
     if (T <= 0 || r <= 0) return 0;
     return fused_ptab_bytes(T) + (size_t)T * fused_vbytes(fused_rp(r));
+}
+
+size_t fused_part_bytes(int32_t T, int32_t H2) {
+    if (T <= 0 || H2 <= 0) return 0;
+    const size_t tiles = ((size_t)H2 + kFusedCols - 1) / kFusedCols;
+    return tiles * kFusedMaxCl * (size_t)((T + 31) / 32 * 32) * kFusedCols * 4u;
 }
 
 int fused_launch(const FusedArgs &g) {

@@ -216,6 +216,7 @@ struct FusedArgs {
     const void *B;
     const float *v;      // the shrink's output [T][r] fp32, or nullptr (no segments)
     void *prep;          // workspace for the pair table and v tiles (fused_prep_bytes), or nullptr
+    float *part;         // workspace for the split partials (fused_part_bytes)
     const int32_t *perm;
     const int32_t *seg_ptr;
     const int32_t *idx;
@@ -231,6 +232,8 @@ struct FusedArgs {
 // Bytes of the fused layer's pair table and v tiles (a bound over any
 // segmentation of T rows).
 size_t fused_prep_bytes(int32_t T, int32_t r);
+// Bytes of the fused layer's fp32 scratch for the partial sums of split tiles.
+size_t fused_part_bytes(int32_t T, int32_t H2);
 
 // Rows the fused kernel takes (the N of its base MMAs) and the largest rank.
 constexpr int kFusedMaxT = 128;

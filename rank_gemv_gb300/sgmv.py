@@ -45,7 +45,7 @@ SIGNATURES = {
                                _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "sgmv_apply_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp,
                                   _i32, _i32, _i32, _i32, _i32, _vp]),
-    "sgmv_fused_workspace_bytes": (_sz, [_i32, _i32]),
+    "sgmv_fused_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "sgmv_fused_linear_lora": (_int, [_vp, _int, _vp, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp,
                                       _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
     "sgmv_load_adapter": (_int, [_vp, _vp, _int, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
@@ -246,16 +246,16 @@ def sgmv_apply_noalloc(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_h
     return y
 
 
-def sgmv_fused_workspace_bytes(T: int, r: int) -> int:
-    return int(load_library().sgmv_fused_workspace_bytes(T, r))
+def sgmv_fused_workspace_bytes(T: int, H2: int, r: int) -> int:
+    return int(load_library().sgmv_fused_workspace_bytes(T, H2, r))
 
 
 def sgmv_fused_linear_lora(y, x, W, A, B, seg_ptr, idx, scale=1.0, perm=None, S=None,
                            workspace=None):
     """y = x @ W + scale * SGMV delta (the LoRA layer in one pass), written
     into y; returns y.  ``workspace`` (uint8 device tensor of at least
-    sgmv_fused_workspace_bytes(T, r) bytes) holds v and its tiles; one is
-    allocated when None."""
+    sgmv_fused_workspace_bytes(T, H2, r) bytes) holds v, its tiles and the
+    partial sums; one is allocated when None."""
     T, H1 = x.shape
     L, _, r = A.shape
     H2 = y.shape[1]
@@ -264,8 +264,8 @@ def sgmv_fused_linear_lora(y, x, W, A, B, seg_ptr, idx, scale=1.0, perm=None, S=
     if W.dtype != x.dtype:
         raise TypeError("W and x types differ")
     nseg = _nseg(idx, S) if idx is not None else 0
-    if workspace is None and nseg > 0:
-        workspace = torch.empty(sgmv_fused_workspace_bytes(T, r), dtype=torch.uint8,
+    if workspace is None and T > 0:
+        workspace = torch.empty(sgmv_fused_workspace_bytes(T, H2, r), dtype=torch.uint8,
                                 device=x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load_library().sgmv_fused_linear_lora(

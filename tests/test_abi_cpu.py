@@ -221,14 +221,19 @@ def test_fused_linear_lora_rejects_bad_arguments(lib):
     assert call(y=MIS) == 3
     assert call(in_dt=2) == 1
     assert call(y_dt=4) == 1
-    assert call(ws=None, wsb=0) == 6   # v needs the workspace
+    assert call(ws=None, wsb=0) == 6   # v and the partials need the workspace
+    assert call(ws=None, wsb=0, S=0) == 6
     assert call(wsb=16) == 6
     assert call(ws=MIS) == 3
     assert call(T=0, x=None, y=None) == 0
-    # v [T][r] fp32, the pair table (1 + 2T int32) and T pairs' v tiles
-    # ([16][64] 16-bit, two of them for r > 32), each part 256-byte rounded
-    assert lib.sgmv_fused_workspace_bytes(128, 16) == 128 * 16 * 4 + 1280 + 128 * 2048
-    assert lib.sgmv_fused_workspace_bytes(3, 5) == 256 + 256 + 3 * 2048
-    assert lib.sgmv_fused_workspace_bytes(100, 32) == 100 * 32 * 4 + 1024 + 100 * 2048
-    assert lib.sgmv_fused_workspace_bytes(7, 64) == 7 * 64 * 4 + 256 + 7 * 4096
-    assert lib.sgmv_fused_workspace_bytes(0, 16) == 0
+    # v [T][r] fp32, the pair table (1 + 2T int32), T pairs' v tiles ([16][64]
+    # 16-bit, two of them for r > 32) and the split partials (8 x 128-column
+    # tiles x round32(T) x 128 fp32), each part 256-byte rounded
+    def part(T, H2):
+        return 8 * ((H2 + 127) // 128) * ((T + 31) // 32 * 32) * 128 * 4
+    f = lib.sgmv_fused_workspace_bytes
+    assert f(128, 4096, 16) == 128 * 16 * 4 + 1280 + 128 * 2048 + part(128, 4096)
+    assert f(3, 64, 5) == 256 + 256 + 3 * 2048 + part(3, 64)
+    assert f(100, 11008, 32) == 100 * 32 * 4 + 1024 + 100 * 2048 + part(100, 11008)
+    assert f(7, 200, 64) == 7 * 64 * 4 + 256 + 7 * 4096 + part(7, 200)
+    assert f(0, 4096, 16) == 0

@@ -123,7 +123,7 @@ def test_no_adapter_at_all_is_the_base_layer():
     ids = torch.full((24,), -1, dtype=torch.int32)
     w, W = _problem(24, 2, 512, 256, 16, ids, seed=2)
     assert_close(_run(w, W), _ref(w, W), "every row without an adapter")
-    # no segments: base product only, no workspace needed
+    # no segments: base product only (one kernel)
     dev = torch.device("cuda")
     y = torch.zeros((24, 256), dtype=F16, device=dev)
     empty = torch.zeros(1, dtype=torch.int32, device=dev)
