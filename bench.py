@@ -75,6 +75,8 @@ def parse_args(argv=None):
                    help="the fused LoRA layer instead: y = x W + LoRA delta in one pass "
                         "(sgmv_fused_linear_lora) against cuBLAS x W alone and x W + SGMV, "
                         "over batch sizes and the Llama-2-7B projection shapes")
+    p.add_argument("--fused-point", default=None, metavar="H1,H2,T",
+                   help="with --fused: that one point only (for profiling)")
     p.add_argument("--figure", action="store_true",
                    help="the pages' micro-benchmark instead: latency of the base layer alone, "
                         "with a per-adapter loop and with SGMV, over batch sizes and adapter counts")
@@ -106,33 +108,44 @@ def host_threads():
         return os.cpu_count() or 1
 
 
-# Sources of the C ABI's host-side argument checks and dispatch: they launch
-# kernels but hold none, so a change there leaves the kernels' counters valid.
-HOST_ONLY_SOURCES = ("sgmv_api.cu", "sgmv_noalloc.cu")
+# Kernel sources behind each workload's launches: a profile's counters stand
+# only for the code that hashes to the value recorded beside them.  Host-side
+# argument checks and dispatch (sgmv_api.cu, sgmv_noalloc.cu) hold no kernel.
+_COMMON_SOURCES = ("sgmv_device.cuh", "sgmv_internal.h", "sgmv_builder.cu")
+KERNEL_SOURCES = {
+    "stream": _COMMON_SOURCES + ("sgmv_stream.cuh", "sgmv_stream_f16.cu", "sgmv_stream_bf16.cu"),
+    "tc": _COMMON_SOURCES + ("sgmv_tc.cu", "sgmv_tcgen05.cuh", "sgmv_tiles.cuh", "sgmv_cc.cuh",
+                             "sgmv_cc_f16.cu", "sgmv_cc_bf16.cu"),
+    "fused": _COMMON_SOURCES + ("sgmv_fused.cu", "sgmv_fused.h", "sgmv_tcgen05.cuh",
+                                "sgmv_tiles.cuh", "sgmv_cc.cuh", "sgmv_cc_f16.cu",
+                                "sgmv_cc_bf16.cu"),
+}
+# which kernels a workload's update call runs (prefill's segments all go to
+# the tensor cores; every decode workload to the streaming kernel)
+WORKLOAD_KERNELS = {"prefill": "tc", "fused-linear-lora-q": "fused"}
 
 
-def source_hash():
-    """Hash of the kernel sources: a profile's counters stand only for this code."""
+def source_hash(family="stream"):
+    """Hash of one kernel family's sources (see KERNEL_SOURCES)."""
     import hashlib
 
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "rank_gemv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")) and f not in HOST_ONLY_SOURCES:
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in sorted(KERNEL_SOURCES[family]):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:12]
 
 
 def profiled_traffic(workload):
     """DRAM bytes per update call measured by ncu for this workload (from
-    profiles/traffic.md), or None when the kernels changed since."""
+    profiles/traffic.md), or None when its kernels changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     try:
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    want = source_hash()
+    want = source_hash(WORKLOAD_KERNELS.get(workload, "stream"))
     for line in lines:
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
         if len(cells) >= 3 and cells[0] == workload and cells[1] == want:
@@ -516,7 +529,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": kname, "kernels_per_call": per_call,
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": frac,
                      "peak_kind": peak_kind, "traffic": profiled_traffic(args.workload),
-                     "source_hash": source_hash(), "bytes_per_call": bytes_apply,
+                     "source_hash": source_hash(WORKLOAD_KERNELS.get(args.workload, "stream")), "bytes_per_call": bytes_apply,
                      "call_us": apply_us,
                      "frac_uses": f"call_us: {n_apply * K} update calls back to back in CUDA "
                                   f"graphs, median of {R} regions",
@@ -1080,6 +1093,8 @@ def run_fused(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     points = [(4096, 4096, T) for T in (1, 8, 32, 64, 128)]
     points += [(4096, 11008, 128), (11008, 4096, 128)]
+    if args.fused_point:
+        points = [tuple(int(v) for v in args.fused_point.split(","))]
     for i, (H1, H2, T) in enumerate(points):
         out = fused_layer_point(sgmv, wl, dev, H1, H2, T, args.seed + 97 * i, args.latency_iters,
                                 flush, l2, peak)

@@ -236,24 +236,6 @@ __device__ __forceinline__ void st_async4(uint32_t remote, float a, float b, flo
         : "memory");
 }
 
-// 1-D bulk copy from this CTA's shared memory into a cluster peer's: `dst` and
-// the peer's mbarrier `bar` are shared::cluster addresses (from peer_addr);
-// completes on that barrier.  16-byte aligned, bytes a multiple of 16.  The
-// source must stay untouched, and its CTA alive, until the copy has landed.
-__device__ __forceinline__ void bulk_s2peer(uint32_t dst, const void *src, uint32_t bytes,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "r"(smem_addr(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void sts128(void *p, float a, float b, float c, float d) {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
-}
-
 // ---- explicit shared-memory access ----------------------------------------
 // Pointers into dynamic shared memory that pass through lambdas or offset
 // arithmetic can lose their address space, and the generic loads the compiler

@@ -63,6 +63,7 @@
 
 #include "sgmv_device.cuh"
 #include "sgmv_internal.h"
+#include "sgmv_fused.h"
 #include "sgmv_tcgen05.cuh"
 
 namespace sgmv {
