@@ -72,6 +72,11 @@ namespace {
 constexpr int kFusedThreads = 160;
 constexpr int kFusedCols = 128;               // columns of W per tile (M of every MMA)
 constexpr int kFusedMaxStages = 16;
+// Ring stages used: more bytes in flight per SM only lengthened the copies'
+// latency (one, 32 and 128 rows at the Llama-2-7B q shape: four stages
+// 15.8 / 21.0 / 36.0 us per call against 16.6 / 23.0 / 35.8 with as many as
+// fit, and no better with three or five)
+constexpr int kFusedRingStages = 4;
 constexpr uint32_t kFusedXOff = 16384;        // x tile at this offset of a stage
 constexpr uint32_t kFusedWBytes = 2u * 64u * 128u;  // two 64-column halves of a k-block of W
 constexpr int kFusedMaxPairs = 128;           // at most T pairs, T <= 128
@@ -664,7 +669,7 @@ int fused_launch_t(const FusedArgs &g) {
     cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return (int)e;
     const size_t smem_max = 227u * 1024u;
-    p.nst = (int)std::min<size_t>(kFusedMaxStages,
+    p.nst = (int)std::min<size_t>(kFusedRingStages,
                                   (smem_max - fa.sharedSizeBytes - 1024u) / p.stage_bytes);
     if (p.nst < 2) return (int)cudaErrorInvalidValue;
     const size_t smem = (size_t)p.nst * p.stage_bytes + 1024u;
