@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     int *const err = P.err;
 
     extern __shared__ __align__(1024) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t full[kFusedMaxStages], empty[kFusedMaxStages], done, tab_ready;
+    __shared__ __align__(8) uint64_t full[kFusedMaxStages], empty[kFusedMaxStages], done, tab_ready,
+        red_full;
     __shared__ int s_pa[kFusedMaxPairs], s_pc[kFusedMaxPairs];  // pair table
     __shared__ int s_kind[kFusedMaxStages], s_cnt[kFusedMaxStages];
     __shared__ int s_chunk[kFusedMaxStages][kFusedMaxPPI];
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         mbar_init(&done, 1);
         mbar_init(&tab_ready, 1);
+        mbar_init(&red_full, 1);  // the owner's slots of partial sums, by bulk copies
         mbar_init_fence();
         s_lost = 0;
     }
@@ -524,48 +526,98 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // [8 quads of rows][128 columns][4 rows] so that a warp moves 512
         // contiguous bytes per access (quads holding rows t < T only); a
         // cluster barrier; then groups g = rank, rank + CL, ... summed over
-        // the CL slots in rank order, with every load of a group in flight
-        // at once (the loads are latency-bound, not bandwidth-bound).
+        // the CL slots in rank order.
         float4 *const part = reinterpret_cast<float4 *>(P.part) + (size_t)blockIdx.y * C * ngrp * 1024;
         auto nq_of = [&](int g) { return min(8, (T - g * 32 + 3) >> 2); };
         if (tid < 128) {
-            for (int g = 0; g < ngrp; ++g) {
-                float f[32];
-                tmem_ld32(lane_addr + (uint32_t)(g * 32), f);
+            // every group's accumulator columns requested before one wait
+            // (ngrp <= 4: the accumulator has at most 128 columns)
+            uint32_t f[4][32];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                if (g < ngrp) tmem_ld32_async(lane_addr + (uint32_t)(g * 32), f[g]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (g >= ngrp) break;
                 const int nq = nq_of(g);
                 float4 *const dst = part + ((size_t)rank * ngrp + g) * 1024 + tid;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    if (q < nq) dst[q * 128] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                    if (q < nq)
+                        dst[q * 128] = make_float4(
+                            __uint_as_float(f[g][4 * q]), __uint_as_float(f[g][4 * q + 1]),
+                            __uint_as_float(f[g][4 * q + 2]), __uint_as_float(f[g][4 * q + 3]));
             }
+            fence_proxy_async_all();  // the owners read these by bulk copies
         }
         // release / acquire at cluster scope: the partials are visible after it
         cluster_sync();
         lost = lost || s_lost != 0;
-        if (tid < 128)
+        // The owner's slots come into the (idle) ring by one bulk copy per
+        // (group, source), compactly, when they fit: one copy engine keeps
+        // them all in flight (register loads of the same bytes took ~3 us).
+        uint32_t rbytes = 0;
+        for (int g = rank; g < ngrp; g += C) rbytes += (uint32_t)(C * nq_of(g)) * 2048u;
+        const bool by_copy = rbytes <= (uint32_t)nst * stage_bytes;
+        float *const recv = reinterpret_cast<float *>(ring);
+        if (by_copy && rbytes > 0) {
+            if (tid == 0) {
+                fence_proxy_async_all();  // generic writes of the peers -> the copy unit
+                mbar_arrive_expect_tx(&red_full, rbytes);
+                uint32_t off = 0;
+                for (int g = rank; g < ngrp; g += C) {
+                    const uint32_t nb = (uint32_t)nq_of(g) * 2048u;
+                    for (int src = 0; src < C; ++src, off += nb)
+                        bulk_g2s(reinterpret_cast<uint8_t *>(recv) + off,
+                                 part + ((size_t)src * ngrp + g) * 1024, nb, &red_full);
+                }
+            }
+            if (tid < 128 && !mbar_wait(&red_full, 0)) {
+                set_error(err, kErrTimeout);
+                lost = true;
+                mbar_wait(&red_full, 0);
+            }
+        }
+        if (tid < 128) {
+            uint32_t off = 0;  // floats
             for (int g = rank; g < ngrp; g += C) {
                 const int nq = nq_of(g);
                 float4 acc[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int s0 = 0; s0 < C; s0 += 4) {
-                    float4 u[4][8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                if (by_copy) {
+                    for (int src = 0; src < C; ++src, off += (uint32_t)nq * 512u) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            if (s0 + i < C && q < nq)
-                                u[i][q] = __ldcg(part + ((size_t)(s0 + i) * ngrp + g) * 1024 + q * 128 + tid);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            if (s0 + i < C && q < nq) {
-                                acc[q].x += u[i][q].x;
-                                acc[q].y += u[i][q].y;
-                                acc[q].z += u[i][q].z;
-                                acc[q].w += u[i][q].w;
+                            if (q < nq) {
+                                const uint4 u = lds128(recv + off + (q * 128 + tid) * 4);
+                                acc[q].x += __uint_as_float(u.x);
+                                acc[q].y += __uint_as_float(u.y);
+                                acc[q].z += __uint_as_float(u.z);
+                                acc[q].w += __uint_as_float(u.w);
                             }
+                    }
+                } else {
+                    for (int s0 = 0; s0 < C; s0 += 4) {
+                        float4 u[4][8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (s0 + i < C && q < nq)
+                                    u[i][q] = __ldcg(part + ((size_t)(s0 + i) * ngrp + g) * 1024 + q * 128 + tid);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (s0 + i < C && q < nq) {
+                                    acc[q].x += u[i][q].x;
+                                    acc[q].y += u[i][q].y;
+                                    acc[q].z += u[i][q].z;
+                                    acc[q].w += u[i][q].w;
+                                }
+                    }
                 }
                 if (!lost && j < H2) {
 #pragma unroll
@@ -579,6 +631,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                     }
                 }
             }
+        }
     }
     tc_fence_before();
     __syncthreads();
