@@ -84,6 +84,8 @@ constexpr int kFusedMaxPPI = 8;               // pairs per ring stage
 constexpr int kPrepThreads = 256;
 constexpr int kPrepMaxCtas = 32;
 constexpr int kFusedMaxCl = 8;                // CTAs per cluster (portable limit)
+constexpr double kFusedCtaUs = 6.0;           // cluster-size model: fixed cost of a CTA
+constexpr double kFusedStageUs = 0.45;        // ... and of one ring stage
 
 __host__ __device__ inline int fused_rp(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
 // 16 x 64 tiles of v per pair: hi and lo share one tile for rp <= 32
@@ -697,19 +699,24 @@ int fused_launch_t(const FusedArgs &g) {
             return (int)cudaErrorInvalidValue;
         p.ptab = static_cast<const int32_t *>(g.prep);
     }
-    // Cluster size: the split of H1 that keeps the most SMs busy over whole
-    // waves of one CTA per SM (ties: the smaller split), each CTA with at
-    // least one k-block.
+    // Cluster size: the split of H1 with the least modelled time, waves of
+    // one CTA per SM times a CTA's fixed cost plus its items (k-blocks of W
+    // and groups of pairs) at a stage each.  Constants measured on the
+    // Llama-2-7B shapes at 128 rows (about 6 us of set-up and reduction per
+    // CTA, 0.45 us per stage); the model picks the measured best split of
+    // the three (4096 -> 4096: 4; 4096 -> 11008: 3, 63 us against 92 with
+    // the most SMs busy; 11008 -> 4096: 4).
     const int ntiles = (g.H2 + kFusedCols - 1) / kFusedCols;
     const int nsm = std::max(1, g.nsm);
+    const int nl = g.prep ? (g.T + p.ppi - 1) / p.ppi : 0;  // groups of pairs, at most
     int best = 1;
-    double best_eff = -1.0;
+    double best_t = 1e30;
     for (int c = 1; c <= std::min(kFusedMaxCl, p.kbt); ++c) {
-        const long long ctas = (long long)ntiles * c;
-        const long long waves = (ctas + nsm - 1) / nsm;
-        const double eff = (double)ctas / (double)(waves * nsm);
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
+        const long long waves = ((long long)ntiles * c + nsm - 1) / nsm;
+        const double items = (double)((p.kbt + c - 1) / c) + (double)((nl + c - 1) / c);
+        const double t = (double)waves * (kFusedCtaUs + items * kFusedStageUs);
+        if (t < best_t - 1e-9) {
+            best_t = t;
             best = c;
         }
     }
