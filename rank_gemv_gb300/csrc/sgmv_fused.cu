@@ -87,6 +87,29 @@ constexpr int kFusedMaxCl = 8;                // CTAs per cluster (portable limi
 constexpr double kFusedCtaUs = 6.0;           // cluster-size model: fixed cost of a CTA
 constexpr double kFusedStageUs = 0.45;        // ... and of one ring stage
 
+// As tmem_ld32 without the wait: the registers are valid after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// The same for every state space (global memory written through the generic
+// proxy, then read by a bulk copy).
+__device__ __forceinline__ void fence_proxy_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
+}
+
 __host__ __device__ inline int fused_rp(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
 // 16 x 64 tiles of v per pair: hi and lo share one tile for rp <= 32
 __host__ __device__ inline int fused_ntile(int rp) { return rp <= 32 ? 1 : 2; }
