@@ -99,6 +99,17 @@ def test_ranks(r):
     assert_close(_run(w, W), _ref(w, W), f"r={r}")
 
 
+@pytest.mark.parametrize("scale", [0.0, -2.0, 1e-3])
+def test_scale_values(scale):
+    """scale multiplies the adapter term only: 0 gives x W exactly, a negative
+    scale flips the term's sign (v's hi / lo halves carry the sign), a small
+    one leaves the term below the base product's rounding."""
+    g = torch.Generator().manual_seed(7)
+    ids = torch.randint(-1, 6, (40,), generator=g, dtype=torch.int32)
+    w, W = _problem(40, 6, 512, 384, 16, ids, seed=11, scale=scale)
+    assert_close(_run(w, W), _ref(w, W), f"scale {scale}")
+
+
 @pytest.mark.parametrize("dtype,y_dtype", [(F16, F16), (F16, F32), (BF16, BF16), (BF16, F32),
                                            (F16, BF16), (BF16, F16)])
 def test_types(dtype, y_dtype):
