@@ -157,32 +157,40 @@ __global__ void __launch_bounds__(kPrepThreads) sgmv_fused_prep_kernel(const Pre
         s_rowslot[tid] = -1;
         s_mask[tid] = 0u;
     }
-    if (warp == 0) {
-        int n = 0;
-        for (int s0 = 0; s0 < S; s0 += 32) {
-            const int s = s0 + lane;
-            int b = 0, e = 0, a = -1;
-            bool ok = false;
-            if (s < S) {
-                b = P.seg_ptr[s];
-                e = P.seg_ptr[s + 1];
-                a = P.idx[s];
-                const bool seg_good = b >= 0 && e >= b && e <= T;
-                if (report && !seg_good) set_error(P.err, kErrBadSegments);
-                if (report && seg_good && e > b && (a < -1 || a >= L)) set_error(P.err, kErrBadIndex);
-                ok = seg_good && e > b && a >= 0 && a < L;
-            }
-            const unsigned m = __ballot_sync(0xffffffffu, ok);
-            const int i = n + __popc(m & ((1u << lane) - 1u));
-            if (ok && i < 128) {
-                s_b[i] = b;
-                s_e[i] = e;
-                s_a[i] = a;
-            }
-            n += __popc(m);
+    // the row at this thread's position, requested first: its load overlaps
+    // the segments' below
+    const int prow = tid < T ? (P.perm ? P.perm[tid] : tid) : 0;
+    // slots: every thread reads one segment's bounds and id (all segments'
+    // loads in flight together), then a block-wide scan numbers the valid ones
+    int nbase = 0;
+    for (int s0 = 0; s0 < S; s0 += kPrepThreads) {
+        const int s = s0 + tid;
+        int b = 0, e = 0, a = -1;
+        bool ok = false;
+        if (s < S) {
+            b = P.seg_ptr[s];
+            e = P.seg_ptr[s + 1];
+            a = P.idx[s];
+            const bool seg_good = b >= 0 && e >= b && e <= T;
+            if (report && !seg_good) set_error(P.err, kErrBadSegments);
+            if (report && seg_good && e > b && (a < -1 || a >= L)) set_error(P.err, kErrBadIndex);
+            ok = seg_good && e > b && a >= 0 && a < L;
         }
-        if (lane == 0) s_nslot = min(n, 128);  // slots hold disjoint rows: n <= T
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) s_wsum[warp] = __popc(m);
+        __syncthreads();
+        int before = nbase;
+        for (int w = 0; w < warp; ++w) before += s_wsum[w];
+        const int i = before + __popc(m & ((1u << lane) - 1u));
+        if (ok && i < 128) {
+            s_b[i] = b;
+            s_e[i] = e;
+            s_a[i] = a;
+        }
+        for (int w = 0; w < kPrepThreads / 32; ++w) nbase += s_wsum[w];
+        __syncthreads();  // s_wsum is reused
     }
+    if (tid == 0) s_nslot = min(nbase, 128);  // slots hold disjoint rows: at most T
     __syncthreads();
     const int nslot = s_nslot;
     if (tid < T) {
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(kPrepThreads) sgmv_fused_prep_kernel(const Pre
             }
         }
         if (i >= 0 && p < s_e[i]) {
-            const int t = P.perm ? P.perm[p] : p;
+            const int t = prow;
             if (t < 0 || t >= T) {
                 if (report) set_error(P.err, kErrBadIndex);
             } else {
