@@ -1,7 +1,9 @@
 """Full-size llama7b-stack workload (32 layers x 7 projections, 128 decode rows
 on 128 adapters, about 10 GB of stacked adapters) in the benchmark's launch
-configuration: one device grouping, then 224 fused updates.  Sampled
-projections are checked against the oracle element by element."""
+configuration: one device grouping, then 224 fused updates.  Five
+projections are checked against the oracle element by element, and three
+rows of every one of the 224 projections (each row against the oracle on
+that row and its adapter alone)."""
 import pytest
 import torch
 
@@ -35,5 +37,14 @@ def test_llama7b_stack_sampled_projections():
         Y0 = torch.zeros(Y.shape, dtype=torch.float16)
         ref = oracle.sgmv_apply(Y0, X, A, B, o_seg, o_idx, 1.0, perm=o_perm)
         assert_close(Y, ref, f"layer {layer} proj {wl.LLAMA7B_PROJ[p][0]}")
+    one = (torch.tensor([0, 1], dtype=torch.int32), torch.tensor([0], dtype=torch.int32))
+    for k, (X, A, B, Y) in enumerate(projs):
+        layer, p = divmod(k, n_proj)
+        for t in ((7 * k + 3) % 128, (13 * k + 64) % 128, (29 * k + 101) % 128):
+            a = int(ra[t])
+            ref = oracle.sgmv_apply(torch.zeros((1, Y.shape[1]), dtype=torch.float16),
+                                    X[t:t + 1].cpu(), A[a:a + 1].cpu(), B[a:a + 1].cpu(),
+                                    one[0], one[1], 1.0)
+            assert_close(Y[t:t + 1], ref, f"layer {layer} proj {wl.LLAMA7B_PROJ[p][0]} row {t}")
     del projs
     torch.cuda.empty_cache()
