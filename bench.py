@@ -387,9 +387,10 @@ def timed_regions(graph_full, n_per_graph, graph_rem, K, repeats, world):
     return out
 
 
-def isolated_us(fn, flush, iters):
-    """Median device time (us) of fn() alone: before each call a write larger
-    than L2 evicts its inputs, and CUDA events bracket the call."""
+def isolated_stats(fn, flush, iters):
+    """Device time (us) of fn() alone, median and 10th / 90th percentiles:
+    before each call a write larger than L2 evicts its inputs, and CUDA events
+    bracket the call."""
     import torch
 
     ts = []
@@ -401,7 +402,14 @@ def isolated_us(fn, flush, iters):
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1) * 1e3)
-    return statistics.median(ts)
+    ts.sort()
+    pick = lambda q: ts[min(len(ts) - 1, int(q * (len(ts) - 1) + 0.5))]
+    return {"median": statistics.median(ts), "p10": pick(0.1), "p90": pick(0.9)}
+
+
+def isolated_us(fn, flush, iters):
+    """Median of isolated_stats."""
+    return isolated_stats(fn, flush, iters)["median"]
 
 
 def back_to_back_us(fns, calls, repeats=3):
@@ -500,16 +508,20 @@ def run_ours(args, rank, world, local):
         iso = {}
         for name, i in (("q", 0), ("gate", 4), ("down", 6)):
             _, H1, H2 = wl.LLAMA7B_PROJ[i]
-            us = isolated_us(lambda i=i: stack.update_one(sgmv, i), flush, args.latency_iters)
-            iso[name] = {"us": us, "bytes": StackBatch.proj_bytes(H1, H2),
+            st = isolated_stats(lambda i=i: stack.update_one(sgmv, i), flush, args.latency_iters)
+            us = st["median"]
+            iso[name] = {"us": us, "us_p10": st["p10"], "us_p90": st["p90"],
+                         "bytes": StackBatch.proj_bytes(H1, H2),
                          "frac": hbm(StackBatch.proj_bytes(H1, H2), us, peak)[1]}
         # a layer has four q-shaped, two gate-shaped and one down-shaped call
         iso_us = (4 * iso["q"]["us"] + 2 * iso["gate"]["us"] + iso["down"]["us"]) / 7
         iso_note = "per projection shape (layer 0), L2 flushed before each; mean over a layer's 7 calls"
     else:
         iso = None
-        iso_us = isolated_us(lambda: batches[0].update(sgmv), flush, args.latency_iters)
-        iso_note = "L2 flushed before each call"
+        iso_st = isolated_stats(lambda: batches[0].update(sgmv), flush, args.latency_iters)
+        iso_us = iso_st["median"]
+        iso_note = (f"L2 flushed before each call; p10 {iso_st['p10']:.2f} us, "
+                    f"p90 {iso_st['p90']:.2f} us")
     iso_gbs, iso_frac = hbm(bytes_apply, iso_us, peak)
     if args.workload == "prefill":
         kname = "sgmv_tc_shrink_kernel + sgmv_tc_expand_kernel (tensor cores; the streaming kernel gets no short segment)"
@@ -585,13 +597,15 @@ def measure_workload(name, args, dev, sgmv, wl, l2, peak, flush):
                      "rotation" + (" (> 2 x L2)" if n_copies * nbytes > 2 * l2 else " (inside L2)")}
     b2b_call = back_to_back_us([(lambda b=b: b.update(sgmv)) for b in batches], calls)
     b2b_step = back_to_back_us([(lambda b=b: b.step(sgmv)) for b in batches], calls)
-    iso_call = isolated_us(lambda: batches[0].update(sgmv), flush, args.latency_iters)
+    iso_st = isolated_stats(lambda: batches[0].update(sgmv), flush, args.latency_iters)
+    iso_call = iso_st["median"]
     iso_step = isolated_us(lambda: batches[0].step(sgmv), flush, args.latency_iters)
     g1, f1 = hbm(nbytes, b2b_call, peak)
     g2, f2 = hbm(nbytes, iso_call, peak)
     res["back_to_back"] = {"call_us": b2b_call, "gbs": g1, "frac": f1, "step_us": b2b_step,
                            "rows_per_s": w.T / (b2b_step * 1e-6)}
-    res["isolated"] = {"call_us": iso_call, "gbs": g2, "frac": f2, "step_us": iso_step}
+    res["isolated"] = {"call_us": iso_call, "call_us_p10": iso_st["p10"],
+                       "call_us_p90": iso_st["p90"], "gbs": g2, "frac": f2, "step_us": iso_step}
     if w.T <= 64 and w.r % 4 == 0 and w.r <= 64:
         nb = (nbytes + 15) // 16 * 16
         src = torch.zeros(n_copies * nb // 4, dtype=torch.int32, device=dev)
