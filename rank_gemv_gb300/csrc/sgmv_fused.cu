@@ -42,9 +42,9 @@
 // CL CTAs; CTA `rank` takes an even share of H1's 64-column k-blocks and
 // every CL-th group of pairs, so all CTAs stream about the same bytes.  The
 // partial accumulators meet in an fp32 scratch area of the workspace (in L2:
-// distributed shared memory moves them several times slower on this part);
-// after a cluster barrier each CTA sums, in rank order, every CL-th group of
-// 32 rows of the tile: deterministic.
+// distributed shared memory moved them no faster); after a cluster barrier
+// each CTA brings the slots of every CL-th group of 32 rows of the tile into
+// its idle ring by bulk copies and sums them in rank order: deterministic.
 //
 // Warps of the fused kernel: 0-3 read the accumulator (one TMEM lane, i.e.
 // one column j, per thread) and write y; before that, warp 3 issues the MMAs
