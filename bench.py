@@ -1172,10 +1172,12 @@ def run_load(args):
     """On-demand adapter loading (the "Punica: Multi-Tenant LoRA Serving" review:
     adapters are loaded on demand, in milliseconds).  One Llama-2-7B adapter =
     32 layers x 7 projections of A [H1, 16] and B [16, H2], fp16, 80 MB, in
-    page-locked host memory, copied with sgmv_load_adapter on a copy stream:
-    (1) alone; (2) while the compute stream replays llama7b-stack steps (all
-    224 SGMV calls over 128 resident adapters), the loads going to spare pools
-    so that no slot a running call reads is overwritten.  Prints one JSON line."""
+    page-locked host memory, loaded on a copy stream (a) as 448 copy-engine
+    transfers (sgmv_load_adapter) and (b) as one sgmv_copy_gather kernel that
+    reads the host memory directly, at several CTA caps: (1) alone; (2) while
+    the compute stream replays llama7b-stack steps (all 224 SGMV calls over 128
+    resident adapters), the loads going to spare pools so that no slot a
+    running call reads is overwritten.  Prints one JSON line."""
     import torch
 
     from rank_gemv_gb300 import build as _build
@@ -1258,6 +1260,83 @@ def run_load(args):
     torch.cuda.synchronize()
     busy_load_ms = e0.elapsed_time(e1) / n
     step_busy = s0.elapsed_time(s1) / steps
+
+    # host time to issue one adapter's loads
+    def host_ms(fn, reps=5):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        torch.cuda.synchronize()
+        return statistics.median(ts)
+
+    issue_copy_ms = host_ms(lambda: load(0))
+    # the link's reference: the same bytes as ONE copy-engine transfer
+    big_h = torch.empty(adapter_bytes, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty(adapter_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(cs):
+        for _ in range(3):
+            big_d.copy_(big_h, non_blocking=True)
+        torch.cuda.synchronize()
+        e0.record(cs)
+        for _ in range(n):
+            big_d.copy_(big_h, non_blocking=True)
+        e1.record(cs)
+    torch.cuda.synchronize()
+    one_transfer_ms = e0.elapsed_time(e1) / n
+    del big_h, big_d
+    dsts = [[t[slot] for A, B in spare for t in (A, B)] for slot in (0, 1)]
+    srcs = [t for a, b in host for t in (a, b)]
+    gather = {}
+    for ctas in (0, 304, 152, 64, 16):
+        def gload(slot, ctas=ctas):
+            sgmv.sgmv_copy_gather(dsts[slot], srcs, stream=cs, max_ctas=ctas)
+            assert sgmv.load_library().sgmv_last_launch_count() == 1
+
+        for A, B in spare:
+            A.zero_()
+            B.zero_()
+        torch.cuda.synchronize()
+        issue_ms = host_ms(lambda: gload(0))
+        gload(1)
+        torch.cuda.synchronize()
+        g_ok = all(torch.equal(A[i].cpu(), a) and torch.equal(B[i].cpu(), b)
+                   for (A, B), (a, b) in zip(spare, host) for i in (0, 1))
+        ggraphs = []
+        for slot in (0, 1):
+            gg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gg, stream=cs, capture_error_mode="relaxed"):
+                gload(slot)
+            ggraphs.append(gg)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cs):
+            for i in range(3):
+                ggraphs[i & 1].replay()
+            torch.cuda.synchronize()
+            e0.record(cs)
+            for i in range(n):
+                ggraphs[i & 1].replay()
+            e1.record(cs)
+        torch.cuda.synchronize()
+        g_alone = e0.elapsed_time(e1) / n
+        s0.record()
+        for _ in range(steps):
+            graph.replay()
+        s1.record()
+        with torch.cuda.stream(cs):
+            e0.record(cs)
+            for i in range(n):
+                ggraphs[i & 1].replay()
+            e1.record(cs)
+        torch.cuda.synchronize()
+        gather[str(ctas or "4 per SM")] = {
+            "load_ms_alone": g_alone, "load_gbs_alone": adapter_bytes / g_alone / 1e6,
+            "load_ms_during_sgmv": e0.elapsed_time(e1) / n,
+            "stack_step_ms_during_loads": s0.elapsed_time(s1) / steps,
+            "host_issue_ms": issue_ms, "bit_exact": g_ok}
+        del ggraphs
     assert sgmv.sgmv_get_device_error(dev) == 0
     print(json.dumps({
         "bench": "adapter_load", "adapter": "llama2-7b, 224 projections, r=16, fp16",
@@ -1265,7 +1344,11 @@ def run_load(args):
         "load_ms_alone": alone_ms, "load_gbs_alone": adapter_bytes / alone_ms / 1e6,
         "load_ms_during_sgmv": busy_load_ms,
         "stack_step_ms_alone": step_alone, "stack_step_ms_during_loads": step_busy,
+        "host_issue_ms": issue_copy_ms,
+        "one_transfer_ms": one_transfer_ms,
+        "one_transfer_gbs": adapter_bytes / one_transfer_ms / 1e6,
         "loads_during_run": n, "steps_during_run": steps, "copies_bit_exact": ok,
+        "gather_by_cta_cap": gather,
         "host_memory": "page-locked"}), flush=True)
 
 

@@ -298,6 +298,33 @@ int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, co
                       void *stream);
 
 /*
+ * Up to 512 copies dst[i] <- src[i] (bytes[i] bytes each) on `stream`, for
+ * loading every piece of an adapter at once (same page and passage as
+ * sgmv_load_adapter: one Llama-2-7B adapter is 448 pieces).  Every copy whose
+ * source and destination the current device reads directly (its own device
+ * memory, or page-locked host memory), both 16-byte aligned, with bytes[i] a
+ * multiple of 16, is moved by ONE kernel launch: the SMs read the sources
+ * (page-locked host memory over the CPU-GPU link) and write the destinations.
+ * Each other copy is enqueued as its own asynchronous copy-engine transfer on
+ * `stream`.  All copies are ordered after earlier work on `stream`.
+ *   n          number of copies, 0 <= n <= 512 (0: nothing happens)
+ *   dst, src   host arrays of n pointers (host or device addresses); the
+ *              ranges must not overlap one another
+ *   bytes      host array of n sizes; a zero size skips its copy (its
+ *              pointers may then be null)
+ *   max_ctas   most CTAs of the kernel; 0 = four per SM.  A small cap leaves
+ *              SMs to kernels that run at the same time on other streams.
+ * The arrays are read before the call returns; the copied memory must stay
+ * valid until the copies complete.  Nothing is allocated.  Errors:
+ * SGMV_ERR_INVALID_ARG for n outside [0, 512], negative max_ctas, null arrays
+ * or a null pointer with a non-zero size; SGMV_ERR_CUDA if a copy or the
+ * launch cannot be enqueued (then some copies may have been enqueued).
+ * sgmv_last_launch_count() is 1 if the kernel was launched, else 0.
+ */
+int sgmv_copy_gather(int32_t n, void *const *dst, const void *const *src, const uint64_t *bytes,
+                     int32_t max_ctas, void *stream);
+
+/*
  * Diagnostics (no counterpart on the pages).
  *
  * sgmv_read_floor: the floor of a decode-sized SGMV launch on this GPU.  Reads

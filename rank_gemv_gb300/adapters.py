@@ -5,8 +5,10 @@ and loads the others on demand, in milliseconds ("Punica: Multi-Tenant LoRA
 Serving", nubint.ai review, "Proposed method" and findings).  Here a model's
 projections each have a stacked pool A [L, H1, r], B [L, r, H2] on the device;
 an AdapterPool maps adapter names to the L slots, least recently used first
-out, and loads a missing adapter's weights into every projection's pool with
-sgmv_load_adapter on a copy stream.
+out, and loads a missing adapter's weights into every projection's pool on a
+copy stream: all of its pieces in one sgmv_copy_gather call (one kernel that
+reads page-locked host memory directly), or, with gather=False, two
+sgmv_load_adapter copy-engine transfers per projection.
 
 Ordering on the GPU:
   * before a slot is overwritten, the copy stream waits for the work already
@@ -16,7 +18,8 @@ Ordering on the GPU:
 With page-locked host weights the copies overlap with the compute stream's
 kernels.
 
-Host logic only: every byte moves through sgmv_load_adapter.
+Host logic only: every byte moves through sgmv_copy_gather or
+sgmv_load_adapter.
 """
 from __future__ import annotations
 
@@ -36,12 +39,17 @@ class AdapterPool:
     source: source(name) -> one (A [H1, r], B [r, H2]) pair per projection,
             host tensors (page-locked for overlap) or device tensors.
     loader: loader(slot, weights) copies one adapter into every pool; the
-            default issues sgmv_load_adapter on the copy stream.
+            default issues sgmv_copy_gather (gather=True) or sgmv_load_adapter
+            (gather=False) on the copy stream.
+    gather_ctas: CTA cap of the gather kernel (0: four per SM).  64 CTAs
+            already read page-locked host memory as fast as the CPU-GPU link
+            delivers it (as fast as one large copy-engine transfer) and leave
+            the other SMs to the SGMV calls running meanwhile.
     gpu:    False skips all stream handling (host-only use and tests).
     """
 
     def __init__(self, pools: Sequence, source: Callable, loader: Callable | None = None,
-                 copy_stream=None, gpu: bool = True):
+                 copy_stream=None, gpu: bool = True, gather: bool = True, gather_ctas: int = 64):
         self.pools = list(pools)
         if not self.pools:
             raise ValueError("no pools")
@@ -56,6 +64,8 @@ class AdapterPool:
             import torch
 
             self.copy_stream = torch.cuda.Stream(self.pools[0][0].device)
+        self.gather = gather
+        self.gather_ctas = gather_ctas
         self.loader = loader if loader is not None else self._load
         self.resident: "OrderedDict[str, int]" = OrderedDict()  # least recent first
         self.free = list(range(self.L))
@@ -64,8 +74,18 @@ class AdapterPool:
     def _load(self, slot: int, weights) -> None:
         from . import sgmv
 
+        if not self.gather:
+            for (A_pool, B_pool), (A, B) in zip(self.pools, weights):
+                sgmv.sgmv_load_adapter(A_pool, B_pool, slot, A, B, stream=self.copy_stream)
+            return
+        dsts, srcs = [], []
         for (A_pool, B_pool), (A, B) in zip(self.pools, weights):
-            sgmv.sgmv_load_adapter(A_pool, B_pool, slot, A, B, stream=self.copy_stream)
+            for pool, w in ((A_pool, A), (B_pool, B)):
+                if tuple(w.shape) != tuple(pool.shape[1:]) or w.dtype != pool.dtype:
+                    raise ValueError("adapter shapes or types do not match the pools")
+                dsts.append(pool[slot])
+                srcs.append(w)
+        sgmv.sgmv_copy_gather(dsts, srcs, stream=self.copy_stream, max_ctas=self.gather_ctas)
 
     def slots_for(self, names: Sequence[str]) -> list[int]:
         """Slot of every name in `names` (one per row of a batch), loading the

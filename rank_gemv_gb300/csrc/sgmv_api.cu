@@ -745,6 +745,62 @@ int sgmv_load_adapter(void *A_pool, void *B_pool, int in_dtype, int32_t slot, co
                                        B_src, b_bytes, cudaMemcpyDefault, s));
 }
 
+// Address under which the current device `dev` reads p, or null if it cannot
+// read it directly: device memory of `dev`, or page-locked host memory mapped
+// into the device's address space.  Pageable and other devices' memory give
+// null (those copies go through the copy engine).
+static const void *device_view(const void *p, int dev) {
+    cudaPointerAttributes a = {};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // an unknown pointer: not an error of this call
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice) return a.device == dev ? p : nullptr;
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    return nullptr;
+}
+
+int sgmv_copy_gather(int32_t n, void *const *dst, const void *const *src, const uint64_t *bytes,
+                     int32_t max_ctas, void *stream) {
+    g_launches = 0;
+    if (n < 0 || n > kGatherMaxCopies || max_ctas < 0) return SGMV_ERR_INVALID_ARG;
+    if (n == 0) return SGMV_OK;
+    if (!dst || !src || !bytes) return SGMV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (bytes[i] && (!dst[i] || !src[i])) return SGMV_ERR_INVALID_ARG;
+    int dev = 0;
+    int st = cuda_status("current device", cudaGetDevice(&dev));
+    if (st != SGMV_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::vector<void *> kd;
+    std::vector<const void *> ks;
+    std::vector<uint64_t> kb;
+    for (int i = 0; i < n; ++i) {
+        if (!bytes[i]) continue;
+        const void *sv = nullptr;
+        void *dv = nullptr;
+        if (bytes[i] % 16u == 0 && aligned16(src[i]) && aligned16(dst[i])) {
+            sv = device_view(src[i], dev);
+            dv = const_cast<void *>(device_view(dst[i], dev));
+        }
+        if (sv && dv && aligned16(sv) && aligned16(dv)) {
+            kd.push_back(dv);
+            ks.push_back(sv);
+            kb.push_back(bytes[i]);
+        } else {
+            st = cuda_status("gather fallback copy",
+                             cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyDefault, s));
+            if (st != SGMV_OK) return st;
+        }
+    }
+    if (kd.empty()) return SGMV_OK;
+    const int cap = max_ctas > 0 ? max_ctas : 4 * std::max(1, num_sms());
+    st = cuda_status("gather kernel",
+                     gather_launch((int32_t)kd.size(), kd.data(), ks.data(), kb.data(), cap, s));
+    if (st == SGMV_OK) g_launches = 1;
+    return st;
+}
+
 // Workspace of the fused layer: v [T][r] fp32, the pair table and the v tiles,
 // then the fp32 partials of split tiles; each part 256-byte aligned.
 size_t fused_v_bytes(int32_t T, int32_t r) { return ((size_t)T * (size_t)r * 4u + 255u) / 256u * 256u; }

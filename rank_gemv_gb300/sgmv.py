@@ -27,6 +27,7 @@ STATUS = {0: "SGMV_OK", 1: "SGMV_ERR_INVALID_ARG", 2: "SGMV_ERR_UNSUPPORTED",
 # Every function include/sgmv.h declares, with its ctypes signature.
 _vp, _i32, _i32p = ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)
 _int, _f32, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_vpp, _u64p = ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_uint64)
 SIGNATURES = {
     "sgmv_status_string": (ctypes.c_char_p, [_int]),
     "sgmv_last_error_string": (ctypes.c_char_p, []),
@@ -49,6 +50,7 @@ SIGNATURES = {
     "sgmv_fused_linear_lora": (_int, [_vp, _int, _vp, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp,
                                       _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
     "sgmv_load_adapter": (_int, [_vp, _vp, _int, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]),
+    "sgmv_copy_gather": (_int, [_i32, _vpp, _vpp, _u64p, _i32, _vp]),
     "sgmv_read_floor": (_int, [_vp, _sz, _i32, _i32, _i32, _i32, _i32, _int, _int, _i32p, _i32p,
                                _vp]),
     "sgmv_debug_inject_wait_timeout": (_int, [_int]),
@@ -294,6 +296,33 @@ def sgmv_load_adapter(A_pool, B_pool, slot, A_src, B_src, stream=None):
     _check(load_library().sgmv_load_adapter(
         _ptr(A_pool), _ptr(B_pool), _DTYPES[A_pool.dtype], int(slot), _ptr(A_src), _ptr(B_src),
         L, H1, H2, r, st), "sgmv_load_adapter")
+
+
+GATHER_MAX_COPIES = 512
+
+
+def sgmv_copy_gather(dsts, srcs, stream=None, max_ctas=0):
+    """Copy every srcs[i] into dsts[i] (contiguous tensors of equal byte size;
+    host -- ideally page-locked -- or device) on `stream` (default: the
+    current stream of the current device): one kernel launch for the pairs
+    the device reads directly, one copy-engine transfer for each other pair.
+    More than GATHER_MAX_COPIES pairs are issued in groups."""
+    if len(dsts) != len(srcs):
+        raise ValueError("dsts and srcs differ in length")
+    for d, s in zip(dsts, srcs):
+        if not d.is_contiguous() or not s.is_contiguous():
+            raise TypeError("tensors must be contiguous")
+        if d.nbytes != s.nbytes:
+            raise ValueError("a destination and its source differ in size")
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    lib = load_library()
+    for g0 in range(0, len(dsts), GATHER_MAX_COPIES):
+        part = range(g0, min(len(dsts), g0 + GATHER_MAX_COPIES))
+        n = len(part)
+        d = (ctypes.c_void_p * n)(*[dsts[i].data_ptr() for i in part])
+        s = (ctypes.c_void_p * n)(*[srcs[i].data_ptr() for i in part])
+        b = (ctypes.c_uint64 * n)(*[srcs[i].nbytes for i in part])
+        _check(lib.sgmv_copy_gather(n, d, s, b, int(max_ctas), st), "sgmv_copy_gather")
 
 
 def sgmv_read_floor(src, nbytes, T, L, H1, H2, r, in_dtype=torch.float16, y_dtype=None):

@@ -180,6 +180,25 @@ def test_load_adapter_rejects_bad_arguments(lib, kw):
                                  None) == 1
 
 
+def test_copy_gather_rejects_bad_arguments(lib):
+    import ctypes
+
+    def arr(t, vals):
+        return (t * max(1, len(vals)))(*vals)
+
+    vp, u64 = ctypes.c_void_p, ctypes.c_uint64
+    d, s, b = arr(vp, [A16, A16]), arr(vp, [A16, A16]), arr(u64, [16, 32])
+    assert lib.sgmv_copy_gather(0, None, None, None, 0, None) == 0    # nothing to do
+    assert lib.sgmv_copy_gather(-1, d, s, b, 0, None) == 1
+    assert lib.sgmv_copy_gather(513, d, s, b, 0, None) == 1          # more than 512 copies
+    assert lib.sgmv_copy_gather(2, d, s, b, -1, None) == 1
+    assert lib.sgmv_copy_gather(2, None, s, b, 0, None) == 1
+    assert lib.sgmv_copy_gather(2, d, None, b, 0, None) == 1
+    assert lib.sgmv_copy_gather(2, d, s, None, 0, None) == 1
+    assert lib.sgmv_copy_gather(2, arr(vp, [A16, None]), s, b, 0, None) == 1
+    assert lib.sgmv_copy_gather(2, d, arr(vp, [None, A16]), b, 0, None) == 1
+
+
 def test_read_floor_rejects_bad_arguments(lib):
     def call(**kw):
         a = dict(src=A16, n=1 << 20, T=32, L=32, H1=4096, H2=4096, r=16, in_dt=0, y_dt=0)

@@ -1,7 +1,8 @@
 """On-demand adapter loading: SGMV on the slots an AdapterPool filled.
 
 Two projections (512 -> 264 and 264 -> 512, r = 16) with 4 slots serve
-batches over 6 adapters, so adapters are loaded, evicted and reloaded.  After
+batches over 6 adapters, so adapters are loaded (by the gather kernel, or by
+copy-engine transfers), evicted and reloaded.  After
 each batch: every resident slot holds its adapter's weights bit for bit, and
 SGMV on the slots gives the oracle's result computed directly from each row's
 adapter weights.
@@ -29,7 +30,8 @@ def host_adapters():
     return out
 
 
-def test_batches_through_loaded_slots():
+@pytest.mark.parametrize("gather", [True, False])
+def test_batches_through_loaded_slots(gather):
     from rank_gemv_gb300 import build, sgmv
     from rank_gemv_gb300.adapters import AdapterPool
 
@@ -39,7 +41,7 @@ def test_batches_through_loaded_slots():
     pools = [(torch.full((L, h1, R), float("nan"), dtype=torch.half, device=DEV),
               torch.full((L, R, h2), float("nan"), dtype=torch.half, device=DEV))
              for h1, h2 in PROJ]
-    pool = AdapterPool(pools, source=lambda n: weights[n])
+    pool = AdapterPool(pools, source=lambda n: weights[n], gather=gather)
     batches = [["a", "b", "c", "a"], ["d", "e", "a", "a", "b"], ["f", "b", "b", "c"],
                ["a", "f"], ["e", "d", "c", "b"]]
     g = torch.Generator().manual_seed(9)
