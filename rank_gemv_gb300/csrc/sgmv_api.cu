@@ -215,6 +215,11 @@ bool sgmv::stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32
     const int rk = r <= 16 ? 16 : r <= 32 ? 32 : 64;
     p.cl = cl;
     p.G = (int32_t)std::min<int64_t>(slots, gmax);
+    // A cluster of several CTAs gets one tile (cl * T <= #SMs above makes
+    // G = slots); only single-CTA clusters walk several tiles.  Clusters that
+    // walked several tiles each (eight CTAs, seven tiles, forced for a
+    // measurement) faulted the GPU once, cause not found: never launched.
+    if (cl > 1 && p.G < slots) return false;
     p.hc = round8(ceil_div(H1, cl));
     p.jc = round8(ceil_div(H2, cl));
     if (H2 % 256 == 0) {  // lets B chunks start on 256-column blocks (one copy each)

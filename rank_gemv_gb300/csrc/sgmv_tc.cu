@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t bar_v, b_full[kExpandBStages], b_empty[kExpandBStages];
     __shared__ __align__(8) uint64_t acc_full[4], acc_empty[4], y_full[2][kExpandYStages];
-    __shared__ int s_info[6];
-    __shared__ int s_row[kTcRows];
+    __shared__ Run s_run;
+    __shared__ int s_row[kMaxPieces][kTcRows];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
@@ -353,8 +353,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const int nblk = (H2 + N - 1) / N;
 
     if (warp == 0) {
-        find_share(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, P.kw, min_len, max_len, err,
-                   (int)blockIdx.x, (int)gridDim.x, report, s_info);
+        find_run(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, P.kw, nblk, min_len, max_len,
+                 err, (int)blockIdx.x, (int)gridDim.x, report, &s_run);
         if (lane == 0) {
             mbar_init(&bar_v, 1);
             for (int i = 0; i < nbs; ++i) {
@@ -371,12 +371,18 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         }
     }
     __syncthreads();
-    if (s_info[0] < 0) return;
-    const int p0 = s_info[1], nrows = s_info[2], a = s_info[3];
-    // this CTA's run of the tile's column blocks: an even split over its CTAs
-    const int b0 = (int)((long long)s_info[4] * nblk / s_info[5]);
-    const int nb = (int)((long long)(s_info[4] + 1) * nblk / s_info[5]) - b0;
+    // this CTA's run: blocks 0 .. nb-1 of its sequence, piece q holding
+    // blocks k0[q] .. k0[q+1]-1 = column blocks b0[q], ... of one tile
+    const int npc = s_run.n;
+    if (npc <= 0) return;
+    const int nb = s_run.k0[npc];
     if (nb <= 0) return;
+    auto piece_of = [&](int k) {
+        int q = 0;
+        while (q + 1 < npc && k >= s_run.k0[q + 1]) ++q;
+        return q;
+    };
+    auto col_of = [&](int k, int q) { return (s_run.b0[q] + k - s_run.k0[q]) * N; };
     if (warp == 0) tmem_alloc(&s_tmem, (uint32_t)(NACC * N));
 
     uint8_t *base = align1024(dsm);
@@ -389,15 +395,17 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const uint32_t ystage_bytes = (uint32_t)kTcRows * YP;
 
     if (tid < kTcRows) {
-        int row = -1;
-        if (tid < nrows) {
-            row = perm ? perm[p0 + tid] : p0 + tid;
-            if (row < 0 || row >= nrows_all) {
-                set_error(err, kErrBadIndex);
-                row = -1;
+        for (int q = 0; q < npc; ++q) {
+            int row = -1;
+            if (tid < s_run.rows[q]) {
+                row = perm ? perm[s_run.p0[q] + tid] : s_run.p0[q] + tid;
+                if (row < 0 || row >= nrows_all) {
+                    set_error(err, kErrBadIndex);
+                    row = -1;
+                }
             }
+            s_row[q][tid] = row;
         }
-        s_row[tid] = row;
     }
     tc_fence_before();
     __syncthreads();
@@ -410,11 +418,11 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         // soon as the products that read it are made
         if (lane == 0) {
             auto load_b = [&](int k) {
-                const int st = k % nbs;
+                const int st = k % nbs, q = piece_of(k), j = col_of(k, q);
                 mbar_arrive_expect_tx(&b_full[st], b_bytes);
                 for (int c = 0; c < N; c += 64)
-                    tma_load_3d(b_stage0 + (size_t)st * b_bytes + c * rk * 2, tmap_b,
-                                (b0 + k) * N + c, 0, a, &b_full[st]);
+                    tma_load_3d(b_stage0 + (size_t)st * b_bytes + c * rk * 2, tmap_b, j + c, 0,
+                                s_run.a[q], &b_full[st]);
             };
             for (int k = 0; k < min(nbs, nb); ++k) load_b(k);  // weights: before the wait
             for (int k = nbs; k < nb; ++k) {
@@ -426,24 +434,32 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             }
         }
     } else if (warp == 2 * kTcRows / 32) {
-        // ---- MMA warp: the tile's v once, then the products of block k into
-        // accumulator buffer k % NACC (read by epilogue group k & 1)
+        // ---- MMA warp: each piece's v (its tile's rows), then the products of
+        // block k into accumulator buffer k % NACC (read by epilogue group k & 1)
         if (lane == 0) {
-            pdl_wait();
-            mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);  // v: written by the shrink kernel
-            for (int kb = 0; kb < rk / kKB; ++kb) {
-                tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, p0, &bar_v);
-                tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, p0, &bar_v);
-            }
-            bool ok = mbar_wait(&bar_v, 0);
+            pdl_wait();  // v: written by the shrink kernel
+            bool ok = true;
             // after a wait runs out, later ones are skipped: the error is set
             // and every wait of the compute warps is bounded as well
             auto pwait = [&](uint64_t *bar, uint32_t par) {
                 if (ok) ok = mbar_wait(bar, par);
             };
             const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, N);
-            for (int k = 0; k < nb; ++k) {
+            for (int k = 0, q = -1; k < nb; ++k) {
                 const int st = k % nbs, ab = k % NACC;
+                if (k == 0 || k == s_run.k0[q + 1]) {
+                    ++q;
+                    // v of the next piece: once the products of the previous
+                    // block (the last to read the old v) are made.  The
+                    // epilogue is still draining up to NACC accumulators.
+                    if (k > 0) pwait(&acc_full[(k - 1) % NACC], (uint32_t)(((k - 1) / NACC) & 1));
+                    mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);
+                    for (int kb = 0; kb < rk / kKB; ++kb) {
+                        tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, s_run.p0[q], &bar_v);
+                        tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, s_run.p0[q], &bar_v);
+                    }
+                    pwait(&bar_v, (uint32_t)(q & 1));
+                }
                 pwait(&b_full[st], (uint32_t)((k / nbs) & 1));
                 if (k >= NACC) pwait(&acc_empty[ab], (uint32_t)(((k / NACC) - 1) & 1));
                 tc_fence_after();
@@ -477,18 +493,18 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         // instruction)
         auto load_y = [&](int i) {
             uint8_t *st = my_y + (size_t)(i % ny) * ystage_bytes;
-            const int j = (b0 + g + 2 * i) * N;
+            const int k = g + 2 * i, q = piece_of(k);
+            const int j = col_of(k, q);
             const int c = lt % CH;
             const bool col_ok = j + c * E16 < H2;
 #pragma unroll 4
             for (int r = lt / CH; r < kTcRows; r += RPI) {
-                const int row = s_row[r];
+                const int row = s_row[q][r];
                 if (row >= 0 && col_ok)
                     cp_async16(st + r * YP + c * 16, gY + (size_t)row * H2 + j + c * E16, 16);
             }
             cp_async_arrive(&y_full[g][i % ny]);
         };
-        const int my_row = s_row[lt];
         bool lost = false;
         auto wait = [&](uint64_t *bar, uint32_t par) {
             if (!mbar_wait(bar, par)) {
@@ -503,7 +519,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             // added in L2, so y never passes through the SM.  Stage i % ny
             // holds scale * acc of the group's i-th block, one row per thread.
             for (int i = 0; i < nmine; ++i) {
-                const int k = g + 2 * i, ab = k % NACC;
+                const int k = g + 2 * i, ab = k % NACC, q = piece_of(k);
+                const int my_row = s_row[q][lt];
                 wait(&acc_full[ab], (uint32_t)((k / NACC) & 1));
                 tc_fence_after();
                 if (i >= ny) {  // the reduction that last read this stage is done with it
@@ -527,7 +544,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
                 fence_proxy_async();  // this thread's row -> the bulk copy unit
-                const int j = (b0 + k) * N;
+                const int j = col_of(k, q);
                 if (!lost && my_row >= 0)
                     bulk_s2g_add_f32(reinterpret_cast<float *>(gY) + (size_t)my_row * H2 + j, yr,
                                      (uint32_t)min(N, H2 - j) * 4u);
@@ -537,7 +554,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         } else {
         for (int i = 0; i < min(ny, nmine); ++i) load_y(i);
         for (int i = 0; i < nmine; ++i) {
-            const int k = g + 2 * i, ab = k % NACC;
+            const int k = g + 2 * i, ab = k % NACC, q = piece_of(k);
+            const int my_row = s_row[q][lt];
             wait(&acc_full[ab], (uint32_t)((k / NACC) & 1));
             tc_fence_after();
             wait(&y_full[g][i % ny], (uint32_t)((i / ny) & 1));
@@ -566,12 +584,12 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             group_sync(g);
             // write the block back: 16-byte stores, two row pieces per warp instruction
             {
-                const int j = k * N + b0 * N;
+                const int j = col_of(k, q);
                 const int c = lt % CH;
                 if (!lost && j + c * E16 < H2) {
 #pragma unroll 4
                     for (int r = lt / CH; r < kTcRows; r += RPI) {
-                        const int row = s_row[r];
+                        const int row = s_row[q][r];
                         if (row >= 0)
                             *reinterpret_cast<uint4 *>(gY + (size_t)row * H2 + j + c * E16) =
                                 lds128(st + r * YP + c * 16);
@@ -749,9 +767,20 @@ int tc_launch_t(const TCArgs &g) {
     ep.nbs = kExpandBStages;
     ep.ny = kExpandYStages;
     auto total = [&]() { return 1024 + vb + ep.nbs * bstage + (size_t)2 * ep.ny * ystage; };
-    while (total() > kExpandSmemMax && ep.nbs > 2) --ep.nbs;
-    if (total() > kExpandSmemMax) ep.ny = 1;
-    while (total() > kExpandSmemMax && ep.nbs > 2) --ep.nbs;
+    // dynamic shared memory: what the block may have, less the kernel's static part
+    size_t cap = kExpandSmemMax;
+    {
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+            cudaFuncGetAttributes(&fa, sgmv_tc_expand_kernel<Tin, Ty>) == cudaSuccess &&
+            (size_t)optin > fa.sharedSizeBytes)
+            cap = std::min(cap, (size_t)optin - fa.sharedSizeBytes);
+    }
+    while (total() > cap && ep.nbs > 2) --ep.nbs;
+    if (total() > cap) ep.ny = 1;
+    while (total() > cap && ep.nbs > 2) --ep.nbs;
     const size_t expand_smem = total();
     return launch(sgmv_tc_expand_kernel<Tin, Ty>, ep, dim3((unsigned)nct, 1, 1), 1, expand_smem,
                   g.stream, kExpandThreads);

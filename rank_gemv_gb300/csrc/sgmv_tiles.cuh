@@ -87,21 +87,34 @@ __device__ __forceinline__ int seg_tiles(const int32_t *seg_ptr, const int32_t *
     return 0;
 }
 
-// Warp 0 of CTA c of G finds the CTA's share of the launch.  Tiles are
-// numbered as in find_tile (segments with an adapter only); tile t weighs
-// w_t = rows_t + kw, and the G CTAs are dealt to the tiles in proportion to
-// weight, at least one each: tile t gets CTAs [start_t, start_t+1) with
-//   start_t = t + floor((G - ntiles) * W_t / W),
-// W_t the weight of the tiles before t and W the total, so start_0 = 0 and
-// start_ntiles = G.  out = {segment or -1, first position, rows, adapter,
-// index of the CTA among its tile's CTAs, CTAs of the tile}.  G below the
-// number of tiles is an error (kErrBadSegments) and every CTA gets nothing.
-__device__ __forceinline__ void find_share(const int32_t *seg_ptr, const int32_t *idx, int S,
-                                           int T, int L, int rows, int kw, int min_len,
-                                           int max_len, int *err, int c, int G, bool report,
-                                           int *out) {
+// Most pieces in one CTA's run (find_run).
+constexpr int kMaxPieces = 4;
+
+// A CTA's run: pieces of consecutive column blocks, each of one tile.
+struct Run {
+    int n;                      // pieces (0: nothing to do)
+    int k0[kMaxPieces + 1];     // first block of piece i in the CTA's sequence; k0[n] = blocks
+    int p0[kMaxPieces];         // tile's first sorted position
+    int rows[kMaxPieces];       // tile's rows
+    int a[kMaxPieces];          // adapter
+    int b0[kMaxPieces];         // first column block
+};
+
+// Warp 0 of CTA c of G finds the CTA's run.  Tiles are numbered as in
+// find_tile (segments with an adapter only), each cut into nblk column
+// blocks; block b of tile t weighs rows_t + kw.  The blocks are laid end to
+// end in (tile, block) order on a line of total weight W, and CTA c takes the
+// blocks that start in [c W / G, (c+1) W / G): equal shares of weight, so a
+// run may end inside one tile and go on into the next.  With G >= ntiles and
+// rows <= kw a share is shorter than two tiles, so a run has at most three
+// pieces.  G below the number of tiles is an error (kErrBadSegments) and
+// every CTA gets nothing.
+__device__ __forceinline__ void find_run(const int32_t *seg_ptr, const int32_t *idx, int S, int T,
+                                         int L, int rows, int kw, int nblk, int min_len,
+                                         int max_len, int *err, int c, int G, bool report,
+                                         Run *out) {
     const int lane = threadIdx.x & 31;
-    // pass 1: number of tiles and total weight
+    // pass 1: number of tiles and total weight per column block
     int ntiles = 0;
     long long wsum = 0;
     for (int s0 = 0; s0 < S; s0 += 32) {
@@ -117,76 +130,78 @@ __device__ __forceinline__ void find_share(const int32_t *seg_ptr, const int32_t
         ntiles += n;
         wsum += w;
     }
-    int f_s = -1, f_p0 = 0, f_n = 0, f_a = -1, f_i = 0, f_c = 0;
-    const long long E = (long long)G - ntiles;
-    if (E < 0 && report && lane == 0) set_error(err, kErrBadSegments);
-    if (E >= 0 && ntiles > 0) {
-        // pass 2: the segment, then the tile, whose CTAs include c
-        auto start = [&](long long t, long long wpre) { return t + E * wpre / wsum; };
-        int tbase = 0;
-        long long wbase = 0;
-        for (int s0 = 0; s0 < S; s0 += 32) {
+    int np = 0;
+    if (ntiles > G && report && lane == 0) set_error(err, kErrBadSegments);
+    if (ntiles > 0 && ntiles <= G) {
+        const long long W = (long long)nblk * wsum;
+        const long long lo = (long long)c * W / G, hi = (long long)(c + 1) * W / G;
+        const long long full = (long long)nblk * (rows + kw);  // weight of a full tile
+        long long wbase = 0;  // weight of the segments before this batch
+        for (int s0 = 0; s0 < S && lo < hi; s0 += 32) {
             const int s = s0 + lane;
             int n = 0, b = 0, e = 0, a = -1;
             if (s < S) n = seg_tiles(seg_ptr, idx, s, T, L, rows, min_len, max_len, err, false, b, e, a);
-            const long long w = n > 0 ? (long long)(e - b) + (long long)kw * n : 0;
-            int in = n;
+            const long long w = n > 0 ? (long long)nblk * ((long long)(e - b) + (long long)kw * n) : 0;
             long long iw = w;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int vn = __shfl_up_sync(0xffffffffu, in, off);
-                const long long vw = __shfl_up_sync(0xffffffffu, iw, off);
-                if (lane >= off) {
-                    in += vn;
-                    iw += vw;
-                }
+                const long long v = __shfl_up_sync(0xffffffffu, iw, off);
+                if (lane >= off) iw += v;
             }
-            const int t0 = tbase + in - n;       // first tile of segment s
-            const long long w0 = wbase + iw - w;  // weight before it
-            const bool mine = n > 0 && c >= start(t0, w0) && c < start(t0 + n, w0 + w);
-            const unsigned m = __ballot_sync(0xffffffffu, mine);
-            if (m) {
-                if (mine) {
-                    // last tile j of the segment with start <= c (all but the
-                    // segment's last tile have `rows` rows)
-                    const long long wf = (long long)rows + kw;
-                    int lo = 0, hi = n - 1;
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (start(t0 + mid, w0 + mid * wf) <= c) lo = mid;
-                        else hi = mid - 1;
+            const long long ws = wbase + iw - w;  // where segment s starts on the line
+            // this segment's pieces: tiles j whose blocks start in [lo, hi)
+            // (one entry more than a run holds, so that an overflow is seen)
+            int cnt = 0, pj[kMaxPieces + 1], pb[kMaxPieces + 1], pn[kMaxPieces + 1];
+            if (n > 0 && ws < hi && ws + w > lo) {
+                int j = lo > ws ? (int)min((long long)(n - 1), (lo - ws) / full) : 0;
+                for (; j < n && cnt <= kMaxPieces; ++j) {
+                    const long long wt = ws + (long long)j * full;  // tiles before j are full
+                    if (wt >= hi) break;
+                    const int nr = min(rows, (e - b) - j * rows);
+                    const long long wb = (long long)(nr + kw);
+                    const long long f = lo > wt ? (lo - wt + wb - 1) / wb : 0;
+                    const long long l = min((long long)nblk, (hi - wt + wb - 1) / wb);
+                    if (f < l) {
+                        pj[cnt] = j;
+                        pb[cnt] = (int)f;
+                        pn[cnt] = (int)(l - f);
+                        ++cnt;
                     }
-                    const int p0 = b + lo * rows, nr = min(rows, e - p0);
-                    const long long st = start(t0 + lo, w0 + lo * wf);
-                    const long long nx = start(t0 + lo + 1, w0 + lo * wf + nr + kw);
-                    f_s = s;
-                    f_p0 = p0;
-                    f_n = nr;
-                    f_a = a;
-                    f_i = (int)(c - st);
-                    f_c = (int)(nx - st);
                 }
-                const int src = __ffs(m) - 1;
-                f_s = __shfl_sync(0xffffffffu, f_s, src);
-                f_p0 = __shfl_sync(0xffffffffu, f_p0, src);
-                f_n = __shfl_sync(0xffffffffu, f_n, src);
-                f_a = __shfl_sync(0xffffffffu, f_a, src);
-                f_i = __shfl_sync(0xffffffffu, f_i, src);
-                f_c = __shfl_sync(0xffffffffu, f_c, src);
-                break;
             }
-            tbase += __shfl_sync(0xffffffffu, in, 31);
+            int ic = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, ic, off);
+                if (lane >= off) ic += v;
+            }
+            for (int q = 0; q < cnt; ++q) {
+                const int slot = np + ic - cnt + q;
+                if (slot < kMaxPieces) {
+                    out->p0[slot] = b + pj[q] * rows;
+                    out->rows[slot] = min(rows, (e - b) - pj[q] * rows);
+                    out->a[slot] = a;
+                    out->b0[slot] = pb[q];
+                    out->k0[slot + 1] = pn[q];  // a count here; prefix sums below
+                }
+            }
+            np += __shfl_sync(0xffffffffu, ic, 31);
             wbase += __shfl_sync(0xffffffffu, iw, 31);
+            // segments after this batch start at or beyond wbase
+            if (wbase >= hi) break;
+        }
+        if (np > kMaxPieces) {
+            if (lane == 0) set_error(err, kErrBadSegments);
+            np = 0;
         }
     }
+    __syncwarp();
     if (lane == 0) {
-        out[0] = f_s;
-        out[1] = f_p0;
-        out[2] = f_n;
-        out[3] = f_a;
-        out[4] = f_i;
-        out[5] = f_c;
+        out->n = np;
+        out->k0[0] = 0;
+        for (int q = 0; q < np; ++q) out->k0[q + 1] += out->k0[q];
     }
+    __syncwarp();
 }
 
 }  // namespace sgmv
