@@ -10,6 +10,7 @@
 #include "sgmv.h"
 #include "sgmv_internal.h"
 #include "sgmv_fused.h"
+#include "sgmv_gather.h"
 
 // Sticky device error word of this library (first reported status wins).
 __device__ int g_sgmv_error;

@@ -15,7 +15,7 @@
 #include <algorithm>
 
 #include "sgmv_device.cuh"
-#include "sgmv_internal.h"
+#include "sgmv_gather.h"
 
 namespace sgmv {
 namespace {

@@ -208,15 +208,6 @@ int read_floor_launch(const void *src, uint64_t bytes, int cl, int G, int nst, u
                       int *err, cudaStream_t stream);
 
 
-// Most copies of one sgmv_copy_gather call (they travel in the kernel's
-// parameters: 32 bytes each).
-constexpr int kGatherMaxCopies = 512;
-// One launch of the gather kernel (sgmv_gather.cu): every source
-// device-accessible, every pointer 16-byte aligned, every size a multiple of
-// 16; at most max_ctas CTAs.  Returns a cudaError_t value.
-int gather_launch(int32_t n, void *const *dst, const void *const *src, const uint64_t *bytes,
-                  int max_ctas, cudaStream_t stream);
-
 // Records a failed CUDA call for sgmv_last_error_string (calling thread).
 void note_cuda_error(const char *what, cudaError_t e);
 
