@@ -394,19 +394,6 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     uint8_t *y_stage0 = b_stage0 + (size_t)nbs * b_bytes;  // [2 groups][ny][128 rows][YP]
     const uint32_t ystage_bytes = (uint32_t)kTcRows * YP;
 
-    if (tid < kTcRows) {
-        for (int q = 0; q < npc; ++q) {
-            int row = -1;
-            if (tid < s_run.rows[q]) {
-                row = perm ? perm[s_run.p0[q] + tid] : s_run.p0[q] + tid;
-                if (row < 0 || row >= nrows_all) {
-                    set_error(err, kErrBadIndex);
-                    row = -1;
-                }
-            }
-            s_row[q][tid] = row;
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -487,6 +474,31 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         // thread, TMEM lanes of warp % 4) takes blocks g, g + 2, ...
         const int g = warp >> 2, lt = tid & (kTcRows - 1);
         const int nmine = (nb - g + 1) >> 1;  // blocks of this group
+        // physical rows of the pieces' tiles (group g looks up pieces g, g + 2;
+        // the loads are independent, so they are in flight together)
+        {
+            int row[(kMaxPieces + 1) / 2];
+            bool in[(kMaxPieces + 1) / 2];
+#pragma unroll
+            for (int h = 0; h < (kMaxPieces + 1) / 2; ++h) {
+                const int q = g + 2 * h;
+                in[h] = q < npc && lt < s_run.rows[q];
+                row[h] = -1;
+                if (in[h]) row[h] = perm ? perm[s_run.p0[q] + lt] : s_run.p0[q] + lt;
+            }
+#pragma unroll
+            for (int h = 0; h < (kMaxPieces + 1) / 2; ++h) {
+                const int q = g + 2 * h;
+                if (q >= npc) continue;
+                if (in[h] && (row[h] < 0 || row[h] >= nrows_all)) {
+                    set_error(err, kErrBadIndex);
+                    row[h] = -1;
+                }
+                s_row[q][lt] = row[h];
+            }
+            // both groups' rows are in (the two epilogue groups only)
+            asm volatile("bar.sync 3, %0;" ::"n"(2 * kTcRows) : "memory");
+        }
         uint8_t *my_y = y_stage0 + (size_t)g * ny * ystage_bytes;
         // y of the group's i-th block into stage i % ny: thread lt copies chunk
         // lt % CH of rows lt / CH + RPI * j (two 256-byte row pieces per warp

@@ -87,8 +87,8 @@ __device__ __forceinline__ int seg_tiles(const int32_t *seg_ptr, const int32_t *
     return 0;
 }
 
-// Most pieces in one CTA's run (find_run).
-constexpr int kMaxPieces = 4;
+// Most pieces in one CTA's run (find_run): three, see there.
+constexpr int kMaxPieces = 3;
 
 // A CTA's run: pieces of consecutive column blocks, each of one tile.
 struct Run {
@@ -105,10 +105,12 @@ struct Run {
 // blocks; block b of tile t weighs rows_t + kw.  The blocks are laid end to
 // end in (tile, block) order on a line of total weight W, and CTA c takes the
 // blocks that start in [c W / G, (c+1) W / G): equal shares of weight, so a
-// run may end inside one tile and go on into the next.  With G >= ntiles and
-// rows <= kw a share is shorter than two tiles, so a run has at most three
-// pieces.  G below the number of tiles is an error (kErrBadSegments) and
-// every CTA gets nothing.
+// run may end inside one tile and go on into the next.  With G >= ntiles a
+// share weighs at most nblk (rows + kw) + 1, a tile at least nblk (1 + kw);
+// with kw > rows - 2 no share holds two whole tiles, so a run has at most
+// three pieces (the end of one tile, a whole one, the start of the next).  G
+// below the number of tiles is an error (kErrBadSegments) and every CTA gets
+// nothing.
 __device__ __forceinline__ void find_run(const int32_t *seg_ptr, const int32_t *idx, int S, int T,
                                          int L, int rows, int kw, int nblk, int min_len,
                                          int max_len, int *err, int c, int G, bool report,

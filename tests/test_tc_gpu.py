@@ -128,6 +128,25 @@ def test_ragged_dims(H1, H2):
     assert_close(y, ref, f"H1={H1} H2={H2}")
 
 
+@pytest.mark.parametrize("y_dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("H2", [1000, 4096])
+def test_runs_cross_tiles(y_dtype, H2):
+    """The expand's CTAs take equal weighted shares of the (tile, column
+    block) line, so most runs end inside one tile and go on into the next:
+    tiles of 128, 77, 5, 64 and 128 + 1 rows (shuffled rows), every block
+    updated exactly once, each piece with its own rows and adapter."""
+    lens = [205, 5, 64, 129]
+    ra = torch.tensor([3, 0, 2, 1], dtype=torch.int32).repeat_interleave(torch.tensor(lens))
+    g = torch.Generator().manual_seed(21)
+    ra = ra[torch.randperm(len(ra), generator=g)]
+    w = wl.draw(len(ra), 4, 256, H2, 64, ra, dtype=torch.float16, y_dtype=y_dtype, y0="randn",
+                seed=H2)
+    y = run(w)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(y, ref, f"H2={H2} y {y_dtype}")
+
+
 @pytest.mark.parametrize("y_dtype", [torch.float32, torch.bfloat16])
 def test_more_tiles_than_sms(y_dtype):
     """More 128-row tiles than SMs: the expand's grid is a multiple of the SM
