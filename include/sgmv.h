@@ -146,8 +146,11 @@ int sgmv_build_segments_device(const int32_t *row_adapter, int32_t T, int32_t L,
 
 /*
  * Bytes of device workspace that lets sgmv_apply use its tensor-core path for
- * long segments.  sgmv_apply also accepts workspace == NULL with
- * workspace_bytes == 0 and then runs every segment on the CUDA-core path.
+ * long segments: v for T rows as two 16-bit halves, plus 256 bytes for a
+ * counter the tensor-core kernels use to share out the last part of the
+ * work.  Calls that run at the same time need separate workspaces.
+ * sgmv_apply also accepts workspace == NULL with workspace_bytes == 0 and
+ * then runs every segment on the CUDA-core path.
  */
 size_t sgmv_workspace_bytes(int32_t T, int32_t H1, int32_t H2, int32_t r);
 

@@ -371,9 +371,10 @@ size_t sgmv_workspace_bytes(int32_t T, int32_t H1, int32_t H2, int32_t r) {
     (void)H1;
     (void)H2;
     if (T <= 0 || r <= 0) return 0;
-    // v as two 16-bit halves, [T][r] each, the second one 256-byte aligned
+    // v as two 16-bit halves, [T][r] each, 256-byte aligned, then 256 bytes
+    // for the tensor-core expand's claim counter
     const size_t half = ((size_t)T * (size_t)r * 2u + 255u) / 256u * 256u;
-    return 2u * half;
+    return 2u * half + 256u;
 }
 
 int sgmv_shrink(float *v, const void *x, const void *A, int in_dtype, const int32_t *perm,
@@ -603,7 +604,7 @@ int sgmv_apply(void *y, int y_dtype, const void *x, const void *A, const void *B
     g.seg_ptr = seg_ptr;
     g.idx = idx;
     g.err = err;
-    const size_t half = sgmv_workspace_bytes(T, H1, H2, r) / 2;
+    const size_t half = ((size_t)T * (size_t)r * 2u + 255u) / 256u * 256u;
     g.vhi = workspace;
     g.vlo = static_cast<uint8_t *>(workspace) + half;
     g.S = S;

@@ -19,11 +19,15 @@
 //   written as two 16-bit halves, hi = round(v) and lo = round(v - hi), so
 //   the expand can run on 16-bit tensor cores and still see v to about
 //   16 significant bits.
-// Expand (sgmv_tc_expand_kernel): one CTA per (128-row tile, run of column
-//   blocks of N = 64 (fp32 y) or 128 columns), one CTA per SM in all; the
-//   CTAs are dealt to the tiles in proportion to each tile's cost (its rows
-//   plus a fixed cost per block).  The tile's v hi/lo is loaded once (TMA,
-//   K-major).  A B warp streams B[a][:, j:j+N] (N-major) through a ring; the
+// Expand (sgmv_tc_expand_kernel): one CTA per SM.  The (128-row tile,
+//   column block of N = 64 (fp32 y) or 128 columns) pairs lie end to end,
+//   each weighing its tile's rows plus a fixed cost per block; each CTA takes
+//   an equal share of the first part of that line (a run that may cross into
+//   the next tile) and, with fp32 y, then claims blocks of the rest four at a
+//   time from a counter the shrink kernel zeroed.  v hi/lo of a block's tile
+//   is loaded by TMA (K-major) whenever the tile changes.  A B warp streams
+//   B[a][:, j:j+N] (N-major) through a ring and hands claimed blocks (column,
+//   tile, rows) to the other warps through a ring of descriptors; the
 //   MMA warp makes 2 x r/16 MMAs per block, v_hi.B + v_lo.B, into one of
 //   four (fp32 y) or two TMEM buffers, so it runs up to that many blocks
 //   ahead of the epilogue.  Two epilogue groups take alternate blocks; each
@@ -69,6 +73,7 @@ struct TCShrinkParams {
     const int32_t *perm, *seg_ptr, *idx;
     int *err;
     void *vhi, *vlo;     // [T][r] each, input type
+    int *claim;          // the expand's claim counter: zeroed here
     int32_t S, T, L, H1, r, hk, cl, min_len, max_len;
 };
 
@@ -84,7 +89,19 @@ struct TCExpandParams {
     int32_t red;  // fp32 y updated by bulk reductions in L2 (H2 % 4 == 0)
     int32_t ny;   // y stages per epilogue group (1 or 2)
     int32_t nbs;  // B stages (2 .. kExpandBStages)
+    int *claim;      // counter of claimed chunks (zeroed by the shrink kernel)
+    int32_t sfrac;   // static part of the work line in 64ths (64: no claiming)
+    int32_t chunk;   // column blocks per claim
     float scale;
+};
+
+// Claimed blocks of the expand: descriptors handed from the B warp (which
+// claims) to the MMA warp and the epilogue group of the block.
+constexpr int kDynSlots = 4;  // descriptors in flight
+constexpr int kDynAhead = 3;  // block k is claimed once block k - 3 has left its accumulator
+struct DynSlot {
+    int col, p0, end, pad;
+    int row[kTcRows];
 };
 
 // ---------------------------------------------------------------- shrink
@@ -187,6 +204,9 @@ __global__ void __launch_bounds__(kTcThreads)
         cp_async_arrive(&full[st]);
     };
     pdl_wait();
+    // the expand that follows claims blocks from this counter (the previous
+    // kernel, which may have used it, is complete)
+    if (P.claim && report && tid == 0) *P.claim = 0;
     if (prod >= 0)
         for (int kb = 0; kb < min(nkb, kStages); ++kb) issue_x(kb);
     pdl_trigger();
@@ -344,8 +364,11 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     extern __shared__ __align__(1024) uint8_t dsm[];
     __shared__ __align__(8) uint64_t bar_v, b_full[kExpandBStages], b_empty[kExpandBStages];
     __shared__ __align__(8) uint64_t acc_full[4], acc_empty[4], y_full[2][kExpandYStages];
+    __shared__ __align__(8) uint64_t d_full[kDynSlots], d_empty[kDynSlots];
     __shared__ Run s_run;
+    __shared__ DynTable s_dyn;
     __shared__ int s_row[kMaxPieces][kTcRows];
+    __shared__ __align__(16) DynSlot s_slot[kDynSlots];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool report = blockIdx.x == 0 && blockIdx.y == 0;
@@ -354,9 +377,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 
     if (warp == 0) {
         find_run(seg_ptr, idx, nseg, nrows_all, nadapters, kTcRows, P.kw, nblk, min_len, max_len,
-                 err, (int)blockIdx.x, (int)gridDim.x, report, &s_run);
+                 err, (int)blockIdx.x, (int)gridDim.x, report, P.sfrac, &s_run, &s_dyn);
         if (lane == 0) {
             mbar_init(&bar_v, 1);
+            for (int i = 0; i < kDynSlots; ++i) {
+                mbar_init(&d_full[i], 1);                // the B warp, once it is written
+                mbar_init(&d_empty[i], 1 + kTcRows);     // the MMA warp + the epilogue group's threads
+            }
             for (int i = 0; i < nbs; ++i) {
                 mbar_init(&b_full[i], 1);
                 mbar_init(&b_empty[i], 1);
@@ -371,12 +398,15 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         }
     }
     __syncthreads();
-    // this CTA's run: blocks 0 .. nb-1 of its sequence, piece q holding
-    // blocks k0[q] .. k0[q+1]-1 = column blocks b0[q], ... of one tile
+    // this CTA's static run: blocks 0 .. nb-1 of its sequence, piece q
+    // holding blocks k0[q] .. k0[q+1]-1 = column blocks b0[q], ... of one
+    // tile; then, when the work line has a claimed part, blocks nb, nb+1, ...
+    // claimed at run time (P.chunk at a time) until none is left
     const int npc = s_run.n;
-    if (npc <= 0) return;
-    const int nb = s_run.k0[npc];
-    if (nb <= 0) return;
+    const int nb = npc > 0 ? s_run.k0[npc] : 0;
+    const bool dyn = s_dyn.n > 0;
+    const int nd = dyn ? s_dyn.d0[s_dyn.n] : 0;
+    if (nb <= 0 && !dyn) return;
     auto piece_of = [&](int k) {
         int q = 0;
         while (q + 1 < npc && k >= s_run.k0[q + 1]) ++q;
@@ -402,22 +432,110 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 
     if (warp == 2 * kTcRows / 32 + 1) {
         // ---- B warp: B[a][:, block k] through the ring, a stage refilled as
-        // soon as the products that read it are made
+        // soon as the products that read it are made; it also claims the
+        // blocks after the static run and hands them on in s_slot
+        auto load_b_at = [&](int k, int j, int a) {
+            const int st = k % nbs;
+            mbar_arrive_expect_tx(&b_full[st], b_bytes);
+            for (int c = 0; c < N; c += 64)
+                tma_load_3d(b_stage0 + (size_t)st * b_bytes + c * rk * 2, tmap_b, j + c, 0, a,
+                            &b_full[st]);
+        };
+        bool ok = true;
         if (lane == 0) {
             auto load_b = [&](int k) {
-                const int st = k % nbs, q = piece_of(k), j = col_of(k, q);
-                mbar_arrive_expect_tx(&b_full[st], b_bytes);
-                for (int c = 0; c < N; c += 64)
-                    tma_load_3d(b_stage0 + (size_t)st * b_bytes + c * rk * 2, tmap_b, j + c, 0,
-                                s_run.a[q], &b_full[st]);
+                const int q = piece_of(k);
+                load_b_at(k, col_of(k, q), s_run.a[q]);
             };
             for (int k = 0; k < min(nbs, nb); ++k) load_b(k);  // weights: before the wait
             for (int k = nbs; k < nb; ++k) {
                 if (!mbar_wait(&b_empty[k % nbs], (uint32_t)(((k / nbs) - 1) & 1))) {
                     set_error(err, kErrTimeout);
+                    ok = false;
                     break;
                 }
                 load_b(k);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (dyn && ok) {
+            pdl_wait();  // the counter is zeroed by the shrink kernel
+            int pj = 0, pend = 0;  // claimed blocks not handed on yet: pj .. pj + pend - 1
+            for (int k = nb, kd = 0;; ++k, ++kd) {
+                const int sl = kd % kDynSlots;
+                // claim late: once block k - kDynAhead has left its accumulator
+                // (with NACC >= kDynAhead that phase cannot have been passed)
+                if (k >= kDynAhead)
+                    ok = mbar_wait(&acc_empty[(k - kDynAhead) % NACC],
+                                   (uint32_t)(((k - kDynAhead) / NACC) & 1));
+                if (ok && kd >= kDynSlots)
+                    ok = mbar_wait(&d_empty[sl], (uint32_t)(((kd / kDynSlots) - 1) & 1));
+                ok = __all_sync(0xffffffffu, ok);  // one decision for the whole warp
+                if (!ok) {
+                    if (lane == 0) set_error(err, kErrTimeout);
+                    break;
+                }
+                if (pend == 0) {
+                    int c0 = 0;
+                    if (lane == 0) c0 = atomicAdd(P.claim, 1);
+                    c0 = __shfl_sync(0xffffffffu, c0, 0);
+                    pj = c0 * P.chunk;
+                    pend = max(0, min(P.chunk, nd - pj));
+                }
+                DynSlot *ds = &s_slot[sl];
+                if (pend == 0) {
+                    // nothing left: an end mark here and in the next slot (the
+                    // next block of the other epilogue group)
+                    if (lane == 0) {
+                        ds->end = 1;
+                        mbar_arrive(&d_full[sl]);
+                    }
+                    const int kd2 = kd + 1, sl2 = kd2 % kDynSlots;
+                    if (kd2 >= kDynSlots)
+                        ok = mbar_wait(&d_empty[sl2], (uint32_t)(((kd2 / kDynSlots) - 1) & 1));
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        if (lane == 0) set_error(err, kErrTimeout);
+                        break;
+                    }
+                    if (lane == 0) {
+                        s_slot[sl2].end = 1;
+                        mbar_arrive(&d_full[sl2]);
+                    }
+                    break;
+                }
+                const int j = pj++;
+                --pend;
+                int t = 0;  // the tile of claimed block j
+                while (t + 1 < s_dyn.n && j >= s_dyn.d0[t + 1]) ++t;
+                const int col = (s_dyn.b0[t] + j - s_dyn.d0[t]) * N, p0 = s_dyn.p0[t];
+                const int nr = s_dyn.rows[t];
+                for (int r = lane; r < kTcRows; r += 32) {
+                    int row = -1;
+                    if (r < nr) {
+                        row = perm ? perm[p0 + r] : p0 + r;
+                        if (row < 0 || row >= nrows_all) {
+                            set_error(err, kErrBadIndex);
+                            row = -1;
+                        }
+                    }
+                    ds->row[r] = row;
+                }
+                if (lane == 0) {
+                    ds->col = col;
+                    ds->p0 = p0;
+                    ds->end = 0;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_full[sl]);
+                // its B, once the stage is free (the whole warp waits)
+                if (k >= nbs) ok = mbar_wait(&b_empty[k % nbs], (uint32_t)(((k / nbs) - 1) & 1));
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) set_error(err, kErrTimeout);
+                    break;
+                }
+                if (lane == 0) load_b_at(k, col, s_dyn.a[t]);
+                __syncwarp();
             }
         }
     } else if (warp == 2 * kTcRows / 32) {
@@ -432,20 +550,33 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                 if (ok) ok = mbar_wait(bar, par);
             };
             const uint32_t idesc = idesc_f16(std::is_same<Tin, __nv_bfloat16>::value, kTcRows, N);
-            for (int k = 0, q = -1; k < nb; ++k) {
+            int vp0 = -1, nv = 0;  // tile (first position) of the v in shared memory; v loads
+            for (int k = 0;; ++k) {
                 const int st = k % nbs, ab = k % NACC;
-                if (k == 0 || k == s_run.k0[q + 1]) {
-                    ++q;
-                    // v of the next piece: once the products of the previous
+                int p0;
+                if (k < nb) {
+                    p0 = s_run.p0[piece_of(k)];
+                } else {
+                    if (!dyn) break;
+                    const int kd = k - nb, sl = kd % kDynSlots;
+                    pwait(&d_full[sl], (uint32_t)((kd / kDynSlots) & 1));
+                    if (!ok || s_slot[sl].end) break;
+                    p0 = s_slot[sl].p0;
+                    mbar_arrive(&d_empty[sl]);
+                }
+                if (p0 != vp0) {
+                    // v of another tile: once the products of the previous
                     // block (the last to read the old v) are made.  The
                     // epilogue is still draining up to NACC accumulators.
                     if (k > 0) pwait(&acc_full[(k - 1) % NACC], (uint32_t)(((k - 1) / NACC) & 1));
                     mbar_arrive_expect_tx(&bar_v, 2 * v_bytes);
                     for (int kb = 0; kb < rk / kKB; ++kb) {
-                        tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, s_run.p0[q], &bar_v);
-                        tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, s_run.p0[q], &bar_v);
+                        tma_load_2d(vhi_tile + kb * 16384, tmap_vhi, kb * kKB, p0, &bar_v);
+                        tma_load_2d(vlo_tile + kb * 16384, tmap_vlo, kb * kKB, p0, &bar_v);
                     }
-                    pwait(&bar_v, (uint32_t)(q & 1));
+                    pwait(&bar_v, (uint32_t)(nv & 1));
+                    ++nv;
+                    vp0 = p0;
                 }
                 pwait(&b_full[st], (uint32_t)((k / nbs) & 1));
                 if (k >= NACC) pwait(&acc_empty[ab], (uint32_t)(((k / NACC) - 1) & 1));
@@ -530,9 +661,23 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             // fp32 y: y += scale * acc by one bulk reduction per row and block,
             // added in L2, so y never passes through the SM.  Stage i % ny
             // holds scale * acc of the group's i-th block, one row per thread.
-            for (int i = 0; i < nmine; ++i) {
-                const int k = g + 2 * i, ab = k % NACC, q = piece_of(k);
-                const int my_row = s_row[q][lt];
+            for (int i = 0;; ++i) {
+                const int k = g + 2 * i, ab = k % NACC;
+                int my_row, j;
+                if (k < nb) {
+                    const int q = piece_of(k);
+                    my_row = s_row[q][lt];
+                    j = col_of(k, q);
+                } else {
+                    // a claimed block: its descriptor, then the slot back
+                    if (!dyn) break;
+                    const int kd = k - nb, sl = kd % kDynSlots;
+                    wait(&d_full[sl], (uint32_t)((kd / kDynSlots) & 1));
+                    if (lost || s_slot[sl].end) break;
+                    my_row = s_slot[sl].row[lt];
+                    j = s_slot[sl].col;
+                    mbar_arrive(&d_empty[sl]);
+                }
                 wait(&acc_full[ab], (uint32_t)((k / NACC) & 1));
                 tc_fence_after();
                 if (i >= ny) {  // the reduction that last read this stage is done with it
@@ -556,7 +701,6 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
                 fence_proxy_async();  // this thread's row -> the bulk copy unit
-                const int j = col_of(k, q);
                 if (!lost && my_row >= 0)
                     bulk_s2g_add_f32(reinterpret_cast<float *>(gY) + (size_t)my_row * H2 + j, yr,
                                      (uint32_t)min(N, H2 - j) * 4u);
@@ -564,6 +708,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             }
             bulk_wait_all();
         } else {
+        // (16-bit y: static runs only, the host asks for no claiming)
         for (int i = 0; i < min(ny, nmine); ++i) load_y(i);
         for (int i = 0; i < nmine; ++i) {
             const int k = g + 2 * i, ab = k % NACC, q = piece_of(k);
@@ -721,6 +866,10 @@ int tc_launch_t(const TCArgs &g) {
     sp.err = g.err;
     sp.vhi = g.vhi;
     sp.vlo = g.vlo;
+    // the claim counter: the workspace's 256 bytes after v's two halves
+    int *const claim = reinterpret_cast<int *>(static_cast<uint8_t *>(g.vlo) +
+                                               ((size_t)g.T * g.r * es + 255u) / 256u * 256u);
+    sp.claim = claim;
     sp.S = g.S;
     sp.T = g.T;
     sp.L = g.L;
@@ -773,6 +922,17 @@ int tc_launch_t(const TCArgs &g) {
     ep.kw = (int32_t)std::max<int64_t>(1, g.r / (int64_t)sizeof(Ty)) + kExpandBlockRows;
     // fp32 rows of whole 16-byte pieces: y += delta by bulk reductions
     ep.red = std::is_same<Ty, float>::value && g.H2 % 4 == 0 ? 1 : 0;
+    // With bulk reductions, the last quarter of the work line is claimed at
+    // run time, four column blocks at a time: CTAs on SMs that stream faster
+    // take more of it (CTAs with equal static shares end up to 1.7x apart).
+    // Measured on the prefill batch (µs per call back to back): 57.8-58.0
+    // against 59.2 with no claiming; a claimed 3/8 took 59.5-61.5, claims of
+    // two or six blocks 59.2-59.8.
+    // (claiming relies on NACC >= kDynAhead accumulators, true for fp32 y)
+    static_assert(256 / tc_cols<float>() >= kDynAhead, "claims run too far ahead");
+    ep.claim = claim;
+    ep.sfrac = ep.red ? 48 : 64;
+    ep.chunk = 4;
     // v once, B ring, two y stages per epilogue group: as deep as fits
     const size_t vb = (size_t)2 * g.r * 256, bstage = (size_t)g.r * N * 2;
     const size_t ystage = (size_t)kTcRows * tc_ypitch<Ty>();

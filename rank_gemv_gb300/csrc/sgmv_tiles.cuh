@@ -100,21 +100,36 @@ struct Run {
     int b0[kMaxPieces];         // first column block
 };
 
+// The blocks claimed at run time (find_run): the tiles from the first one with
+// a block past the static part of the line to the last, at most kMaxDyn.
+constexpr int kMaxDyn = 32;
+struct DynTable {
+    int n;                  // tiles (0: every block is dealt statically)
+    int d0[kMaxDyn + 1];    // first claimed block of tile i; d0[n] = claimed blocks
+    int p0[kMaxDyn];        // tile's first sorted position
+    int rows[kMaxDyn];      // tile's rows
+    int a[kMaxDyn];         // adapter
+    int b0[kMaxDyn];        // first claimed column block of the tile
+};
+
 // Warp 0 of CTA c of G finds the CTA's run.  Tiles are numbered as in
 // find_tile (segments with an adapter only), each cut into nblk column
 // blocks; block b of tile t weighs rows_t + kw.  The blocks are laid end to
-// end in (tile, block) order on a line of total weight W, and CTA c takes the
-// blocks that start in [c W / G, (c+1) W / G): equal shares of weight, so a
-// run may end inside one tile and go on into the next.  With G >= ntiles a
-// share weighs at most nblk (rows + kw) + 1, a tile at least nblk (1 + kw);
-// with kw > rows - 2 no share holds two whole tiles, so a run has at most
-// three pieces (the end of one tile, a whole one, the start of the next).  G
-// below the number of tiles is an error (kErrBadSegments) and every CTA gets
-// nothing.
+// end in (tile, block) order on a line of total weight W.  The blocks that
+// start before Ws = W sfrac / 64 are dealt statically: CTA c takes those that
+// start in [c Ws / G, (c+1) Ws / G), equal shares of weight, so a run may end
+// inside one tile and go on into the next.  With G >= ntiles a share weighs
+// at most nblk (rows + kw) + 1, a tile at least nblk (1 + kw); with
+// kw > rows - 2 no share holds two whole tiles, so a run has at most three
+// pieces (the end of one tile, a whole one, the start of the next).  The
+// blocks from Ws on, in the same order, are listed in *dyn for the CTAs to
+// claim at run time; when they span more than kMaxDyn tiles (or sfrac is 64)
+// the whole line is dealt statically and dyn->n is 0.  G below the number of
+// tiles is an error (kErrBadSegments) and every CTA gets nothing.
 __device__ __forceinline__ void find_run(const int32_t *seg_ptr, const int32_t *idx, int S, int T,
                                          int L, int rows, int kw, int nblk, int min_len,
                                          int max_len, int *err, int c, int G, bool report,
-                                         Run *out) {
+                                         int sfrac, Run *out, DynTable *dyn) {
     const int lane = threadIdx.x & 31;
     // pass 1: number of tiles and total weight per column block
     int ntiles = 0;
@@ -132,12 +147,59 @@ __device__ __forceinline__ void find_run(const int32_t *seg_ptr, const int32_t *
         ntiles += n;
         wsum += w;
     }
-    int np = 0;
+    int np = 0, nd = 0;
     if (ntiles > G && report && lane == 0) set_error(err, kErrBadSegments);
     if (ntiles > 0 && ntiles <= G) {
         const long long W = (long long)nblk * wsum;
-        const long long lo = (long long)c * W / G, hi = (long long)(c + 1) * W / G;
         const long long full = (long long)nblk * (rows + kw);  // weight of a full tile
+        long long Ws = W;
+        if (sfrac < 64) {
+            // the claimed part: tiles j >= jd of each segment, jd the first
+            // whose last block starts at or after Wd
+            const long long Wd = W * sfrac / 64;
+            long long wbase = 0;
+            for (int s0 = 0; s0 < S && nd <= kMaxDyn; s0 += 32) {
+                const int s = s0 + lane;
+                int n = 0, b = 0, e = 0, a = -1;
+                if (s < S) n = seg_tiles(seg_ptr, idx, s, T, L, rows, min_len, max_len, err, false, b, e, a);
+                const long long w = n > 0 ? (long long)nblk * ((long long)(e - b) + (long long)kw * n) : 0;
+                long long iw = w;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const long long v = __shfl_up_sync(0xffffffffu, iw, off);
+                    if (lane >= off) iw += v;
+                }
+                const long long ws = wbase + iw - w;
+                int jd = n, f0 = 0;
+                if (n > 0 && ws + w > Wd) {
+                    jd = Wd > ws ? (int)min((long long)(n - 1), (Wd - ws) / full) : 0;
+                    const long long wt = ws + (long long)jd * full;
+                    const long long wb = (long long)(min(rows, (e - b) - jd * rows) + kw);
+                    const long long f = Wd > wt ? (Wd - wt + wb - 1) / wb : 0;
+                    if (f >= nblk) ++jd;
+                    else f0 = (int)f;
+                }
+                const int cnt = n - jd;
+                int ic = cnt;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, ic, off);
+                    if (lane >= off) ic += v;
+                }
+                for (int q = 0; q < cnt && nd + ic - cnt + q < kMaxDyn; ++q) {
+                    const int slot = nd + ic - cnt + q, j = jd + q;
+                    dyn->p0[slot] = b + j * rows;
+                    dyn->rows[slot] = min(rows, (e - b) - j * rows);
+                    dyn->a[slot] = a;
+                    dyn->b0[slot] = q == 0 ? f0 : 0;
+                }
+                nd += __shfl_sync(0xffffffffu, ic, 31);
+                wbase += __shfl_sync(0xffffffffu, iw, 31);
+            }
+            if (nd > 0 && nd <= kMaxDyn) Ws = Wd;
+            else nd = 0;
+        }
+        const long long lo = (long long)c * Ws / G, hi = (long long)(c + 1) * Ws / G;
         long long wbase = 0;  // weight of the segments before this batch
         for (int s0 = 0; s0 < S && lo < hi; s0 += 32) {
             const int s = s0 + lane;
@@ -202,6 +264,9 @@ __device__ __forceinline__ void find_run(const int32_t *seg_ptr, const int32_t *
         out->n = np;
         out->k0[0] = 0;
         for (int q = 0; q < np; ++q) out->k0[q + 1] += out->k0[q];
+        dyn->n = nd;
+        dyn->d0[0] = 0;
+        for (int q = 0; q < nd; ++q) dyn->d0[q + 1] = dyn->d0[q] + (nblk - dyn->b0[q]);
     }
     __syncwarp();
 }

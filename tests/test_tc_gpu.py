@@ -128,6 +128,26 @@ def test_ragged_dims(H1, H2):
     assert_close(y, ref, f"H1={H1} H2={H2}")
 
 
+def test_claimed_blocks_with_a_reused_workspace():
+    """fp32 y: the last part of the expand's work is claimed at run time from
+    a counter in the workspace, zeroed by each call's shrink kernel.  Three
+    calls on one workspace, back to back: every call updates every block once
+    (the oracle's result, and bit for bit the same y each time, whichever CTA
+    took a block)."""
+    w = wl.make("prefill", 1, y_dtype=torch.float32, y0="randn")
+    X, A, B = w.X.to(DEV), w.A.to(DEV), w.B.to(DEV)
+    perm, seg_ptr, idx, _ = sg().sgmv_build_segments_device(w.row_adapter.to(DEV), w.L)
+    ws = torch.full((sg().sgmv_workspace_bytes(w.T, w.H1, w.H2, w.r),), 0x7f, dtype=torch.uint8,
+                    device=DEV)  # the counter starts as garbage
+    ys = [w.Y0.to(DEV).clone() for _ in range(3)]
+    for y in ys:
+        sg().sgmv_apply(y, X, A, B, seg_ptr, idx, w.scale, perm=perm, workspace=ws)
+    check_error_word(0)
+    ref, *_ = oracle_apply_rows(w)
+    assert_close(ys[0], ref, "first call")
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+
+
 @pytest.mark.parametrize("y_dtype", [torch.float32, torch.float16])
 @pytest.mark.parametrize("H2", [1000, 4096])
 def test_runs_cross_tiles(y_dtype, H2):
