@@ -59,6 +59,9 @@ def parse_args(argv=None):
                    help="timed regions of --steps steps each; value from the median one")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama7b-stack", choices=WORKLOADS)
+    p.add_argument("--stack-calls", default="grouped", choices=["grouped", "single"],
+                   help="llama7b-stack: a layer's q/k/v and gate/up as one launch each "
+                        "(sgmv_apply_multi; 128 update launches per step), or 224 single calls")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=6.0,
                    help="host-core budget of each oracle baseline sample (one thread, all cores)")
@@ -166,10 +169,13 @@ def config_of(name, w, l2_note=None):
     return cfg
 
 
-def stack_config(l2_note=None):
+def stack_config(l2_note=None, grouped=True):
     cfg = {"workload": "llama7b-stack", "T": 128, "L": 128, "r": 16, "layers": 32,
            "projections": 7, "inputs": "float16", "y": "float16", "segments": 128,
-           "parallelism": "replicas"}
+           "parallelism": "replicas",
+           "update_launches": ("per layer: q+k+v, o, gate+up and down, one sgmv_apply_multi "
+                               "launch each (128 per step)") if grouped
+           else "one sgmv_apply per projection (224 per step)"}
     if l2_note:
         cfg["l2"] = l2_note
     return cfg
@@ -285,13 +291,21 @@ class Batch:
 
 
 class StackBatch:
-    """All 224 projections of the llama7b-stack workload, resident on the device."""
+    """All 224 projections of the llama7b-stack workload, resident on the device.
 
-    def __init__(self, seed, dev, sgmv):
+    grouped (the default): a layer's projections run as a model runs them --
+    q, k and v read the same rows and are one sgmv_apply_multi launch, gate
+    and up another, o and down (which read the attention output and the
+    activation) one sgmv_apply_multi launch each: 4 update launches per
+    layer, 128 per step.  Otherwise 224 sgmv_apply calls, one per
+    projection."""
+
+    def __init__(self, seed, dev, sgmv, grouped=True):
         import torch
         from rank_gemv_gb300 import workloads as wl
 
         self.T, self.L, self.r = 128, 128, 16
+        self.grouped = grouped
         self.projs = []
         for layer in range(wl.LLAMA7B_LAYERS):
             for p in range(len(wl.LLAMA7B_PROJ)):
@@ -303,39 +317,58 @@ class StackBatch:
                      torch.empty(self.smax + 1, dtype=torch.int32, device=dev),
                      torch.empty(self.smax, dtype=torch.int32, device=dev),
                      torch.empty(1, dtype=torch.int32, device=dev))
+        n_proj = len(wl.LLAMA7B_PROJ)
+        groups = [[0, 1, 2], [3], [4, 5], [6]] if grouped else [[k] for k in range(n_proj)]
+        # launches of a step: (layer, projections), in order
+        self.launches = [(layer, g) for layer in range(wl.LLAMA7B_LAYERS) for g in groups]
+        self.n_apply = len(self.launches)
 
-    n_apply = 224
+    def run_group(self, sgmv, layer, g):
+        """The update of projections g of a layer, on the last grouping."""
+        perm, seg_ptr, idx, _ = self.meta
+        pr = [self.projs[layer * 7 + k] for k in g]
+        if not self.grouped:
+            X, A, B, Y = pr[0]
+            sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
+        else:  # every launch through the multi-problem entry (one kernel for the step)
+            sgmv.sgmv_apply_multi([Y for _, _, _, Y in pr], [X for X, _, _, _ in pr],
+                                  [A for _, A, _, _ in pr], [B for _, _, B, _ in pr],
+                                  seg_ptr, idx, 1.0, perm=perm, S=self.smax)
+        return sgmv.sgmv_last_launch_count()
 
     def apply(self, sgmv):
         """One decode step over all 224 projections, as a serving loop runs it:
-        the first call groups the batch (sgmv_apply_rows writes the grouping
-        out), the other 223 reuse it through sgmv_apply."""
-        perm, seg_ptr, idx, _ = self.meta
-        n = 0
-        for i, (X, A, B, Y) in enumerate(self.projs):
-            if i == 0:
-                sgmv.sgmv_apply_rows(Y, X, A, B, self.ra, 1.0, out=self.meta)
-            else:
-                sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
-            n += sgmv.sgmv_last_launch_count()
+        the first projection's call groups the batch (sgmv_apply_rows writes
+        the grouping out); every launch after it reuses the grouping.
+        Returns the kernels launched."""
+        X, A, B, Y = self.projs[0]
+        sgmv.sgmv_apply_rows(Y, X, A, B, self.ra, 1.0, out=self.meta)
+        n = sgmv.sgmv_last_launch_count()
+        for layer, g in self.launches:
+            if layer == 0 and 0 in g:
+                g = [k for k in g if k != 0]  # q of layer 0 went with the grouping
+                if not g:
+                    continue
+            n += self.run_group(sgmv, layer, g)
         return n
 
     def step(self, sgmv):
         self.apply(sgmv)
 
-    def update_one(self, sgmv, i):
-        perm, seg_ptr, idx, _ = self.meta
-        X, A, B, Y = self.projs[i]
-        sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=self.smax)
-
     def update(self, sgmv):
-        """All 224 update calls on the grouping of the last step (roofline)."""
-        for i in range(len(self.projs)):
-            self.update_one(sgmv, i)
+        """All update launches of a step on the grouping of the last step
+        (roofline)."""
+        for layer, g in self.launches:
+            self.run_group(sgmv, layer, g)
 
     @staticmethod
     def proj_bytes(H1, H2, T=128, L=128, r=16):
         return L * (H1 * r + r * H2) * 2 + T * H1 * 2 + 2 * T * H2 * 2
+
+    def group_bytes(self, g):
+        from rank_gemv_gb300 import workloads as wl
+
+        return sum(self.proj_bytes(*wl.LLAMA7B_PROJ[k][1:]) for k in g)
 
     def bytes_moved(self):
         from rank_gemv_gb300 import workloads as wl
@@ -445,7 +478,7 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     if args.workload == "llama7b-stack":
-        stack = StackBatch(seed, dev, sgmv)
+        stack = StackBatch(seed, dev, sgmv, grouped=args.stack_calls == "grouped")
         batches = [stack]
         T = stack.T
         bytes_step = stack.bytes_moved()
@@ -505,17 +538,23 @@ def run_ours(args, rank, world, local):
     bytes_apply = bytes_step / n_apply
     achieved, frac = hbm(bytes_apply, apply_us, peak)
     if args.workload == "llama7b-stack":
+        # every launch of layer 0 alone after an L2 flush; the mean over them
+        # is one launch of the step on average (all layers have these shapes)
+        from rank_gemv_gb300 import workloads as wl
+
         iso = {}
-        for name, i in (("q", 0), ("gate", 4), ("down", 6)):
-            _, H1, H2 = wl.LLAMA7B_PROJ[i]
-            st = isolated_stats(lambda i=i: stack.update_one(sgmv, i), flush, args.latency_iters)
+        for layer, g in stack.launches:
+            if layer != 0:
+                continue
+            name = "+".join(wl.LLAMA7B_PROJ[k][0] for k in g)
+            st = isolated_stats(lambda g=g: stack.run_group(sgmv, 0, g), flush, args.latency_iters)
             us = st["median"]
             iso[name] = {"us": us, "us_p10": st["p10"], "us_p90": st["p90"],
-                         "bytes": StackBatch.proj_bytes(H1, H2),
-                         "frac": hbm(StackBatch.proj_bytes(H1, H2), us, peak)[1]}
-        # a layer has four q-shaped, two gate-shaped and one down-shaped call
-        iso_us = (4 * iso["q"]["us"] + 2 * iso["gate"]["us"] + iso["down"]["us"]) / 7
-        iso_note = "per projection shape (layer 0), L2 flushed before each; mean over a layer's 7 calls"
+                         "bytes": stack.group_bytes(g),
+                         "frac": hbm(stack.group_bytes(g), us, peak)[1]}
+        iso_us = sum(v["us"] for v in iso.values()) / len(iso)
+        iso_note = ("every update launch of layer 0, L2 flushed before each; mean over the "
+                    f"layer's {len(iso)} launches")
     else:
         iso = None
         iso_st = isolated_stats(lambda: batches[0].update(sgmv), flush, args.latency_iters)
@@ -533,7 +572,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(args.workload, w0, l2_note) if w0 is not None else stack_config(l2_note),
+        "config": (config_of(args.workload, w0, l2_note) if w0 is not None
+                   else stack_config(l2_note, args.stack_calls == "grouped")),
         "repeats": {"n": R, "ms_per_step": [t / K * 1e3 for t in regions],
                     "value_from": "median region"},
         "hbm_gbs": bytes_step * K / elapsed / 1e9,
@@ -543,7 +583,7 @@ def run_ours(args, rank, world, local):
                      "peak_kind": peak_kind, "traffic": profiled_traffic(args.workload),
                      "source_hash": source_hash(WORKLOAD_KERNELS.get(args.workload, "stream")), "bytes_per_call": bytes_apply,
                      "call_us": apply_us,
-                     "frac_uses": f"call_us: {n_apply * K} update calls back to back in CUDA "
+                     "frac_uses": f"call_us: {n_apply * K} update launches back to back in CUDA "
                                   f"graphs, median of {R} regions",
                      "isolated": {"call_us": iso_us, "achieved": iso_gbs, "frac": iso_frac,
                                   "method": f"median of {args.latency_iters}; {iso_note}",
@@ -954,7 +994,8 @@ def run_reference(args, rank, world):
         close()
     value = args.steps * rows / el
     w = None if args.workload == "llama7b-stack" else wl.make(args.workload, args.seed)
-    cfg = config_of(args.workload, w) if w is not None else stack_config()
+    cfg = (config_of(args.workload, w) if w is not None
+           else stack_config(None, args.stack_calls == "grouped"))
     sample = (f"{desc}; one oracle pass (grouping + fp64 update, {nthr} threads over ranges of "
               "rows) per step")
     print(json.dumps({

@@ -280,6 +280,30 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
                            size_t workspace_bytes, void *stream);
 
 /*
+ * sgmv_apply for P problems at once (1 <= P <= 4) that share the rows, the
+ * segments and the shapes but have their own x, A, B and y: the projections
+ * of one layer that read the same rows, q / k / v, or gate / up ([Article]
+ * §2.1: a LoRA pair A, B sits beside a weight matrix W; §3.2: the pairs are
+ * injected into the model's linear layers, e.g. each layer's attention q
+ * projection; §2.2 for the operation).  y[k] += scale * (x[k] . A[k][idx]) . B[k][idx], every
+ * argument otherwise as for sgmv_apply (host arrays of P device pointers for
+ * y, x, A, B; x[k] may all be the same pointer).  The P problems run as one
+ * launch of the streaming CUDA-core kernel when r <= 64, r % 4 == 0 and the
+ * batch is large enough for one-CTA clusters (T > 76 on 152 SMs; each CTA
+ * walks several (problem, tile) units), with each row's arithmetic exactly
+ * that of P separate sgmv_apply calls without a workspace (the same bits);
+ * otherwise it makes those P calls.  P = 1 is allowed: a serving loop that
+ * sends all its calls here runs a single kernel.
+ * No workspace, nothing allocated.  Errors: SGMV_ERR_INVALID_ARG for P out
+ * of range or null arrays or pointers, then as sgmv_apply.
+ */
+int sgmv_apply_multi(int32_t P, void *const *y, int y_dtype, const void *const *x,
+                     const void *const *A, const void *const *B, int in_dtype, float scale,
+                     const int32_t *perm, const int32_t *seg_ptr, const int32_t *idx, int32_t S,
+                     const int32_t *seg_ptr_host, int32_t T, int32_t L, int32_t H1, int32_t H2,
+                     int32_t r, void *stream);
+
+/*
  * Loads one adapter into slot `slot` of the stacked pools: A_src [H1][r] into
  * A_pool[slot] and B_src [r][H2] into B_pool[slot], as two asynchronous copies
  * on `stream`.  Page: [Review] "Punica: Multi-Tenant LoRA Serving" (nubint.ai

@@ -13,7 +13,7 @@ __version__ = "0.1.0"
 _BINDING_NAMES = {
     "sgmv_status_string", "sgmv_max_segments", "sgmv_build_segments",
     "sgmv_build_segments_device", "sgmv_workspace_bytes", "sgmv_shrink", "sgmv_expand",
-    "sgmv_apply", "sgmv_apply_rows", "sgmv_apply_noalloc", "sgmv_load_adapter", "sgmv_copy_gather",
+    "sgmv_apply", "sgmv_apply_multi", "sgmv_apply_rows", "sgmv_apply_noalloc", "sgmv_load_adapter", "sgmv_copy_gather",
     "sgmv_get_device_error", "sgmv_last_launch_count", "sgmv_read_floor",
     "sgmv_debug_inject_wait_timeout", "sgmv_fused_workspace_bytes", "sgmv_fused_linear_lora",
     "SgmvError", "load_library",

@@ -151,15 +151,21 @@ constexpr int kStreamChunkElems = 16384;
 // (slices [rank*hc, ...) of H1 and [rank*jc, ...) of H2), y = cluster; cluster
 // c walks the tiles c, c + G, c + 2G, ... of the batch.  Every CTA streams its
 // slices of the tiles' A and B through a ring of `nst` shared-memory stages.
+// Most problems (same rows and segments, own x, A, B and y) in one launch of
+// the streaming kernel.
+constexpr int kStreamMaxProblems = 4;
+
 struct StreamParams {
-    // B, no swizzle: as [L][H2/256][r][256] with box {256, r, chunk/256, 1}
-    // (b4d, whole chunk in one copy), else as [L][r][H2] with box {256, r, 1}
-    CUtensorMap tmap_b;
+    // B of each problem, no swizzle: as [L][H2/256][r][256] with box
+    // {256, r, chunk/256, 1} (b4d, whole chunk in one copy), else as
+    // [L][r][H2] with box {256, r, 1}
+    CUtensorMap tmap_b[kStreamMaxProblems];
     int32_t b4d;
-    void *y;
-    const void *x;
-    const void *A;
-    const void *B;
+    int32_t np;                  // problems: 1 .. kStreamMaxProblems (1 in the grouped form)
+    void *y[kStreamMaxProblems];
+    const void *x[kStreamMaxProblems];
+    const void *A[kStreamMaxProblems];
+    const void *B[kStreamMaxProblems];
     const int32_t *perm;
     const int32_t *seg_ptr;
     const int32_t *idx;
@@ -189,6 +195,7 @@ struct StreamLaunch {
     int rk;          // 16, 32 or 64: compile-time bound on r
     int cw;          // compute warps: 8 or 16
     bool grouped;
+    bool multi;      // the instantiation for several problems (one-CTA clusters, cw 16)
     cudaStream_t stream;
 };
 
@@ -196,11 +203,11 @@ struct StreamLaunch {
 int stream_launch_f16(const StreamLaunch &l);
 int stream_launch_bf16(const StreamLaunch &l);
 
-// Launch shape of the streaming kernel (see sgmv_api.cu); false when the
-// kernel does not apply to the problem.
+// Launch shape of the streaming kernel for np problems of these shapes (see
+// sgmv_api.cu); false when the kernel does not apply.
 bool stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len, int32_t H1,
                   int32_t H2, int32_t r, int in_dtype, int y_dtype, StreamLaunch &l,
-                  bool grouped);
+                  bool grouped, int np = 1);
 
 // Read-only kernel with a given grid, cluster size and ring (sgmv_floor.cu);
 // returns a cudaError_t value.

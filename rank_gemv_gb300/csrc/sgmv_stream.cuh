@@ -11,8 +11,12 @@
 //   * a tile is up to `trows` (1..8) consecutive rows of one segment;
 //   * CL CTAs form a cluster (CL = 1, 2, 4 or 8, fewer for larger batches);
 //     CTA `rank` owns the slice [rank*hc, ...) of H1 and [rank*jc, ...) of H2;
-//   * cluster c walks the tiles c, c + G, c + 2G, ...: the kernel is
-//     persistent over tiles, and each CTA streams its slices of every tile's
+//   * one launch may carry up to four problems with the same rows, segments
+//     and shapes but their own x, A, B and y (the projections of a layer
+//     that read the same rows); a unit is a (problem, tile) pair, numbered
+//     problem by problem;
+//   * cluster c walks the units c, c + G, c + 2G, ...: the kernel is
+//     persistent over units, and each CTA streams its slices of every unit's
 //     A and B through a ring of shared-memory stages, 32 KB of weights per
 //     chunk at the rank bound: one 1-D bulk (TMA) copy per A chunk
 //     (contiguous in A[a]), tiled tensor (TMA) boxes of 256 columns x r rows
@@ -217,7 +221,11 @@ __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes,
     }
 }
 
-template <typename Tin, typename Ty, int RK, bool GROUPED, int CW>
+// MULTI: the launch may carry several problems (P.np).  Single-problem
+// launches use the instantiation without it, where every problem number is
+// the constant 0: with a run-time problem number in the copy warp's tensor-map
+// address and in the tile numbering, single calls measured 2-4 % slower.
+template <typename Tin, typename Ty, int RK, bool GROUPED, int CW, bool MULTI = false>
 __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
     sgmv_stream_kernel(const __grid_constant__ StreamParams P) {
     constexpr int kStreamConsumers = CW * 32, kStreamWarps = CW, kStreamThreads = CW * 32 + 32;
@@ -241,11 +249,15 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
     __shared__ __align__(16) int g_key[kG];
     __shared__ int g_pn[kG], g_pkey[kG], g_flag[kG], g_sperm[kG];
     __shared__ int g_nseg_s;
+    // A, x and y of every problem (copied out of the parameters with
+    // constant indices)
+    __shared__ const void *s_pp[3][kStreamMaxProblems];
+    const int np = MULTI ? P.np : 1;
 
     float *const red = reinterpret_cast<float *>(sm + P.red_off);    // [8 warps][8][RK]
     float *const recv = reinterpret_cast<float *>(sm + P.recv_off);  // [2][cl][8][RK]
     float *const s_v = reinterpret_cast<float *>(sm + P.v_off);      // [2][8][RK]
-    int *const tab = reinterpret_cast<int *>(sm + P.tab_off);        // [tiles][4]: p0, n, a
+    int *const tab = reinterpret_cast<int *>(sm + P.tab_off);        // [tiles][4]: p0, n, a, problem
     int *const trow = tab + 4 * kStreamMaxTiles;                     // [tiles][8] rows
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -265,6 +277,14 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
         mbar_init(&vfull[1], 1);
         mbar_init_fence();
         s_total = 0;
+        if (MULTI) {
+#pragma unroll
+            for (int q = 0; q < kStreamMaxProblems; ++q) {
+                s_pp[0][q] = P.A[q];
+                s_pp[1][q] = P.x[q];
+                s_pp[2][q] = P.y[q];
+            }
+        }
     }
 
     // ---- this cluster's tiles: tab[m] = global tile cid + m*G ---------------
@@ -319,16 +339,22 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
         }
         __syncthreads();
         int gbase = s_wsum[warp] + incl - own;  // first global tile of this thread's segments
+        const int ntile = s_total;               // tiles of one problem
         for (int s = s0; s < s1; ++s) {
             int b = 0, len = 0, a = 0;
             const int n = seg(s, b, len, a, false);
-            // tiles j of this segment with (gbase + j) % G == cid
-            for (int j = ((cid - gbase % G) % G + G) % G; j < n; j += G) {
-                const int m = (gbase + j) / G;
-                if (m < kStreamMaxTiles) {
-                    tab[4 * m] = b + trows * j;
-                    tab[4 * m + 1] = min(trows, len - trows * j);
-                    tab[4 * m + 2] = a;
+            // unit u = problem * ntile + tile: tiles j of this segment with
+            // (u0 + j) % G == cid, u0 the unit of the segment's first tile
+            for (int pb = 0; pb < np; ++pb) {
+                const int u0 = pb * ntile + gbase;
+                for (int j = ((cid - u0 % G) % G + G) % G; j < n; j += G) {
+                    const int m = (u0 + j) / G;
+                    if (m < kStreamMaxTiles) {
+                        tab[4 * m] = b + trows * j;
+                        tab[4 * m + 1] = min(trows, len - trows * j);
+                        tab[4 * m + 2] = a;
+                        tab[4 * m + 3] = pb;
+                    }
                 }
             }
             gbase += n;
@@ -392,6 +418,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                     tab[4 * m] = tid;
                     tab[4 * m + 1] = g_pn[tid];
                     tab[4 * m + 2] = g_pkey[tid];
+                    tab[4 * m + 3] = 0;  // one problem
                 }
             }
             g_flag[tid] = before;  // segment number (high half) of position tid
@@ -405,7 +432,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
         g_nseg = g_nseg_s;
     }
     __syncthreads();
-    const int ntot = s_total;
+    const int ntot = s_total * np;  // units: tiles of every problem
     int nt = ntot > cid ? (ntot - 1 - cid) / G + 1 : 0;
     if (nt > kStreamMaxTiles) {
         if (rank == 0) set_error(err, kErrBadSegments);
@@ -452,9 +479,12 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
         // ---- copy warp: fills the ring in the order the compute warps use it.
         // Weights need only the adapter ids, so they are requested while the
         // compute warps look up the tiles' rows.
-        const Tin *gA = static_cast<const Tin *>(P.A);
-        const Tin *gX = static_cast<const Tin *>(P.x);
-        const Ty *gY = static_cast<const Ty *>(P.y);
+        // the unit's problem picks its A, B (tensor map), x and y
+        const CUtensorMap *const tmb0 = &P.tmap_b[0];
+        const Tin *gA = static_cast<const Tin *>(P.A[0]);
+        const Tin *gX = static_cast<const Tin *>(P.x[0]);
+        const Ty *gY = static_cast<const Ty *>(P.y[0]);
+        const CUtensorMap *tmb = tmb0;
         const uint32_t bbox = (uint32_t)rk * 256u * (uint32_t)sizeof(Tin);
         const bool b4d = P.b4d != 0;
         RingIter it;
@@ -464,6 +494,11 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
             if (it.tile() != cur_a) {
                 cur_a = it.tile();
                 a = (int)lds32(tab + 4 * cur_a + 2);
+                if (MULTI) {
+                    const int pb = (int)lds32(tab + 4 * cur_a + 3);
+                    gA = static_cast<const Tin *>(s_pp[0][pb]);
+                    tmb = tmb0 + pb;
+                }
             }
             uint8_t *dst = sm + (size_t)s * stage_bytes;
             if (lane == 0) {
@@ -476,7 +511,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                     const int jlo = j0 + it.i * JN;
                     if (b4d && j1 - jlo >= JN) {  // a whole chunk in one copy
                         mbar_arrive_expect_tx(&full[s], bbox * (uint32_t)(JN / 256));
-                        tma_load_4d(dst, &P.tmap_b, 0, 0, jlo >> 8, a, &full[s]);
+                        tma_load_4d(dst, tmb, 0, 0, jlo >> 8, a, &full[s]);
                     }
                 }
             }
@@ -486,7 +521,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], bbox * (uint32_t)nbox);
                 __syncwarp();
                 if (lane < nbox)
-                    tma_load_3d(dst + lane * bbox, &P.tmap_b, jlo + 256 * lane, 0, a, &full[s]);
+                    tma_load_3d(dst + lane * bbox, tmb, jlo + 256 * lane, 0, a, &full[s]);
             }
         };
         auto issue_act = [&](int s) {  // x or y rows of chunk `it` into stage s
@@ -494,6 +529,11 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                 cur_r = it.tile();
                 row = lane < kTileRows ? (int)lds32(trow + kTileRows * cur_r + lane) : -1;
                 nvalid = (uint32_t)__popc(__ballot_sync(0xffffffffu, row >= 0));
+                if (MULTI) {
+                    const int pb = (int)lds32(tab + 4 * cur_r + 3);
+                    gX = static_cast<const Tin *>(s_pp[1][pb]);
+                    gY = static_cast<const Ty *>(s_pp[2][pb]);
+                }
             }
             uint8_t *dst = sm + (size_t)s * stage_bytes + act_off;
             if (!it.isB) {
@@ -526,23 +566,27 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
             const int tile = own ? mine.tile() : 0;
             uint8_t *dst = sm + (size_t)lane * stage_bytes;
             uint64_t *bar = &full[own ? lane : 0];
+            const int mp = MULTI && own ? (int)lds32(tab + 4 * tile + 3) : 0;  // the chunk's problem
             if (own) {
                 const int ma = (int)lds32(tab + 4 * tile + 2);
                 if (!mine.isB) {
                     const int hlo = h0 + mine.i * hn, n = min(hn, h1 - hlo);
                     const uint32_t bytes = (uint32_t)(n * rk) * (uint32_t)sizeof(Tin);
                     mbar_arrive_expect_tx(bar, bytes);
-                    bulk_g2s(dst, gA + ((size_t)ma * H1 + hlo) * rk, bytes, bar);
+                    bulk_g2s(dst,
+                             static_cast<const Tin *>(MULTI ? s_pp[0][mp] : P.A[0]) +
+                                 ((size_t)ma * H1 + hlo) * rk,
+                             bytes, bar);
                 } else {
                     const int jlo = j0 + mine.i * JN, n = min(JN, j1 - jlo);
                     if (b4d && n >= JN) {
                         mbar_arrive_expect_tx(bar, bbox * (uint32_t)(JN / 256));
-                        tma_load_4d(dst, &P.tmap_b, 0, 0, jlo >> 8, ma, bar);
+                        tma_load_4d(dst, tmb0 + mp, 0, 0, jlo >> 8, ma, bar);
                     } else {
                         const int nbox = (n + 255) >> 8;
                         mbar_arrive_expect_tx(bar, bbox * (uint32_t)nbox);
                         for (int bx = 0; bx < nbox; ++bx)
-                            tma_load_3d(dst + bx * bbox, &P.tmap_b, jlo + 256 * bx, 0, ma, bar);
+                            tma_load_3d(dst + bx * bbox, tmb0 + mp, jlo + 256 * bx, 0, ma, bar);
                     }
                 }
             }
@@ -565,7 +609,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                     for (int t = 0; t < kTileRows; ++t)
                         if (rows_[t] >= 0)
                             bulk_g2s(adst + (size_t)t * hn * sizeof(Tin),
-                                     gX + (size_t)rows_[t] * H1 + hlo, rowb, bar);
+                                     static_cast<const Tin *>(MULTI ? s_pp[1][mp] : P.x[0]) +
+                                         (size_t)rows_[t] * H1 + hlo,
+                                     rowb, bar);
                 } else {
                     const int jlo = j0 + mine.i * JN, n = min(JN, j1 - jlo);
                     const uint32_t rowb = (uint32_t)n * (uint32_t)sizeof(Ty);
@@ -574,7 +620,9 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
                     for (int t = 0; t < kTileRows; ++t)
                         if (rows_[t] >= 0)
                             bulk_g2s(adst + (size_t)t * JN * sizeof(Ty),
-                                     gY + (size_t)rows_[t] * H2 + jlo, rowb, bar);
+                                     static_cast<const Ty *>(MULTI ? s_pp[2][mp] : P.y[0]) +
+                                         (size_t)rows_[t] * H2 + jlo,
+                                     rowb, bar);
                 }
             }
         }
@@ -608,7 +656,6 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
         pdl_wait();  // y is written below: only after the previous kernel
         if (meta_out) write_meta();
         if (ncl > 1) cluster_wait();  // every CTA of the cluster has started
-        Ty *gY = static_cast<Ty *>(P.y);
         bool lost = false;
         int q = 0;
         float4 part;  // elements (t, 4q .. 4q+3) of this CTA's partial v, tid = t * (rk/4) + q
@@ -693,6 +740,8 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
 #pragma unroll
                 for (int t = 0; t < kTileRows; ++t) row[t] = (int)lds32(trow + kTileRows * mm + t);
                 const float *sv = s_v + (mm & 1) * kTileRows * RK;
+                Ty *gY = static_cast<Ty *>(
+                    MULTI ? const_cast<void *>(s_pp[2][(int)lds32(tab + 4 * mm + 3)]) : P.y[0]);
                 if (n <= 1)
                     stream_expand<Tin, Ty, RK, 1, CW>(sm, stage_bytes, act_off, nst, q, nB, j1 - j0, j0,
                                                   rk, sv, row, gY, H2, scale, full, empty, lost, err);
@@ -715,18 +764,19 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
 
 // ---- host-side launcher for one input type ----------------------------------
 template <typename Tin, typename Ty, int RK>
-static void *stream_pick(bool grouped, int cw) {
+static void *stream_pick(bool grouped, int cw, bool multi) {
     if (grouped) return (void *)sgmv_stream_kernel<Tin, Ty, RK, true, 8>;
+    if (multi) return (void *)sgmv_stream_kernel<Tin, Ty, RK, false, 16, true>;
     return cw == 16 ? (void *)sgmv_stream_kernel<Tin, Ty, RK, false, 16>
                     : (void *)sgmv_stream_kernel<Tin, Ty, RK, false, 8>;
 }
 
 template <typename Tin, typename Ty>
-static void *stream_pick_rk(int rk, bool grouped, int cw) {
+static void *stream_pick_rk(int rk, bool grouped, int cw, bool multi) {
     switch (rk) {
-        case 16: return stream_pick<Tin, Ty, 16>(grouped, cw);
-        case 32: return stream_pick<Tin, Ty, 32>(grouped, cw);
-        default: return stream_pick<Tin, Ty, 64>(grouped, cw);
+        case 16: return stream_pick<Tin, Ty, 16>(grouped, cw, multi);
+        case 32: return stream_pick<Tin, Ty, 32>(grouped, cw, multi);
+        default: return stream_pick<Tin, Ty, 64>(grouped, cw, multi);
     }
 }
 
@@ -734,9 +784,9 @@ template <typename Tin>
 static int stream_launch_impl(const StreamLaunch &l) {
     void *fn;
     switch (l.y_dtype) {
-        case 0: fn = stream_pick_rk<Tin, __half>(l.rk, l.grouped, l.cw); break;
-        case 1: fn = stream_pick_rk<Tin, __nv_bfloat16>(l.rk, l.grouped, l.cw); break;
-        default: fn = stream_pick_rk<Tin, float>(l.rk, l.grouped, l.cw); break;
+        case 0: fn = stream_pick_rk<Tin, __half>(l.rk, l.grouped, l.cw, l.multi); break;
+        case 1: fn = stream_pick_rk<Tin, __nv_bfloat16>(l.rk, l.grouped, l.cw, l.multi); break;
+        default: fn = stream_pick_rk<Tin, float>(l.rk, l.grouped, l.cw, l.multi); break;
     }
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)l.p.smem_bytes);

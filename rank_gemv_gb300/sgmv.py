@@ -44,6 +44,8 @@ SIGNATURES = {
                           _i32, _i32, _i32, _i32, _vp, _sz, _vp]),
     "sgmv_apply_rows": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _i32, _i32, _i32, _i32,
                                _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "sgmv_apply_multi": (_int, [_i32, _vpp, _int, _vpp, _vpp, _vpp, _int, _f32, _vp, _vp, _vp,
+                                _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
     "sgmv_apply_noalloc": (_int, [_vp, _int, _vp, _vp, _vp, _int, _f32, _vp, _vp, _vp, _i32, _vp,
                                   _i32, _i32, _i32, _i32, _i32, _vp]),
     "sgmv_fused_workspace_bytes": (_sz, [_i32, _i32, _i32]),
@@ -209,6 +211,36 @@ def sgmv_apply(y, x, A, B, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_host=None
         _nseg(idx, S), _ptr(sph), T, L, H1, H2, r, _ptr(workspace), ws_bytes,
         _stream(x.device)), "sgmv_apply")
     return y
+
+
+def sgmv_apply_multi(ys, xs, As, Bs, seg_ptr, idx, scale=1.0, perm=None, seg_ptr_host=None,
+                     S=None):
+    """sgmv_apply for up to 4 problems with the same rows, segments and
+    shapes (e.g. a layer's q / k / v): ys[k][row(p)] += scale * (xs[k][row(p)]
+    @ As[k][idx[s]]) @ Bs[k][idx[s]], in place, in one launch when the kernel
+    allows (the same bits as separate calls); returns ys."""
+    P = len(ys)
+    if not (len(xs) == len(As) == len(Bs) == P):
+        raise ValueError("ys, xs, As and Bs differ in length")
+    T, H1 = xs[0].shape
+    L, _, r = As[0].shape
+    H2 = ys[0].shape[1]
+    for y, x, A, B in zip(ys, xs, As, Bs):
+        if (tuple(x.shape) != (T, H1) or tuple(A.shape) != (L, H1, r)
+                or tuple(B.shape) != (L, r, H2) or tuple(y.shape) != (T, H2)):
+            raise ValueError("the problems' shapes differ")
+        if x.dtype != xs[0].dtype or A.dtype != x.dtype or B.dtype != x.dtype or y.dtype != ys[0].dtype:
+            raise TypeError("the problems' types differ")
+    sph = _host_i32(seg_ptr_host)
+
+    def arr(ts):
+        return (ctypes.c_void_p * max(1, P))(*[_ptr(t) for t in ts])
+    _check(load_library().sgmv_apply_multi(
+        P, arr(ys), _DTYPES[ys[0].dtype], arr(xs), arr(As), arr(Bs), _DTYPES[xs[0].dtype],
+        float(scale), _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")),
+        _ptr(_meta(idx, "idx")), _nseg(idx, S), _ptr(sph), T, L, H1, H2, r,
+        _stream(xs[0].device)), "sgmv_apply_multi")
+    return ys
 
 
 def sgmv_apply_rows(y, x, A, B, row_adapter, scale=1.0, out=None, workspace=None):

@@ -180,6 +180,28 @@ def test_load_adapter_rejects_bad_arguments(lib, kw):
                                  None) == 1
 
 
+def test_apply_multi_rejects_bad_arguments(lib):
+    import ctypes
+
+    vp = ctypes.c_void_p
+    four = (vp * 4)(A16, A16, A16, A16)
+
+    def call(P=2, y=four, x=four, A=four, B=four, **kw):
+        a = dict(y_dt=0, in_dt=0, T=4, L=2, H1=64, H2=64, r=16)
+        a.update(kw)
+        return lib.sgmv_apply_multi(P, y, a["y_dt"], x, A, B, a["in_dt"], 1.0, None, A16, A16, 1,
+                                    None, a["T"], a["L"], a["H1"], a["H2"], a["r"], None)
+    assert call(P=0) == 1
+    assert call(P=5) == 1               # at most four problems
+    assert call(y=None) == 1
+    assert call(B=None) == 1
+    assert call(y=(vp * 4)(A16, None, A16, A16)) == 1
+    assert call(x=(vp * 4)(A16, MIS, A16, A16)) == 3
+    assert call(r=0) == 1
+    assert call(H1=20) == 3
+    assert call(y_dt=7) == 1
+
+
 def test_copy_gather_rejects_bad_arguments(lib):
     import ctypes
 

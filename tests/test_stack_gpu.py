@@ -1,6 +1,7 @@
 """Full-size llama7b-stack workload (32 layers x 7 projections, 128 decode rows
 on 128 adapters, about 10 GB of stacked adapters) in the benchmark's launch
-configuration: one device grouping, then 224 fused updates.  Five
+configuration: one device grouping, then per layer q+k+v, o, gate+up and
+down as one sgmv_apply_multi launch each.  Five
 projections are checked against the oracle element by element, and three
 rows of every one of the 224 projections (each row against the oracle on
 that row and its adapter alone)."""
@@ -27,11 +28,16 @@ def test_llama7b_stack_sampled_projections():
     ra = wl.stack_row_adapter(128)
     perm, seg_ptr, idx, S = sgmv.sgmv_build_segments_device(ra.to(dev), 128)
     smax = sgmv.sgmv_max_segments(128, 128)
-    for X, A, B, Y in projs:
-        sgmv.sgmv_apply(Y, X, A, B, seg_ptr, idx, 1.0, perm=perm, S=smax)
+    n_proj = len(wl.LLAMA7B_PROJ)
+    for layer in range(wl.LLAMA7B_LAYERS):
+        for g in ([0, 1, 2], [3], [4, 5], [6]):
+            pr = [projs[layer * n_proj + k] for k in g]
+            sgmv.sgmv_apply_multi([p[3] for p in pr], [p[0] for p in pr],
+                                  [p[1] for p in pr], [p[2] for p in pr], seg_ptr, idx, 1.0,
+                                  perm=perm, S=smax)
+            assert sgmv.load_library().sgmv_last_launch_count() == 1
     check_error_word(0)
     o_perm, o_seg, o_idx = oracle.build_segments(ra, 128)
-    n_proj = len(wl.LLAMA7B_PROJ)
     for layer, p in SAMPLES:
         X, A, B, Y = projs[layer * n_proj + p]
         Y0 = torch.zeros(Y.shape, dtype=torch.float16)
