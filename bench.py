@@ -290,6 +290,18 @@ class Batch:
                         S=self.smax, workspace=self.ws)
 
 
+def stack_launch_groups(grouped=True):
+    """The update launches of one llama7b-stack step: (layer, projections),
+    in order.  Grouped: per layer q+k+v (they read the same rows), o, gate+up
+    (the same rows again) and down, each one launch; else one per
+    projection."""
+    from rank_gemv_gb300 import workloads as wl
+
+    n_proj = len(wl.LLAMA7B_PROJ)
+    groups = [[0, 1, 2], [3], [4, 5], [6]] if grouped else [[k] for k in range(n_proj)]
+    return [(layer, g) for layer in range(wl.LLAMA7B_LAYERS) for g in groups]
+
+
 class StackBatch:
     """All 224 projections of the llama7b-stack workload, resident on the device.
 
@@ -317,10 +329,7 @@ class StackBatch:
                      torch.empty(self.smax + 1, dtype=torch.int32, device=dev),
                      torch.empty(self.smax, dtype=torch.int32, device=dev),
                      torch.empty(1, dtype=torch.int32, device=dev))
-        n_proj = len(wl.LLAMA7B_PROJ)
-        groups = [[0, 1, 2], [3], [4, 5], [6]] if grouped else [[k] for k in range(n_proj)]
-        # launches of a step: (layer, projections), in order
-        self.launches = [(layer, g) for layer in range(wl.LLAMA7B_LAYERS) for g in groups]
+        self.launches = stack_launch_groups(grouped)
         self.n_apply = len(self.launches)
 
     def run_group(self, sgmv, layer, g):

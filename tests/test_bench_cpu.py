@@ -5,6 +5,7 @@ copy: they live in one byte buffer as views at 256-byte-aligned offsets (the
 C ABI wants 16-byte-aligned rows).  The views must hold the original values,
 not overlap, and together span the buffer.
 """
+import pytest
 import torch
 
 import bench
@@ -65,3 +66,23 @@ def test_rotation_copies():
 def test_default_workload_is_the_full_stack():
     args = bench.parse_args([])
     assert args.workload == "llama7b-stack" and args.gpus == 1 and args.warmup >= 3
+
+
+@pytest.mark.parametrize("grouped", [True, False])
+def test_stack_launch_groups_cover_every_projection_once(grouped):
+    """Each layer's seven projections appear once, in layer order; a grouped
+    launch only joins projections that read the same rows and have the same
+    shapes (q, k, v; gate, up), never o or down (they read other rows)."""
+    import bench
+    from rank_gemv_gb300 import workloads as wl
+
+    launches = bench.stack_launch_groups(grouped)
+    assert len(launches) == wl.LLAMA7B_LAYERS * (4 if grouped else 7)
+    seen = [(layer, k) for layer, g in launches for k in g]
+    assert seen == [(layer, k) for layer in range(wl.LLAMA7B_LAYERS) for k in range(7)]
+    same_rows = [{0, 1, 2}, {4, 5}]
+    for _, g in launches:
+        assert 1 <= len(g) <= 4
+        if len(g) > 1:
+            assert any(set(g) <= s for s in same_rows)
+            assert len({wl.LLAMA7B_PROJ[k][1:] for k in g}) == 1
