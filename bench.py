@@ -1353,7 +1353,7 @@ def run_load(args):
     dsts = [[t[slot] for A, B in spare for t in (A, B)] for slot in (0, 1)]
     srcs = [t for a, b in host for t in (a, b)]
     gather = {}
-    for ctas in (0, 304, 152, 64, 16):
+    for ctas in (0, 304, 152, 64, 32, 16):
         def gload(slot, ctas=ctas):
             sgmv.sgmv_copy_gather(dsts[slot], srcs, stream=cs, max_ctas=ctas)
             assert sgmv.load_library().sgmv_last_launch_count() == 1
