@@ -155,17 +155,10 @@ constexpr int kStreamChunkElems = 16384;
 // the streaming kernel.
 constexpr int kStreamMaxProblems = 4;
 
-struct StreamParams {
-    // B of each problem, no swizzle: as [L][H2/256][r][256] with box
-    // {256, r, chunk/256, 1} (b4d, whole chunk in one copy), else as
-    // [L][r][H2] with box {256, r, 1}
-    CUtensorMap tmap_b[kStreamMaxProblems];
-    int32_t b4d;
+// Everything of a launch but the problems' operands.
+struct StreamCommon {
+    int32_t b4d;                 // B read as whole chunks through a 4-D view (below)
     int32_t np;                  // problems: 1 .. kStreamMaxProblems (1 in the grouped form)
-    void *y[kStreamMaxProblems];
-    const void *x[kStreamMaxProblems];
-    const void *A[kStreamMaxProblems];
-    const void *B[kStreamMaxProblems];
     const int32_t *perm;
     const int32_t *seg_ptr;
     const int32_t *idx;
@@ -188,6 +181,26 @@ struct StreamParams {
     float scale;
     int32_t inject;              // 1: diagnostic launch with an injected wait timeout
 };
+
+// The operands of NP problems.
+template <int NP> struct StreamOperands {
+    // B of each problem, no swizzle: as [L][H2/256][r][256] with box
+    // {256, r, chunk/256, 1} (b4d, whole chunk in one copy), else as
+    // [L][r][H2] with box {256, r, 1}
+    CUtensorMap tmap_b[NP];
+    void *y[NP];
+    const void *x[NP];
+    const void *A[NP];
+    const void *B[NP];
+};
+
+// The parameters with the operands of NP problems (first, so that the tensor
+// maps open the parameter block).  The kernel for one problem takes NP = 1:
+// its parameter block is 400 bytes smaller, which measured 1-2 % faster per
+// call on decode batches.
+template <int NP> struct StreamParamsT : StreamOperands<NP>, StreamCommon {};
+using StreamParams = StreamParamsT<kStreamMaxProblems>;  // what the host fills
+using StreamParams1 = StreamParamsT<1>;
 
 struct StreamLaunch {
     StreamParams p;

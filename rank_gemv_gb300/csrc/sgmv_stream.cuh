@@ -227,7 +227,7 @@ __device__ __forceinline__ void stream_expand(uint8_t *sm, uint32_t stage_bytes,
 // address and in the tile numbering, single calls measured 2-4 % slower.
 template <typename Tin, typename Ty, int RK, bool GROUPED, int CW, bool MULTI = false>
 __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
-    sgmv_stream_kernel(const __grid_constant__ StreamParams P) {
+    sgmv_stream_kernel(const __grid_constant__ StreamParamsT<MULTI ? kStreamMaxProblems : 1> P) {
     constexpr int kStreamConsumers = CW * 32, kStreamWarps = CW, kStreamThreads = CW * 32 + 32;
     // Parameters read once into registers (see sgmv_cc.cuh).
     const int T = P.T, L = P.L, H1 = P.H1, H2 = P.H2, rk = P.r;
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(CW * 32 + 32, CW == 8 ? 2 : 1)
         mbar_init(&vfull[1], 1);
         mbar_init_fence();
         s_total = 0;
-        if (MULTI) {
+        if constexpr (MULTI) {
 #pragma unroll
             for (int q = 0; q < kStreamMaxProblems; ++q) {
                 s_pp[0][q] = P.A[q];
@@ -810,7 +810,19 @@ static int stream_launch_impl(const StreamLaunch &l) {
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    void *args[] = {(void *)&l.p};
+    if (l.multi) {
+        void *args[] = {(void *)&l.p};
+        return (int)cudaLaunchKernelExC(&cfg, fn, args);
+    }
+    // one problem: the smaller parameter block of that instantiation
+    StreamParams1 p1;
+    static_cast<StreamCommon &>(p1) = static_cast<const StreamCommon &>(l.p);
+    p1.tmap_b[0] = l.p.tmap_b[0];
+    p1.y[0] = l.p.y[0];
+    p1.x[0] = l.p.x[0];
+    p1.A[0] = l.p.A[0];
+    p1.B[0] = l.p.B[0];
+    void *args[] = {(void *)&p1};
     return (int)cudaLaunchKernelExC(&cfg, fn, args);
 }
 
