@@ -575,6 +575,9 @@ def run_ours(args, rank, world, local):
         kname = "sgmv_tc_shrink_kernel + sgmv_tc_expand_kernel (tensor cores; the streaming kernel gets no short segment)"
     elif w0 is not None and w0.T <= 64:
         kname = "sgmv_stream_kernel (grouping + shrink + expand in one launch, CUDA cores)"
+    elif w0 is None and args.stack_calls == "grouped":
+        kname = ("sgmv_stream_kernel, multi-problem instantiation (per layer q+k+v, o, gate+up, "
+                 "down: 4 launches; shrink + expand on CUDA cores; grouping excluded)")
     else:
         kname = "sgmv_stream_kernel (shrink + expand, CUDA cores; grouping excluded)"
     out = {
