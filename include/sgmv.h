@@ -82,7 +82,7 @@ extern "C" {
 typedef enum {
     SGMV_OK = 0,
     SGMV_ERR_INVALID_ARG = 1,   /* NULL pointer, size out of range, bad dtype */
-    SGMV_ERR_UNSUPPORTED = 2,   /* valid but outside what this build handles */
+    SGMV_ERR_UNSUPPORTED = 2,   /* valid but outside what the library handles */
     SGMV_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned, H1/H2 % 8 != 0 */
     SGMV_ERR_BAD_INDEX = 4,     /* adapter id or perm entry out of range */
     SGMV_ERR_CUDA = 5,          /* a CUDA runtime call failed */
