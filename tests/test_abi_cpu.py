@@ -191,6 +191,7 @@ def test_apply_multi_rejects_bad_arguments(lib):
         a.update(kw)
         return lib.sgmv_apply_multi(P, y, a["y_dt"], x, A, B, a["in_dt"], 1.0, None, A16, A16, 1,
                                     None, a["T"], a["L"], a["H1"], a["H2"], a["r"], None)
+    assert call(T=0) == 0               # nothing to do: returns before any CUDA call
     assert call(P=0) == 1
     assert call(P=5) == 1               # at most four problems
     assert call(y=None) == 1
