@@ -305,12 +305,13 @@ def stack_launch_groups(grouped=True):
 class StackBatch:
     """All 224 projections of the llama7b-stack workload, resident on the device.
 
-    grouped (the default): a layer's projections run as a model runs them --
-    q, k and v read the same rows and are one sgmv_apply_multi launch, gate
-    and up another, o and down (which read the attention output and the
-    activation) one sgmv_apply_multi launch each: 4 update launches per
-    layer, 128 per step.  Otherwise 224 sgmv_apply calls, one per
-    projection."""
+    grouped (the default): the batch is grouped once per step
+    (sgmv_build_segments_device), then a layer's projections run as a model
+    runs them -- q, k and v read the same rows and are one sgmv_apply_multi
+    launch, gate and up another, o and down (which read the attention output
+    and the activation) one sgmv_apply_multi launch each: 4 update launches
+    per layer, 128 per step.  Otherwise 224 sgmv_apply calls, one per
+    projection, the first one grouping the batch (sgmv_apply_rows)."""
 
     def __init__(self, seed, dev, sgmv, grouped=True):
         import torch
@@ -347,9 +348,16 @@ class StackBatch:
 
     def apply(self, sgmv):
         """One decode step over all 224 projections, as a serving loop runs it:
-        the first projection's call groups the batch (sgmv_apply_rows writes
-        the grouping out); every launch after it reuses the grouping.
-        Returns the kernels launched."""
+        the batch is grouped once, and every update launch after it reuses
+        the grouping (grouped: sgmv_build_segments_device, then the 128
+        launches; else the first projection's sgmv_apply_rows writes the
+        grouping out).  Returns the kernels launched."""
+        if self.grouped:
+            sgmv.sgmv_build_segments_device(self.ra, self.L, out=self.meta)
+            n = sgmv.sgmv_last_launch_count()
+            for layer, g in self.launches:
+                n += self.run_group(sgmv, layer, g)
+            return n
         X, A, B, Y = self.projs[0]
         sgmv.sgmv_apply_rows(Y, X, A, B, self.ra, 1.0, out=self.meta)
         n = sgmv.sgmv_last_launch_count()
