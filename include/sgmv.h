@@ -287,7 +287,8 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
  * injected into the model's linear layers, e.g. each layer's attention q
  * projection; §2.2 for the operation).  y[k] += scale * (x[k] . A[k][idx]) . B[k][idx], every
  * argument otherwise as for sgmv_apply (host arrays of P device pointers for
- * y, x, A, B; x[k] may all be the same pointer).  The P problems run as one
+ * y, x, A, B; x[k] may all be the same pointer, the y[k] must not overlap
+ * one another: the problems' updates run at the same time).  The P problems run as one
  * launch of the streaming CUDA-core kernel when r <= 64, r % 4 == 0 and the
  * batch is large enough for one-CTA clusters (T > 76 on 152 SMs; each CTA
  * walks several (problem, tile) units), with each row's arithmetic exactly
