@@ -116,3 +116,13 @@ def test_rank_above_the_streaming_kernel():
     ra = torch.randint(0, 6, (40,), generator=g, dtype=torch.int32)
     ws = problems(2, 40, 6, 256, 264, 128, ra, torch.float16, torch.float32, 500)
     run_case(ws, host_meta=True, expect_launches=2)
+
+
+@pytest.mark.parametrize("r,y_dtype", [(12, torch.float32), (64, torch.bfloat16)])
+def test_ranks_of_the_multi_problem_instantiation(r, y_dtype):
+    # r = 12 runs the rank-16 instantiation with masked columns, r = 64 the
+    # rank-64 one; 128 rows on 40 adapters (one-CTA clusters)
+    g = torch.Generator().manual_seed(r)
+    ra = torch.randint(0, 40, (128,), generator=g, dtype=torch.int32)
+    ws = problems(2, 128, 40, 2048, 1032, r, ra, torch.bfloat16, y_dtype, 600 + r)
+    run_case(ws, host_meta=True, expect_launches=1)

@@ -64,3 +64,41 @@ def test_injected_timeout_is_reported_and_the_context_stays_usable(name, T):
     y2 = _run(w, False)
     check_error_word(0)
     assert_close(y2, oracle_apply_rows(w)[0], f"{name}: the call after the reported timeout")
+
+
+def test_injected_timeout_in_a_multi_problem_launch():
+    """Three problems on 100 rows in one launch of the multi-problem
+    instantiation: the injected timeout is reported, no y is written, and the
+    next launch is correct."""
+    import oracle
+    from rank_gemv_gb300 import sgmv
+
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(7)
+    ids = torch.randint(0, 12, (100,), generator=g, dtype=torch.int32)
+    ws = [wl.draw(100, 12, 1024, 520, 16, ids, seed=70 + k, y0="randn") for k in range(3)]
+    perm, seg_ptr, idx, _ = sgmv.sgmv_build_segments_device(ids.to(dev), 12)
+    S = sgmv.sgmv_max_segments(100, 12)
+    args = ([w.X.to(dev) for w in ws], [w.A.to(dev) for w in ws], [w.B.to(dev) for w in ws])
+
+    def run(inject):
+        ys = [w.Y0.to(dev) for w in ws]
+        sgmv.sgmv_debug_inject_wait_timeout(inject)
+        try:
+            sgmv.sgmv_apply_multi(ys, *args, seg_ptr, idx, 1.0, perm=perm, S=S)
+            assert sgmv.load_library().sgmv_last_launch_count() == 1
+        finally:
+            sgmv.sgmv_debug_inject_wait_timeout(False)
+        return ys
+
+    check_error_word(0)
+    ys = run(True)
+    assert sgmv.sgmv_get_device_error() == 7
+    for y, w in zip(ys, ws):
+        assert torch.equal(y.cpu(), w.Y0)
+    ys = run(False)
+    check_error_word(0)
+    o_perm, o_seg, o_idx = oracle.build_segments(ids, 12)
+    for k, (y, w) in enumerate(zip(ys, ws)):
+        ref = oracle.sgmv_apply(w.Y0, w.X, w.A, w.B, o_seg, o_idx, 1.0, perm=o_perm)
+        assert_close(y, ref, f"problem {k} after the reported timeout")
