@@ -192,8 +192,9 @@ int *sgmv::device_error_word() { return error_word(); }
 // again from L2), up to 8 for longer segments, whose rows then share each
 // staged weight chunk.  The cluster size -- and with it the summation order
 // -- depends on T and the dimensions only, never on the segmentation: as
-// many CTAs per tile (8, 4, 2, 1) as keep CTAs x T within the SM count, each
-// with at least 64 columns of H1 and of H2.
+// many CTAs per tile (8, 4, 2, 1) as keep CTAs x T within the SM count (within
+// twice the SM count, at two CTAs per SM, for 39..64 rows), each with at least
+// 64 columns of H1 and of H2.
 bool sgmv::stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32_t max_len,
                         int32_t H1, int32_t H2, int32_t r, int in_dtype, int y_dtype,
                         StreamLaunch &l, bool grouped, int np) {
@@ -216,10 +217,20 @@ bool sgmv::stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32
     if (nsm <= 0) return false;
     int cl = 8;
     while (cl > 1 && ((int64_t)cl * T > nsm || H1 < cl * 64 || H2 < cl * 64)) cl >>= 1;
+    // 39..64 rows: clusters twice as large at two CTAs per SM, each CTA
+    // streaming half as much of its tile's adapter (measured on a Zipf batch
+    // of 64 rows: 7.50 against 8.85 us back to back, 14.96 against 17.04
+    // isolated).  Like the rule above, a function of T and the dimensions.
+    bool half = false;
+    if (np == 1 && 4 * (int64_t)T > nsm && T <= kGroupMaxT && cl < 8 && H1 >= 2 * cl * 64 &&
+        H2 >= 2 * cl * 64) {
+        cl *= 2;
+        half = true;
+    }
     // several problems: single-CTA clusters only (large batches), where the
     // kernel has an instantiation for them
     if (np > 1 && cl != 1) return false;
-    const int64_t gmax = std::max(1, nsm / cl);
+    const int64_t gmax = std::max<int64_t>(1, (half ? 2 : 1) * (int64_t)nsm / cl);
     if (ceil_div((int64_t)T * np, gmax) > kStreamMaxTiles) return false;
     StreamParams &p = l.p;
     const int rk = r <= 16 ? 16 : r <= 32 ? 32 : 64;
@@ -258,7 +269,9 @@ bool sgmv::stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32
     // early.  A CTA with many chunks, or with large stages, takes a whole SM
     // for a deeper ring: more bytes in flight per SM.
     int64_t nst = (int64_t)(kStreamSmemBudget - fixed) / p.stage_bytes;
-    if (nst < 3 || chunks > 2 * nst) nst = (int64_t)(kStreamSmemMax - fixed) / p.stage_bytes;
+    if (!half && (nst < 3 || chunks > 2 * nst))
+        nst = (int64_t)(kStreamSmemMax - fixed) / p.stage_bytes;
+    if (half && nst < 2) return false;  // two CTAs per SM need two stages each (r <= 64 has them)
     nst = std::min<int64_t>(std::min<int64_t>(nst, kStreamMaxStages), chunks);
     if (nst < 1) return false;
     p.nst = (int32_t)nst;

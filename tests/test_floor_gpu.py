@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("name,ctas,cluster", [("decode-distinct", 128, 4),
-                                               ("decode-zipf", 128, 2),
+                                               ("decode-zipf", 256, 4),
                                                ("llama7b-q", 128, 1), ("tiny", 64, 8)])
 def test_read_floor_runs_with_the_streaming_shape(name, ctas, cluster):
     from rank_gemv_gb300 import sgmv
