@@ -296,7 +296,9 @@ int sgmv_fused_linear_lora(void *y, int y_dtype, const void *x, const void *W, c
  * otherwise it makes those P calls.  P = 1 is allowed: a serving loop that
  * sends all its calls here runs a single kernel.
  * No workspace, nothing allocated.  Errors: SGMV_ERR_INVALID_ARG for P out
- * of range or null arrays or pointers, then as sgmv_apply.
+ * of range or null arrays or pointers, then as sgmv_apply; when the problems
+ * run as P calls and call k fails, problems 0 .. k-1 are already queued on
+ * `stream` and k .. P-1 are not.
  */
 int sgmv_apply_multi(int32_t P, void *const *y, int y_dtype, const void *const *x,
                      const void *const *A, const void *const *B, int in_dtype, float scale,
