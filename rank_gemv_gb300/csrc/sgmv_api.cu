@@ -201,14 +201,14 @@ bool sgmv::stream_shape(int32_t T, int32_t S, const int32_t *seg_ptr_host, int32
     if (r % 4 != 0 || r > 64 || T <= 0 || S <= 0) return false;
     if (np < 1 || np > kStreamMaxProblems || (grouped && np != 1)) return false;
     const int64_t avg = ceil_div(T, S);
-    // The one-launch grouped form cannot see the segments.  Above 32 rows its
-    // clusters have at most two CTAs, each streaming large slices of a tile's
-    // adapter, and tiles of two rows halve that streaming for repeated
-    // adapters (measured on a Zipf batch of 64 rows: 9.1 against 10.3 us;
-    // all-distinct rows unchanged; taller tiles leave a few CTAs
-    // compute-bound).  Up to 32 rows, one-row tiles measured faster (one
-    // shared adapter, 32 rows: 4.0 against 4.4 us).  Tile height does not
-    // change any row's summation order.
+    // The one-launch grouped form cannot see the segments.  Above 32 rows
+    // tiles of two rows halve the streaming of repeated adapters (measured on
+    // a Zipf batch of 64 rows in clusters of four at two CTAs per SM, us per
+    // call back to back: 7.46 with two-row tiles, 8.03 with one, 9.21 with
+    // four, 12.55 with eight: taller tiles leave a few CTAs compute-bound).
+    // Up to 32 rows, one-row tiles measured faster (one shared adapter, 32
+    // rows: 4.0 against 4.4 us).  Tile height does not change any row's
+    // summation order.
     const int trows = grouped && T > 32 ? 2 : avg <= 2 ? 1 : avg <= 4 ? 2 : avg <= 8 ? 4 : 8;
     // units: (problem, tile) pairs
     const int64_t slots = tile_slots(T, S, seg_ptr_host, trows, 1, max_len) * np;
