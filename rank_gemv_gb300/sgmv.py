@@ -99,6 +99,10 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+# pointer-array types for the multi-problem entry (P = 1 .. 4)
+_PTR_ARRAYS = [None] + [ctypes.c_void_p * n for n in range(1, 5)]
+
+
 def _stream(device):
     return torch.cuda.current_stream(device).cuda_stream
 
@@ -220,26 +224,26 @@ def sgmv_apply_multi(ys, xs, As, Bs, seg_ptr, idx, scale=1.0, perm=None, seg_ptr
     @ As[k][idx[s]]) @ Bs[k][idx[s]], in place, in one launch when the kernel
     allows (the same bits as separate calls); returns ys."""
     P = len(ys)
-    if not (len(xs) == len(As) == len(Bs) == P):
-        raise ValueError("ys, xs, As and Bs differ in length")
-    T, H1 = xs[0].shape
+    if not (len(xs) == len(As) == len(Bs) == P) or P < 1:
+        raise ValueError("ys, xs, As and Bs must hold the same number (>= 1) of tensors")
+    x0, y0 = xs[0], ys[0]
+    T, H1 = x0.shape
     L, _, r = As[0].shape
-    H2 = ys[0].shape[1]
+    H2 = y0.shape[1]
+    xshape, ashape, bshape, yshape = (T, H1), (L, H1, r), (L, r, H2), (T, H2)
+    tin, ty = x0.dtype, y0.dtype
     for y, x, A, B in zip(ys, xs, As, Bs):
-        if (tuple(x.shape) != (T, H1) or tuple(A.shape) != (L, H1, r)
-                or tuple(B.shape) != (L, r, H2) or tuple(y.shape) != (T, H2)):
+        if x.shape != xshape or A.shape != ashape or B.shape != bshape or y.shape != yshape:
             raise ValueError("the problems' shapes differ")
-        if x.dtype != xs[0].dtype or A.dtype != x.dtype or B.dtype != x.dtype or y.dtype != ys[0].dtype:
+        if x.dtype != tin or A.dtype != tin or B.dtype != tin or y.dtype != ty:
             raise TypeError("the problems' types differ")
-    sph = _host_i32(seg_ptr_host)
-
-    def arr(ts):
-        return (ctypes.c_void_p * max(1, P))(*[_ptr(t) for t in ts])
+    arr = _PTR_ARRAYS[P] if P < len(_PTR_ARRAYS) else ctypes.c_void_p * P
     _check(load_library().sgmv_apply_multi(
-        P, arr(ys), _DTYPES[ys[0].dtype], arr(xs), arr(As), arr(Bs), _DTYPES[xs[0].dtype],
+        P, arr(*[t.data_ptr() for t in ys]), _DTYPES[ty], arr(*[t.data_ptr() for t in xs]),
+        arr(*[t.data_ptr() for t in As]), arr(*[t.data_ptr() for t in Bs]), _DTYPES[tin],
         float(scale), _ptr(_meta(perm, "perm")), _ptr(_meta(seg_ptr, "seg_ptr")),
-        _ptr(_meta(idx, "idx")), _nseg(idx, S), _ptr(sph), T, L, H1, H2, r,
-        _stream(xs[0].device)), "sgmv_apply_multi")
+        _ptr(_meta(idx, "idx")), _nseg(idx, S), _ptr(_host_i32(seg_ptr_host)), T, L, H1, H2, r,
+        _stream(x0.device)), "sgmv_apply_multi")
     return ys
 
 

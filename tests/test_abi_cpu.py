@@ -279,3 +279,48 @@ def test_fused_linear_lora_rejects_bad_arguments(lib):
     assert f(100, 11008, 32) == 100 * 32 * 4 + 1024 + 100 * 2048 + part(100, 11008)
     assert f(7, 200, 64) == 7 * 64 * 4 + 256 + 7 * 4096 + part(7, 200)
     assert f(0, 4096, 16) == 0
+
+
+def test_multi_binding_marshals_each_problems_pointers(monkeypatch):
+    """The Python side of sgmv_apply_multi: the arrays it hands the C ABI hold
+    each problem's data pointers in order, and mismatched problems are
+    refused before the library is called."""
+    import torch
+
+    from rank_gemv_gb300 import sgmv
+
+    calls = []
+
+    class Recorder:
+        def sgmv_apply_multi(self, *args):
+            calls.append(args)
+            return 0
+
+    monkeypatch.setattr(sgmv, "load_library", lambda: Recorder())
+    monkeypatch.setattr(sgmv, "_stream", lambda device: None)
+    T, H1, H2, L, r = 6, 32, 48, 3, 8
+    P = 3
+    xs = [torch.zeros(T, H1, dtype=torch.half) for _ in range(P)]
+    As = [torch.zeros(L, H1, r, dtype=torch.half) for _ in range(P)]
+    Bs = [torch.zeros(L, r, H2, dtype=torch.half) for _ in range(P)]
+    ys = [torch.zeros(T, H2, dtype=torch.float32) for _ in range(P)]
+    seg = torch.tensor([0, 2, 6], dtype=torch.int32)
+    idx = torch.tensor([2, 0], dtype=torch.int32)
+    sgmv.sgmv_apply_multi(ys, xs, As, Bs, seg, idx, 0.5, seg_ptr_host=seg)
+    (a,) = calls
+    assert a[0] == P
+    for arr, ts in ((a[1], ys), (a[3], xs), (a[4], As), (a[5], Bs)):
+        assert [arr[k] for k in range(P)] == [t.data_ptr() for t in ts]
+    assert a[2] == sgmv.SGMV_F32 and a[6] == sgmv.SGMV_F16
+    assert a[7] == 0.5 and a[8] is None and a[9] == seg.data_ptr() and a[10] == idx.data_ptr()
+    assert a[11] == 2 and a[13:18] == (T, L, H1, H2, r)
+    with pytest.raises(ValueError):
+        sgmv.sgmv_apply_multi(ys, xs[:2], As, Bs, seg, idx)
+    with pytest.raises(ValueError):
+        sgmv.sgmv_apply_multi([], [], [], [], seg, idx)
+    with pytest.raises(ValueError):
+        sgmv.sgmv_apply_multi(ys, xs[:2] + [torch.zeros(T, H1 + 8, dtype=torch.half)], As, Bs,
+                              seg, idx)
+    with pytest.raises(TypeError):
+        sgmv.sgmv_apply_multi(ys, xs, As[:2] + [As[2].bfloat16()], Bs, seg, idx)
+    assert len(calls) == 1
