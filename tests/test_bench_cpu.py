@@ -1,4 +1,5 @@
-"""Host helpers of bench.py that need no GPU.
+"""Host helpers of bench.py that need no GPU, and its reference arm (the
+oracle on the host cores), which runs end to end here.
 
 The end-to-end measurement moves a step's x, y and row -> adapter ids in one
 copy: they live in one byte buffer as views at 256-byte-aligned offsets (the
@@ -86,3 +87,27 @@ def test_stack_launch_groups_cover_every_projection_once(grouped):
         if len(g) > 1:
             assert any(set(g) <= s for s in same_rows)
             assert len({wl.LLAMA7B_PROJ[k][1:] for k in g}) == 1
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the arm's keys, the same metric and unit as the GPU arm,
+    and an end-to-end figure that copies nothing."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    out = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "3", "--warmup", "3", "--workload", "tiny"],
+                         capture_output=True, text=True, timeout=600, check=True).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
+    assert d["metric"] == bench.METRIC and d["unit"] == "rows/s" and d["higher_is_better"]
+    assert d["value"] > 0 and d["config"]["workload"] == "tiny"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
