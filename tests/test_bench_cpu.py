@@ -111,3 +111,18 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under a two-rank launch only rank 0 runs the oracle and prints; rank 1
+    exits at once with status 0 and prints nothing."""
+    import os
+    import subprocess
+    import sys
+
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
+    res = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl",
+                          "reference", "--steps", "3", "--warmup", "3", "--workload", "tiny"],
+                         capture_output=True, text=True, timeout=600, env=env)
+    assert res.returncode == 0
+    assert not [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
