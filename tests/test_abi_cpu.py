@@ -324,3 +324,11 @@ def test_multi_binding_marshals_each_problems_pointers(monkeypatch):
     with pytest.raises(TypeError):
         sgmv.sgmv_apply_multi(ys, xs, As[:2] + [As[2].bfloat16()], Bs, seg, idx)
     assert len(calls) == 1
+
+
+def test_a_missing_library_fails_loudly(tmp_path):
+    """No CPU fallback: without the built library every entry point raises."""
+    from rank_gemv_gb300 import sgmv
+
+    with pytest.raises(RuntimeError, match="is not built"):
+        sgmv.load_library(tmp_path / "libsgmv.so")
